@@ -1,0 +1,179 @@
+"""GB300 (sm_103a) prefill of the clef-flash hybrid decoder: thin Python binding of libclef.so.
+
+Every function here only marshals arguments into the C ABI declared in include/clef.h; all of the
+computation runs in the library's CUDA kernels.  PyTorch is used for device memory and streams.
+There is no fallback: if libclef.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libclef.so")
+
+HIDDEN = 4096
+INTER = 12288
+GDN_HK, GDN_HV, GDN_D = 16, 32, 128
+ATT_HQ, ATT_HKV, ATT_D = 16, 4, 256
+MAX_LEN = 16384
+SWIGLU_BLOCK = 128
+
+STATUS_NAMES = {
+    0: "CLEF_OK", 1: "CLEF_E_INVALID", 2: "CLEF_E_SHAPE", 3: "CLEF_E_TOO_LONG", 4: "CLEF_E_ALIGN",
+    5: "CLEF_E_CUDA", 6: "CLEF_E_DEVICE_TIMEOUT", 7: "CLEF_E_NONFINITE", 8: "CLEF_E_WORKSPACE",
+    9: "CLEF_E_BAD_TOKEN",
+}
+
+
+class ClefError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}: {msg}")
+
+
+class Lut6(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("lut", ctypes.c_void_p)]
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int32),
+        ("attn_norm", ctypes.c_void_p),
+        ("mlp_norm", ctypes.c_void_p),
+        ("in_proj", Lut6),
+        ("out_proj", Lut6),
+        ("gate_up", Lut6),
+        ("down", Lut6),
+        ("ab_w", ctypes.c_void_p),
+        ("A_log", ctypes.c_void_p),
+        ("dt_bias", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p),
+        ("o_norm", ctypes.c_void_p),
+    ]
+
+
+class Model(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("layers", ctypes.POINTER(Layer)),
+        ("embed", ctypes.c_void_p),
+        ("vocab", ctypes.c_int64),
+        ("final_norm", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+_SIGS = {
+    "clef_last_error": (ctypes.c_char_p, []),
+    "clef_version": (ctypes.c_int32, []),
+    "clef_debug_fail_next": (None, [ctypes.c_int32]),
+    "clef_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "clef_lut6_pack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "clef_lut6_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "clef_lut6_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "clef_lut6_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_void_p]),
+    "clef_gdn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "clef_gdn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int64, ctypes.c_int64,
+                                                                  ctypes.c_void_p, ctypes.c_size_t,
+                                                                  ctypes.c_void_p]),
+    "clef_gqa_attn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]),
+    "clef_prefill_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "clef_prefill_forward": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_size_t, ctypes.c_void_p]),
+    "clef_decoder_layer": (ctypes.c_int, [ctypes.POINTER(Layer), ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
+                                          ctypes.c_void_p]),
+}
+
+
+def lib():
+    """The loaded libclef.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name, None)
+            if fn is None:
+                continue
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise ClefError(code, where, lib().clef_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("expected contiguous CUDA tensors")
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise if a kernel reported a device-side problem."""
+    _check(lib().clef_sync_status(_stream(stream)), "clef_sync_status")
+
+
+# ------------------------------------------------------------------------------------- LUT-6
+def lut6_pack(idx):
+    """Host: pack uint8 indices [n, k] (numpy or CPU tensor) into [n, k*3/4] bytes."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(idx, dtype=np.uint8))
+    n, k = a.shape
+    out = np.empty((n, k * 3 // 4), dtype=np.uint8)
+    _check(lib().clef_lut6_pack(a.ctypes.data, n, k, out.ctypes.data), "clef_lut6_pack")
+    return out
+
+
+def lut6_unpack(packed, k):
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(packed, dtype=np.uint8))
+    n = a.shape[0]
+    out = np.empty((n, k), dtype=np.uint8)
+    _check(lib().clef_lut6_unpack(a.ctypes.data, n, k, out.ctypes.data), "clef_lut6_unpack")
+    return out
+
+
+def lut6_dequant(packed, lut, k, stream=None):
+    """Device: dense fp16 W [n, k] from a LUT-6 weight."""
+    _need_cuda(packed, lut)
+    n = lut.shape[0] * 16
+    w = torch.empty((n, k), dtype=torch.float16, device=packed.device)
+    _check(lib().clef_lut6_dequant(_ptr(packed), _ptr(lut), n, k, _ptr(w), _stream(stream)),
+           "clef_lut6_dequant")
+    return w
+
+
+def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None):
+    """Device: y = x . W^T for fp16 x [m, k] and LUT-6 W [n, k]; y fp16 (or fp32) [m, n]."""
+    _need_cuda(x, packed, lut)
+    m, k = x.shape
+    n = lut.shape[0] * 16
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32 if out_fp32 else torch.float16, device=x.device)
+    _check(lib().clef_lut6_gemm(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out), 1 if out_fp32 else 0,
+                                m, n, k, _stream(stream)), "clef_lut6_gemm")
+    return out

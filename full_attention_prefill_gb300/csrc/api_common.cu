@@ -1,0 +1,235 @@
+// Library plumbing behind the C ABI: error messages, the device status word, TMA descriptor
+// encoding, the host-side fault hook, and the LUT-6 entry points.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "lut6.cuh"
+
+namespace clef {
+
+static thread_local char g_err[512] = "";
+
+const char* set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return g_err;
+}
+
+// The device status word: one per device that loads the library (a module-scope variable).
+__device__ unsigned g_status_word = 0;
+
+unsigned* status_word_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static unsigned* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+cudaError_t tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                          uint32_t box_outer, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_error("cuTensorMapEncodeTiled is not available from the driver");
+    return cudaErrorNotSupported;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, stride %llu, box %u x %u", (int)r,
+              (unsigned long long)inner, (unsigned long long)outer,
+              (unsigned long long)row_stride_bytes, box_inner, box_outer);
+    return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+// host-side fault hook (tests of error paths without any GPU fault)
+static int g_fail_next = 0;
+static std::mutex g_fail_mu;
+bool debug_should_fail() {
+  std::lock_guard<std::mutex> lock(g_fail_mu);
+  if (g_fail_next > 0) {
+    --g_fail_next;
+    set_error("failure injected by clef_debug_fail_next");
+    return true;
+  }
+  return false;
+}
+
+}  // namespace clef
+
+using namespace clef;
+
+static inline bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+extern "C" {
+
+const char* clef_last_error(void) { return g_err; }
+
+int32_t clef_version(void) { return (1 << 16) | 0; }
+
+void clef_debug_fail_next(int32_t n_calls) {
+  std::lock_guard<std::mutex> lock(g_fail_mu);
+  g_fail_next = n_calls > 0 ? n_calls : 0;
+}
+
+clef_status clef_sync_status(clef_stream stream) {
+  CLEF_CUDA_CHECK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  unsigned* p = status_word_ptr();
+  if (!p) {
+    set_error("cannot resolve the device status word");
+    return CLEF_E_CUDA;
+  }
+  unsigned v = 0, zero = 0;
+  CLEF_CUDA_CHECK(cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost));
+  CLEF_CUDA_CHECK(cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  if (v == DEV_OK) return CLEF_OK;
+  if (v == DEV_BAD_TOKEN) {
+    set_error("a token id was outside [0, vocab)");
+    return CLEF_E_BAD_TOKEN;
+  }
+  set_error("a device wait ran out (code 0x%x)", v);
+  return CLEF_E_DEVICE_TIMEOUT;
+}
+
+clef_status clef_lut6_pack(const uint8_t* idx, int64_t n, int64_t k, uint8_t* packed) {
+  if (!idx || !packed || n < 0 || k < 0) {
+    set_error("clef_lut6_pack: NULL pointer or negative size");
+    return CLEF_E_INVALID;
+  }
+  if (k % 4) {
+    set_error("clef_lut6_pack: k = %lld is not a multiple of 4", (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  const int64_t quads = n * (k / 4);
+  for (int64_t q = 0; q < quads; ++q) {
+    const uint8_t* i = idx + 4 * q;
+    if ((i[0] | i[1] | i[2] | i[3]) & 0xC0) {
+      set_error("clef_lut6_pack: index >= 64 at quadruple %lld", (long long)q);
+      return CLEF_E_INVALID;
+    }
+    const uint32_t w = (uint32_t)i[0] | ((uint32_t)i[1] << 6) | ((uint32_t)i[2] << 12) |
+                       ((uint32_t)i[3] << 18);
+    packed[3 * q + 0] = (uint8_t)(w & 0xFFu);
+    packed[3 * q + 1] = (uint8_t)((w >> 8) & 0xFFu);
+    packed[3 * q + 2] = (uint8_t)((w >> 16) & 0xFFu);
+  }
+  return CLEF_OK;
+}
+
+clef_status clef_lut6_unpack(const uint8_t* packed, int64_t n, int64_t k, uint8_t* idx) {
+  if (!idx || !packed || n < 0 || k < 0) {
+    set_error("clef_lut6_unpack: NULL pointer or negative size");
+    return CLEF_E_INVALID;
+  }
+  if (k % 4) {
+    set_error("clef_lut6_unpack: k = %lld is not a multiple of 4", (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  const int64_t quads = n * (k / 4);
+  for (int64_t q = 0; q < quads; ++q) {
+    const uint32_t w = (uint32_t)packed[3 * q] | ((uint32_t)packed[3 * q + 1] << 8) |
+                       ((uint32_t)packed[3 * q + 2] << 16);
+    for (int j = 0; j < 4; ++j) idx[4 * q + j] = (uint8_t)((w >> (6 * j)) & 63u);
+  }
+  return CLEF_OK;
+}
+
+clef_status clef_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_t n, int64_t k,
+                              uint16_t* w, clef_stream stream) {
+  if (!packed || !lut || !w || n < 0 || k < 0) {
+    set_error("clef_lut6_dequant: NULL pointer or negative size");
+    return CLEF_E_INVALID;
+  }
+  if (n % 16 || k % 4) {
+    set_error("clef_lut6_dequant: need n %% 16 == 0 and k %% 4 == 0 (n=%lld k=%lld)", (long long)n,
+              (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  if (misaligned(lut) || misaligned(w)) {
+    set_error("clef_lut6_dequant: device pointers must be 16-byte aligned");
+    return CLEF_E_ALIGN;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  return lut6_dequant_launch(packed, reinterpret_cast<const __half*>(lut), n, k,
+                             reinterpret_cast<__half*>(w), static_cast<cudaStream_t>(stream));
+}
+
+clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,
+                           int32_t y_is_fp32, int64_t m, int64_t n, int64_t k, clef_stream stream) {
+  if (m < 0 || n <= 0 || k <= 0 || (y_is_fp32 != 0 && y_is_fp32 != 1)) {
+    set_error("clef_lut6_gemm: bad size or bad y_is_fp32");
+    return CLEF_E_INVALID;
+  }
+  if (m == 0) return CLEF_OK;  /* nothing to compute; x and y may be NULL */
+  if (!x || !packed || !lut || !y) {
+    set_error("clef_lut6_gemm: NULL pointer");
+    return CLEF_E_INVALID;
+  }
+  if (n % 16 || k % 64) {
+    set_error("clef_lut6_gemm: need n %% 16 == 0 and k %% 64 == 0 (n=%lld k=%lld)", (long long)n,
+              (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  if (m > (int64_t)INT32_MAX / 2 || n > (1 << 24) || k > (1 << 20)) {
+    set_error("clef_lut6_gemm: size out of the supported range");
+    return CLEF_E_SHAPE;
+  }
+  if (misaligned(x) || misaligned(packed) || misaligned(lut) || misaligned(y)) {
+    set_error("clef_lut6_gemm: device pointers must be 16-byte aligned");
+    return CLEF_E_ALIGN;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  return lut6_gemm_launch(reinterpret_cast<const __half*>(x), packed,
+                          reinterpret_cast<const __half*>(lut), y, n, m, n, k,
+                          y_is_fp32 ? EPI_F32 : EPI_F16, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

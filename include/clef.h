@@ -1,0 +1,215 @@
+/*
+ * clef.h - C ABI of the GB300 (sm_103a) prefill library for the clef-flash hybrid decoder.
+ *
+ * The model: the clef-flash text backbone ("Clef-Flash-ANE-LUT6" model card, section "Model
+ * architecture"): 32 layers of hidden size 4,096 and MLP size 12,288; 24 Gated DeltaNet layers
+ * (16 key / 32 value heads of 128) and 8 gated full-attention layers (16 query / 4 kv heads of
+ * 256), full attention every fourth layer.  Every large linear is LUT-6 (section "LUT-6 text
+ * weights"): 6-bit indices, one 64-entry FP16 table per 16 output channels, four indices in
+ * three bytes.  One call of clef_prefill_forward is one single prefill: token ids in, the
+ * final-norm hidden state at every position out ("clef-flash-LiteRT" README, section "Host
+ * contract", steps 3-6; no state carries over between calls).
+ *
+ * Conventions of every entry point:
+ *   - All buffers are owned by the caller.  The library never allocates device memory; calls
+ *     that need scratch take a caller-provided workspace (see the *_workspace_size queries).
+ *   - "device" pointers point to memory of the current CUDA device; "host" pointers to host
+ *     memory.  fp16 tensors are passed as uint16_t bit patterns (IEEE binary16).
+ *   - Tensors are dense and row-major, last index fastest, with the shapes given per call.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Arguments are validated on the host before anything is launched; on a validation error
+ *     nothing is launched and the call returns the error.
+ *   - Device pointers must be 16-byte aligned (CLEF_E_ALIGN otherwise).
+ *   - Kernels never trap.  A device-side problem (a wait that ran out, a token id outside the
+ *     vocabulary) is written to a device status word that clef_sync_status() reads.
+ *   - Error messages: clef_last_error() returns the message of the last failing call on the
+ *     calling thread.
+ *   - Calls are reentrant given distinct output buffers and workspaces.
+ */
+#ifndef CLEF_H_
+#define CLEF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CLEF_API __attribute__((visibility("default")))
+#else
+#define CLEF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CLEF_OK = 0,
+  CLEF_E_INVALID = 1,          /* NULL pointer, negative size, bad enum, index out of range  */
+  CLEF_E_SHAPE = 2,            /* a size the call does not support (see each call)           */
+  CLEF_E_TOO_LONG = 3,         /* more than CLEF_MAX_LEN positions: refused, never cut       */
+  CLEF_E_ALIGN = 4,            /* a device pointer not 16-byte aligned                       */
+  CLEF_E_CUDA = 5,             /* a CUDA runtime/driver call failed                          */
+  CLEF_E_DEVICE_TIMEOUT = 6,   /* a device wait ran out (from clef_sync_status)              */
+  CLEF_E_NONFINITE = 7,        /* reserved                                                   */
+  CLEF_E_WORKSPACE = 8,        /* workspace smaller than the size query returned             */
+  CLEF_E_BAD_TOKEN = 9         /* a token id outside [0, vocab) (from clef_sync_status)      */
+} clef_status;
+
+/* Model constants (clef-flash text backbone). */
+#define CLEF_HIDDEN 4096
+#define CLEF_INTER 12288
+#define CLEF_GDN_HK 16
+#define CLEF_GDN_HV 32
+#define CLEF_GDN_D 128
+#define CLEF_ATT_HQ 16
+#define CLEF_ATT_HKV 4
+#define CLEF_ATT_D 256
+#define CLEF_ROPE_DIMS 64
+/* Longest prefill the provider's code reads ("clef-flash-LiteRT" README, section "Limits"). */
+#define CLEF_MAX_LEN 16384
+/* Rows per block in the interleaved gate/up weight of the SwiGLU MLP (see clef_layer). */
+#define CLEF_SWIGLU_BLOCK 128
+
+typedef void* clef_stream; /* a cudaStream_t */
+
+/* Message of the last failing call on this thread ("" if none). */
+CLEF_API const char* clef_last_error(void);
+
+/* ABI version: (major << 16) | minor. */
+CLEF_API int32_t clef_version(void);
+
+/* ------------------------------------------------------------------------------------------
+ * LUT-6 format ("Clef-Flash-ANE-LUT6" model card, sections "Weight precision" and "LUT-6 text
+ * weights").  A weight matrix W [n, k] (n output channels, k inputs) is stored as
+ *   packed [n, k*3/4] uint8: the 6-bit indices idx[n][k] as one LSB-first bit stream in
+ *          row-major order (k fastest); indices i0..i3 of a quadruple form the 24-bit word
+ *          i0 | i1<<6 | i2<<12 | i3<<18, stored as its three little-endian bytes;
+ *   lut    [n/16, 64] fp16: table g serves output rows 16g .. 16g+15;
+ *   W[r][c] = lut[r/16][idx[r][c]].
+ * ------------------------------------------------------------------------------------------ */
+
+/* host: pack idx [n, k] (each < 64; k % 4 == 0) into packed [n, k*3/4].  Host buffers, caller
+   owned.  CLEF_E_INVALID for an index >= 64 or a NULL pointer, CLEF_E_SHAPE if k % 4 != 0. */
+CLEF_API clef_status clef_lut6_pack(const uint8_t* idx, int64_t n, int64_t k, uint8_t* packed);
+
+/* host: the inverse of clef_lut6_pack. */
+CLEF_API clef_status clef_lut6_unpack(const uint8_t* packed, int64_t n, int64_t k, uint8_t* idx);
+
+/* device: w [n, k] fp16 = the dequantised LUT-6 weight (bit-exact table values).  n % 16 == 0,
+   k % 4 == 0.  A debugging / parity aid; the GEMM never materialises W. */
+CLEF_API clef_status clef_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_t n, int64_t k,
+                              uint16_t* w, clef_stream stream);
+
+/* device: y [m, n] = x [m, k] . W^T, fp32 accumulation; y is fp16 (y_is_fp32 = 0) or fp32
+   (y_is_fp32 = 1).  The LUT-6 weight is dequantised in shared memory and fed to tcgen05
+   tensor-core MMAs; W is never written to global memory.  Requirements: m >= 0 (m == 0 is a
+   no-op and x, y may then be NULL), n % 16 == 0, k % 64 == 0, k > 0 (CLEF_E_SHAPE otherwise).
+   x, packed, lut, y device,
+   16-byte aligned. */
+CLEF_API clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,
+                           int32_t y_is_fp32, int64_t m, int64_t n, int64_t k, clef_stream stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Gated DeltaNet scan ("Clef-Flash-ANE-LUT6" section "Model architecture"; "clef-flash - Core
+ * AI" README, section "Core AI shape": recurrent state [.., 32, 128, 128] per layer;
+ * "clef-flash-LiteRT" section "Provenance": the recurrence evaluated in chunks of 64 positions).
+ * For value head h (key head h/2), from S_0 (zero, or s0):
+ *     S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,   o_t = S_t q_t / sqrt(128)
+ * q, k [B, L, 16, 128] fp16 (already convolved and L2-normalised), v [B, L, 32, 128] fp16,
+ * alpha, beta [B, L, 32] fp32 with 0 <= alpha <= 1; o [B, L, 32, 128] fp16.
+ * s0 [B, 32, 128, 128] fp32 (row = value dim, column = key dim) or NULL for a zero state;
+ * s_out (same shape) receives S_L, or NULL.  L <= CLEF_MAX_LEN.  Needs a workspace of
+ * clef_gdn_workspace_size(B, L) bytes (device, 256-byte aligned).
+ * ------------------------------------------------------------------------------------------ */
+CLEF_API size_t clef_gdn_workspace_size(int64_t B, int64_t L);
+CLEF_API clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             const float* alpha, const float* beta, const float* s0, uint16_t* o,
+                             float* s_out, int64_t B, int64_t L, void* workspace,
+                             size_t workspace_bytes, clef_stream stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Causal GQA attention of a gated full-attention layer ("Clef-Flash-ANE-LUT6" section "Model
+ * architecture": 16 query and 4 kv heads of 256; "clef-flash-LiteRT" section "Host contract"
+ * step 5: rotary theta 1e7, text positions (i, i, i); "clef-flash-coreml": cos/sin [L, 64]).
+ * q [B, L, 16, 256], k, v [B, L, 4, 256] fp16, before rotary; rotary (rotate-half pairs
+ * (j, j+32), angle pos * 1e7^(-j/32)) is applied to dims 0..63 of q and k with pos = 0..L-1;
+ * query head h reads kv head h/4; P = softmax(q k^T / 16 + causal mask); o = P v.
+ * gate [B, L, 16, 256] fp16 or NULL: o <- o * sigmoid(gate).  o [B, L, 16, 256] fp16.
+ * q, k, v and gate may be row-strided: row_stride_* is the element distance between positions
+ * (e.g. 10240 when they are column slices of one projection output); 0 means packed.
+ * ------------------------------------------------------------------------------------------ */
+CLEF_API clef_status clef_gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const uint16_t* gate, uint16_t* o, int64_t B, int64_t L,
+                                  int64_t row_stride_q, int64_t row_stride_kv,
+                                  int64_t row_stride_gate, clef_stream stream);
+
+/* ------------------------------------------------------------------------------------------
+ * The model.  All pointers are device pointers except `layers` (a host array).
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  const uint8_t* packed; /* [n, k*3/4] */
+  const uint16_t* lut;   /* [n/16, 64] fp16 */
+} clef_lut6;
+
+typedef enum { CLEF_LAYER_GDN = 0, CLEF_LAYER_ATTENTION = 1 } clef_layer_kind;
+
+typedef struct {
+  int32_t kind;              /* clef_layer_kind */
+  const uint16_t* attn_norm; /* [4096] fp16 pre-mixer RMSNorm weight */
+  const uint16_t* mlp_norm;  /* [4096] fp16 pre-MLP RMSNorm weight */
+  /* GDN: rows [q 2048 | k 2048 | v 4096 | z 4096] = [12288, 4096].
+     attention: rows [query 4096 | gate 4096 | k 1024 | v 1024] = [10240, 4096]. */
+  clef_lut6 in_proj;
+  clef_lut6 out_proj;        /* [4096, 4096] */
+  /* MLP gate and up, interleaved in blocks of CLEF_SWIGLU_BLOCK rows: rows
+     [256j, 256j+128) are gate rows [128j, 128j+128), rows [256j+128, 256j+256) are up rows
+     [128j, 128j+128).  [24576, 4096]. */
+  clef_lut6 gate_up;
+  clef_lut6 down;            /* [4096, 12288] */
+  /* GDN only (NULL for attention layers), fp16: */
+  const uint16_t* ab_w;      /* [64, 4096]: rows 0..31 = a projection, 32..63 = b projection */
+  const uint16_t* A_log;     /* [32] */
+  const uint16_t* dt_bias;   /* [32] */
+  const uint16_t* conv_w;    /* [8192, 4] depthwise causal conv taps, tap 3 = current position */
+  const uint16_t* o_norm;    /* [128] z-gated RMSNorm weight, shared by the 32 heads */
+} clef_layer;
+
+typedef struct {
+  int32_t n_layers;          /* 32 for clef-flash; 1..64 accepted */
+  const clef_layer* layers;  /* host array [n_layers] */
+  const uint16_t* embed;     /* [vocab, 4096] fp16 token embeddings */
+  int64_t vocab;             /* 248320 for clef-flash */
+  const uint16_t* final_norm;/* [4096] fp16 */
+} clef_model;
+
+/* Bytes of workspace clef_prefill_forward / clef_decoder_layer need for B requests of L
+   positions. */
+CLEF_API size_t clef_prefill_workspace_size(int64_t B, int64_t L);
+
+/* device: the hybrid prefill.  ids [B, L] int32 (device) -> hidden [B, L, 4096] fp16, the hidden
+   states after the final RMSNorm at every position.  B independent requests of L positions each
+   (right-padded to a bucket by the caller: padding rows are computed like real tokens and, by
+   causality, never change the real rows).  1 <= L <= CLEF_MAX_LEN (CLEF_E_TOO_LONG above),
+   B >= 1.  Ids outside [0, vocab) set CLEF_E_BAD_TOKEN in the device status (their rows are
+   zero).  Residual stream in fp32, activations between kernels in fp16. */
+CLEF_API clef_status clef_prefill_forward(const clef_model* model, const int32_t* ids, int64_t B, int64_t L,
+                                 uint16_t* hidden, void* workspace, size_t workspace_bytes,
+                                 clef_stream stream);
+
+/* device: one decoder layer on the fp32 residual stream x [B, L, 4096], updated in place:
+   x <- h + mlp(rmsnorm(h)),  h = x + mixer(rmsnorm(x)).  Same workspace as the forward. */
+CLEF_API clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64_t B, int64_t L,
+                               void* workspace, size_t workspace_bytes, clef_stream stream);
+
+/* Wait for `stream`, then read and clear the device status word.  Returns CLEF_OK,
+   CLEF_E_DEVICE_TIMEOUT, CLEF_E_BAD_TOKEN or CLEF_E_CUDA. */
+CLEF_API clef_status clef_sync_status(clef_stream stream);
+
+/* Host-side fault hook for tests of the error paths: the next `n_calls` device entry points fail
+   with CLEF_E_CUDA before launching anything.  Affects the calling process only. */
+CLEF_API void clef_debug_fail_next(int32_t n_calls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CLEF_H_ */

@@ -1,0 +1,75 @@
+"""LUT-6 kernels against the oracle (GPU): bit-exact dequant, then the tcgen05 GEMM."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import lut6 as olut
+from tests._util import rel_rmse
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import full_attention_prefill_gb300 as clef  # noqa: E402
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("n,k", [(4096, 4096), (48, 12), (16, 64), (12288, 4096)])
+def test_dequant_bit_exact(n, k):
+    packed, lut = synth.lut6_weight(0, "dq", 0, n, k)
+    w = clef.lut6_dequant(_dev(packed), _dev(lut), k).cpu().numpy()
+    ref = olut.dequant_f16(packed, lut, n, k)
+    assert np.array_equal(w.view(np.uint16), ref.view(np.uint16))
+
+
+# (m, n, k): config-0 smoke size, ragged m, ragged n (not a multiple of the 256-row tile),
+# one k-block, several k-blocks with a ring wrap, and a tall m spanning many tiles
+CASES = [(128, 4096, 4096), (77, 256, 128), (300, 784, 320), (1, 16, 64), (129, 512, 64 * 7),
+         (1000, 1024, 1024)]
+
+
+@pytest.mark.parametrize("m,n,k", CASES)
+@pytest.mark.parametrize("fp32", [False, True])
+def test_gemm_matches_oracle(m, n, k, fp32):
+    x = synth.normal_f16(0, "x", m, (m, k))
+    packed, lut = synth.lut6_weight(0, "w", n + k, n, k)
+    y = clef.lut6_gemm(_dev(x), _dev(packed), _dev(lut), out_fp32=fp32)
+    clef.sync_status()
+    y = y.double().cpu().numpy()
+    ref = olut.linear(x, packed, lut, n)
+    rms = np.sqrt(np.mean(ref ** 2))
+    if fp32:
+        # fp16 x fp16 products are exact; the tensor core's fp32 accumulation over k terms loses
+        # about 2^-23 * sqrt(k) * rms (7.6e-6 rms at k = 4096): bound it at 1e-4 rms
+        np.testing.assert_allclose(y, ref, rtol=1e-3, atol=1e-4 * rms)
+        assert rel_rmse(y, ref) < 2e-5
+    else:
+        # plus one rounding to fp16 (unit roundoff 2^-11)
+        np.testing.assert_allclose(y, ref, rtol=1e-3, atol=1e-3 * rms)
+        assert rel_rmse(y, ref) < 1e-3
+
+
+def test_gemm_empty_m_is_noop():
+    packed, lut = synth.lut6_weight(0, "w", 1, 256, 64)
+    x = torch.empty((0, 64), dtype=torch.float16, device="cuda")
+    y = clef.lut6_gemm(x, _dev(packed), _dev(lut))
+    assert y.shape == (0, 256)
+
+
+def test_gemm_rejects_bad_shapes():
+    packed, lut = synth.lut6_weight(0, "w", 1, 256, 64)
+    x = torch.zeros((4, 60), dtype=torch.float16, device="cuda")
+    with pytest.raises(clef.ClefError) as e:
+        clef.lut6_gemm(x, _dev(packed), _dev(lut))
+    assert e.value.code == 2
+
+
+def test_gemm_deterministic():
+    x = _dev(synth.normal_f16(3, "x", 0, (512, 1024)))
+    packed, lut = synth.lut6_weight(3, "w", 0, 1024, 1024)
+    p, l = _dev(packed), _dev(lut)
+    a = clef.lut6_gemm(x, p, l)
+    b = clef.lut6_gemm(x, p, l)
+    assert torch.equal(a, b)
