@@ -83,7 +83,9 @@ _SIGS = {
     "clef_gdn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int64, ctypes.c_int64,
                                                                   ctypes.c_void_p, ctypes.c_size_t,
                                                                   ctypes.c_void_p]),
-    "clef_gqa_attn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]),
+    "clef_attn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "clef_gqa_attn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 +
+                              [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "clef_prefill_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "clef_prefill_forward": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -177,3 +179,51 @@ def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None):
     _check(lib().clef_lut6_gemm(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out), 1 if out_fp32 else 0,
                                 m, n, k, _stream(stream)), "clef_lut6_gemm")
     return out
+
+
+# --------------------------------------------------------------------------- GDN and attention
+def _workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def gdn_prefill(q, k, v, alpha, beta, s0=None, want_state=False, stream=None):
+    """Device: the gated delta rule over B requests of L positions.
+
+    q, k [B, L, 16, 128] fp16; v [B, L, 32, 128] fp16; alpha, beta [B, L, 32] fp32;
+    s0 [B, 32, 128, 128] fp32 or None.  Returns o [B, L, 32, 128] fp16 (and S_L if want_state).
+    """
+    _need_cuda(q, k, v, alpha, beta, s0)
+    B, L = q.shape[0], q.shape[1]
+    o = torch.empty((B, L, GDN_HV, GDN_D), dtype=torch.float16, device=q.device)
+    s_out = torch.empty((B, GDN_HV, GDN_D, GDN_D), dtype=torch.float32, device=q.device) if want_state else None
+    ws = _workspace(lib().clef_gdn_workspace_size(B, L), q.device)
+    _check(lib().clef_gdn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(s0), _ptr(o),
+                                  _ptr(s_out), B, L, _ptr(ws), ws.numel(), _stream(stream)),
+           "clef_gdn_prefill")
+    return (o, s_out) if want_state else o
+
+
+def gqa_attn_prefill(q, k, v, gate=None, stream=None):
+    """Device: causal GQA attention with rotary; q [B, L, 16, 256], k, v [B, L, 4, 256] fp16,
+    gate [B, L, 16, 256] fp16 or None.  Returns o [B, L, 16, 256] fp16."""
+    _need_cuda(q, k, v, gate)
+    B, L = q.shape[0], q.shape[1]
+    o = torch.empty((B, L, ATT_HQ, ATT_D), dtype=torch.float16, device=q.device)
+    ws = _workspace(lib().clef_attn_workspace_size(B, L), q.device)
+    _check(lib().clef_gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), B, L, 0, 0, 0,
+                                       _ptr(ws), ws.numel(), _stream(stream)), "clef_gqa_attn_prefill")
+    return o
+
+
+def prefill_workspace_size(B, L):
+    return int(lib().clef_prefill_workspace_size(B, L))
+
+
+def decoder_layer(layer, x, workspace=None, stream=None):
+    """Device: one decoder layer on the fp32 residual stream x [B, L, 4096], in place."""
+    _need_cuda(x)
+    B, L = x.shape[0], x.shape[1]
+    ws = workspace if workspace is not None else _workspace(prefill_workspace_size(B, L), x.device)
+    _check(lib().clef_decoder_layer(ctypes.byref(layer.struct), _ptr(x), B, L, _ptr(ws), ws.numel(),
+                                    _stream(stream)), "clef_decoder_layer")
+    return x

@@ -1,0 +1,173 @@
+// Memory-bound glue of the decoder: embedding gather, RMSNorm, and the small fp16 gate
+// projections a, b of the Gated DeltaNet layers.
+//
+// "clef-flash-LiteRT" README, "Host contract" step 4: the input rows are the embedding table's
+// rows at the request's ids; step 6: the output is the hidden state after the final RMSNorm.
+// "Clef-Flash-ANE-LUT6" model card, "Weight precision": normalisation weights and the small gate
+// projections are FP16.
+#include "common.cuh"
+#include "glue.cuh"
+#include "mma.cuh"
+
+namespace clef {
+namespace glue {
+
+constexpr int H = 4096;
+
+__global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids,
+                                                    const __half* __restrict__ table,
+                                                    int64_t vocab, float* __restrict__ x,
+                                                    unsigned* status) {
+  const int64_t tok = blockIdx.x;
+  const int32_t id = ids[tok];
+  const bool ok = id >= 0 && (int64_t)id < vocab;
+  if (!ok && threadIdx.x == 0) report(status, DEV_BAD_TOKEN);
+  const int c0 = threadIdx.x * 16;
+  float4* dst = reinterpret_cast<float4*>(x + tok * H + c0);
+  if (!ok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(table + (int64_t)id * H + c0);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint4 u = src[i];
+    const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+    const float2 a = __half22float2(h2[0]), b = __half22float2(h2[1]);
+    const float2 c = __half22float2(h2[2]), d = __half22float2(h2[3]);
+    dst[2 * i] = make_float4(a.x, a.y, b.x, b.y);
+    dst[2 * i + 1] = make_float4(c.x, c.y, d.x, d.y);
+  }
+}
+
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x,
+                                                      const __half* __restrict__ w,
+                                                      __half* __restrict__ y) {
+  __shared__ float red[8];
+  const int64_t tok = blockIdx.x;
+  const int c0 = threadIdx.x * 16;
+  const float4* src = reinterpret_cast<const float4*>(x + tok * H + c0);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = src[i];
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss += v[i] * v[i];
+#pragma unroll
+  for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += red[i];
+  const float r = rsqrtf(tot * (1.f / H) + 1e-6f);
+  const uint4* wp = reinterpret_cast<const uint4*>(w + c0);
+  uint4 out[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint4 wu = wp[i];
+    const __half2* wh = reinterpret_cast<const __half2*>(&wu);
+    uint32_t* o = reinterpret_cast<uint32_t*>(&out[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 wf = __half22float2(wh[j]);
+      o[j] = h2u(v[8 * i + 2 * j] * r * wf.x, v[8 * i + 2 * j + 1] * r * wf.y);
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(y + tok * H + c0);
+  dst[0] = out[0];
+  dst[1] = out[1];
+}
+
+// ab = xn . W_ab^T: 64 tokens x 64 outputs per CTA, k streamed in blocks of 64 (cp.async double
+// buffer), warp w owns tokens 16w..16w+15.
+constexpr int AB_T = 64, AB_K = 64, AB_LD = AB_K + 8;
+struct AbSmem {
+  __half X[2][AB_T][AB_LD];
+  __half W[2][64][AB_LD];
+};
+
+__global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__ xn,
+                                                      const __half* __restrict__ wab,
+                                                      float* __restrict__ ab, int64_t M) {
+  __shared__ __align__(16) AbSmem s;
+  const int64_t t0 = (int64_t)blockIdx.x * AB_T;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto load = [&](int buf, int kb) {
+    for (int i = tid; i < AB_T * (AB_K / 8); i += 128) {
+      const int r = i / (AB_K / 8), c8 = (i % (AB_K / 8)) * 8;
+      const bool ok = t0 + r < M;
+      cp_async16(smem_u32(&s.X[buf][r][c8]), xn + (ok ? t0 + r : 0) * H + kb * AB_K + c8, ok);
+      cp_async16(smem_u32(&s.W[buf][r][c8]), wab + (int64_t)r * H + kb * AB_K + c8, true);
+    }
+    cp_async_commit();
+  };
+  float acc[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  constexpr int NKB = H / AB_K;
+  load(0, 0);
+  for (int kb = 0; kb < NKB; ++kb) {
+    if (kb + 1 < NKB) load((kb + 1) & 1, kb + 1); else cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const uint32_t sX = smem_u32(&s.X[kb & 1][0][0]), sW = smem_u32(&s.W[kb & 1][0][0]);
+#pragma unroll
+    for (int ks = 0; ks < AB_K / 16; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(a, a_addr(sX, AB_LD, warp * 16, ks * 16, lane));
+#pragma unroll
+      for (int n = 0; n < 8; n += 2) {
+        uint32_t bq[4];
+        ldsm_x4(bq, bn_addr(sW, AB_LD, n * 8, ks * 16, lane));
+        mma16816(acc[n], a, bq[0], bq[1]);
+        mma16816(acc[n + 1], a, bq[2], bq[3]);
+      }
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int64_t tok = t0 + warp * 16 + gq + hf * 8;
+    if (tok >= M) continue;
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+      *reinterpret_cast<float2*>(ab + tok * 64 + n * 8 + 2 * tq) =
+          make_float2(acc[n][2 * hf], acc[n][2 * hf + 1]);
+  }
+}
+
+}  // namespace glue
+
+clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab, float* x,
+                         int64_t M, cudaStream_t stream) {
+  if (M == 0) return CLEF_OK;
+  glue::embed_kernel<<<(unsigned)M, 256, 0, stream>>>(ids, table, vocab, x, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
+                           cudaStream_t stream) {
+  if (M == 0) return CLEF_OK;
+  glue::rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(x, w, y);
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status ab_proj_launch(const __half* xn, const __half* w_ab, float* ab, int64_t M,
+                           cudaStream_t stream) {
+  if (M == 0) return CLEF_OK;
+  glue::ab_proj_kernel<<<(unsigned)((M + glue::AB_T - 1) / glue::AB_T), 128, 0, stream>>>(xn, w_ab,
+                                                                                         ab, M);
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+}  // namespace clef

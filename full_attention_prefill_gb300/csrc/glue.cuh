@@ -1,0 +1,20 @@
+// Internal launchers of the memory-bound glue kernels (not part of the C ABI).
+#pragma once
+#include "common.cuh"
+
+namespace clef {
+
+// x [M, 4096] fp32 = table[ids] (fp16 rows widened); ids outside [0, vocab) give zero rows and
+// set the device status to DEV_BAD_TOKEN.
+clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab, float* x,
+                         int64_t M, cudaStream_t stream);
+
+// y [M, 4096] fp16 = x * rsqrt(mean(x^2) + 1e-6) * w.
+clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
+                           cudaStream_t stream);
+
+// ab [M, 64] fp32 = xn [M, 4096] . W_ab^T, W_ab [64, 4096] fp16 (tensor cores).
+clef_status ab_proj_launch(const __half* xn, const __half* w_ab, float* ab, int64_t M,
+                           cudaStream_t stream);
+
+}  // namespace clef

@@ -1,0 +1,133 @@
+"""Device-resident clef-flash weights in the library's layout, and the prefill call.
+
+The layout is the C ABI's (include/clef.h, clef_layer / clef_model): per layer one fused input
+projection (GDN: q | k | v | z rows; attention: query | gate | k | v rows), the output
+projection, the MLP gate and up rows interleaved in blocks of 128, and the down projection, all
+LUT-6; GDN small weights fp16.  Building a layer only moves bytes (row blocks of the packed
+indices and their tables are concatenated or interleaved); no weight value changes.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import (HIDDEN, SWIGLU_BLOCK, Layer, Lut6, Model, _check, _ptr, _stream, _workspace, lib,
+               prefill_workspace_size)
+
+GDN, ATTENTION = 0, 1
+
+
+def _cat_lut6(parts):
+    packed = np.concatenate([p for p, _ in parts], axis=0)
+    lut = np.concatenate([t for _, t in parts], axis=0)
+    return packed, lut
+
+
+def interleave_gate_up(gate, up, block=SWIGLU_BLOCK):
+    """Rows [2jb, 2jb+b) = gate rows [jb, jb+b), rows [2jb+b, 2jb+2b) = up rows [jb, jb+b)."""
+    gp, gl = gate
+    upk, ul = up
+    n = gp.shape[0]
+    assert n % block == 0 and upk.shape[0] == n
+    nb = n // block
+    packed = np.stack([gp.reshape(nb, block, -1), upk.reshape(nb, block, -1)], axis=1).reshape(2 * n, -1)
+    tb = block // 16
+    lut = np.stack([gl.reshape(nb, tb, 64), ul.reshape(nb, tb, 64)], axis=1).reshape(2 * n // 16, 64)
+    return packed, lut
+
+
+class DeviceLayer:
+    """One decoder layer's weights on the device plus its clef_layer struct."""
+
+    def __init__(self, w: dict, kind: int, device="cuda"):
+        self.kind = kind
+        self._keep = []
+
+        def dev(a):
+            t = torch.from_numpy(np.ascontiguousarray(a)).to(device)
+            self._keep.append(t)
+            return t
+
+        def lut6(pair):
+            packed, lut = pair
+            return Lut6(_ptr(dev(packed)), _ptr(dev(lut)))
+
+        st = Layer()
+        st.kind = kind
+        st.attn_norm = _ptr(dev(w["attn_norm"]))
+        st.mlp_norm = _ptr(dev(w["mlp_norm"]))
+        if kind == GDN:
+            st.in_proj = lut6(_cat_lut6([w["qkv"], w["z"]]))
+            st.out_proj = lut6(w["out"])
+            st.ab_w = _ptr(dev(np.concatenate([w["a_w"], w["b_w"]], axis=0)))
+            st.A_log = _ptr(dev(w["A_log"]))
+            st.dt_bias = _ptr(dev(w["dt_bias"]))
+            st.conv_w = _ptr(dev(w["conv_w"]))
+            st.o_norm = _ptr(dev(w["o_norm"]))
+        else:
+            st.in_proj = lut6(_cat_lut6([w["q"], w["k"], w["v"]]))
+            st.out_proj = lut6(w["o"])
+        st.gate_up = lut6(interleave_gate_up(w["gate"], w["up"]))
+        st.down = lut6(w["down"])
+        self.struct = st
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in self._keep)
+
+
+class DeviceModel:
+    """The hybrid decoder on the device: layers, embedding table, final norm."""
+
+    def __init__(self, layers, embed, final_norm, device="cuda"):
+        self.layers = layers
+        if isinstance(embed, np.ndarray):
+            embed = torch.from_numpy(np.ascontiguousarray(embed)).to(device)
+        self.embed = embed
+        self.final_norm = torch.from_numpy(np.ascontiguousarray(final_norm)).to(device)
+        arr = (Layer * len(layers))(*[l.struct for l in layers])
+        self._arr = arr
+        m = Model()
+        m.n_layers = len(layers)
+        m.layers = ctypes.cast(arr, ctypes.POINTER(Layer))
+        m.embed = _ptr(self.embed)
+        m.vocab = self.embed.shape[0]
+        m.final_norm = _ptr(self.final_norm)
+        self.struct = m
+        self._ws = None
+
+    @staticmethod
+    def kind_of(layer_index: int) -> int:
+        return ATTENTION if layer_index % 4 == 3 else GDN
+
+    def workspace(self, B, L):
+        need = prefill_workspace_size(B, L)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = None
+            self._ws = _workspace(need, self.embed.device)
+        return self._ws
+
+    def forward(self, ids, out=None, stream=None):
+        """ids [B, L] int32 (device) -> final-norm hidden [B, L, 4096] fp16."""
+        if not (ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous()):
+            raise ValueError("ids must be a contiguous int32 CUDA tensor")
+        B, L = ids.shape
+        if out is None:
+            out = torch.empty((B, L, HIDDEN), dtype=torch.float16, device=ids.device)
+        ws = self.workspace(B, L)
+        _check(lib().clef_prefill_forward(ctypes.byref(self.struct), _ptr(ids), B, L, _ptr(out), _ptr(ws),
+                                          ws.numel(), _stream(stream)), "clef_prefill_forward")
+        return out
+
+
+def synth_model(seed=0, n_layers=32, device="cuda", embed=None):
+    """The synthetic model (seeded random weights, the recipe of the `synth` module)."""
+    import synth
+    layers = []
+    for l in range(n_layers):
+        kind = DeviceModel.kind_of(l)
+        layers.append(DeviceLayer(synth.layer_weights(seed, l), kind, device))
+    if embed is None:
+        embed = synth.embedding_table(seed)
+    return DeviceModel(layers, embed, synth.final_norm_weight(seed), device)

@@ -137,11 +137,14 @@ CLEF_API clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, cons
  * gate [B, L, 16, 256] fp16 or NULL: o <- o * sigmoid(gate).  o [B, L, 16, 256] fp16.
  * q, k, v and gate may be row-strided: row_stride_* is the element distance between positions
  * (e.g. 10240 when they are column slices of one projection output); 0 means packed.
+ * Needs a workspace of clef_attn_workspace_size(B, L) bytes (device; the rotated copies of q, k).
  * ------------------------------------------------------------------------------------------ */
+CLEF_API size_t clef_attn_workspace_size(int64_t B, int64_t L);
 CLEF_API clef_status clef_gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                  const uint16_t* gate, uint16_t* o, int64_t B, int64_t L,
-                                  int64_t row_stride_q, int64_t row_stride_kv,
-                                  int64_t row_stride_gate, clef_stream stream);
+                                           const uint16_t* gate, uint16_t* o, int64_t B, int64_t L,
+                                           int64_t row_stride_q, int64_t row_stride_kv,
+                                           int64_t row_stride_gate, void* workspace,
+                                           size_t workspace_bytes, clef_stream stream);
 
 /* ------------------------------------------------------------------------------------------
  * The model.  All pointers are device pointers except `layers` (a host array).
