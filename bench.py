@@ -1,0 +1,320 @@
+"""Prefill throughput of the clef-flash 32-layer hybrid decoder on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload l16384|l512|b32x512]
+                    [--impl clef|reference]
+
+A step is one full prefill (embedding gather, 24 Gated DeltaNet + 8 gated full-attention layers,
+final RMSNorm) of the workload's synthetic requests through clef_prefill_forward.  Default
+workload: one request of 16,384 positions (the longest prefill; the 32-layer L=16384 target).
+Weights are seeded random LUT-6 weights of the model's shapes; ids are uniform over the
+248,320-token vocabulary.  Inputs (5.2 GB of packed weights per step) are far larger than L2.
+
+With --gpus N (launched by torchrun, one rank per GPU) every rank runs its own replica on its
+own requests: the path has no exchange step, so there is no collective on the data path
+(weak scaling); the barrier and the max-over-ranks timing are the only communication.
+
+--impl reference times the oracle (plain fp64 numpy, CPU) as it stands, on a bounded sample of
+the same workload, in the same metric and unit; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s, 32-layer hybrid (L=512, L=16384); % of HBM/tensor roofline"
+WORKLOADS = {
+    "l16384": dict(B=1, L=16384, desc="32-layer hybrid prefill, 1 request x 16384 positions"),
+    "l512": dict(B=1, L=512, desc="32-layer hybrid prefill, 1 request x 512 positions"),
+    "b32x512": dict(B=32, L=512, desc="32-layer hybrid prefill, 32 independent requests x 512 positions"),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], tc_burst=d["bf16_tflops"], tc_sust=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, tc_burst=1900.0, tc_sust=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"clef_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_oracle_sample(seed, ids_row, n_tokens):
+    """Oracle seconds for one GDN layer and one attention layer on the first n_tokens of a request,
+    extrapolated to the 32-layer model (24 GDN + 8 attention layers): tokens/s."""
+    import numpy as np
+
+    import synth
+    from oracle import layers as Lr
+    from oracle import model as om
+
+    ids = ids_row[:n_tokens]
+    x = synth.embedding_rows(seed, ids).astype(np.float64)
+    t_layer = {}
+    for layer in (0, 3):
+        w = synth.layer_weights(seed, layer)
+        t0 = time.perf_counter()
+        om.decoder_layer(x, w, synth.is_attention_layer(layer))
+        t_layer[layer] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    Lr.rmsnorm(x, synth.final_norm_weight(seed))
+    t_final = time.perf_counter() - t0
+    total = 24 * t_layer[0] + 8 * t_layer[3] + t_final
+    return n_tokens / total, t_layer[0] + t_layer[3] + t_final
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    ids = synth.token_ids(0, wl["B"], wl["L"])
+    n_tok = 64
+    vals = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(0, ids[0], n_tok)
+    t_all = 0.0
+    for _ in range(args.steps):
+        v, t = cpu_oracle_sample(0, ids[0], n_tok)
+        vals.append(v)
+        t_all += t
+    value = statistics.median(vals)
+    cores = os.cpu_count()
+    sample = (f"oracle (fp64 numpy) on the first {n_tok} positions of the workload's first request: "
+              f"one GDN layer (layer 0) and one attention layer (layer 3) timed, scaled to 24 + 8 "
+              f"layers; the quadratic attention term is that of {n_tok} positions")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t_all / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl["desc"], "global_batch": wl["B"], "seq_len": wl["L"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_clef(args, wl):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import full_attention_prefill_gb300 as clef
+    import synth
+    from full_attention_prefill_gb300.model import synth_model
+
+    B, L = wl["B"], wl["L"]
+    model = synth_model(0, 32, device=dev)
+    ids_np = synth.token_ids(1000 + rank, B, L)      # each rank: its own requests
+    ids = torch.from_numpy(ids_np).to(dev)
+    out = torch.empty((B, L, 4096), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        model.forward(ids, out=out)
+    clef.sync_status()
+
+    # ---- timed region: device-resident inputs
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    lib = clef.lib()
+    lib.clef_trace_begin()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        model.forward(ids, out=out)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    import ctypes
+    entries = (TraceEntry * 32)()
+    n = ctypes.c_int32(0)
+    lib.clef_trace_begin.restype = ctypes.c_int
+    lib.clef_trace_end.argtypes = [ctypes.POINTER(TraceEntry), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    rc = lib.clef_trace_end(entries, 32, ctypes.byref(n))
+    clk = clocks.stop()
+    clef.sync_status()
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = B * L * args.steps * world
+    value = tokens / (total_ms / 1000.0)
+    trace = {}
+    if rc == 0:
+        for i in range(n.value):
+            e = entries[i]
+            trace[e.name.decode()] = dict(launches=e.launches, ms=e.ms, flops=e.flops, bytes=e.bytes)
+
+    # ---- end to end through the public API: pinned host ids in, pinned host hidden out
+    ids_host = torch.from_numpy(ids_np).pin_memory()
+    out_host = torch.empty((B, L, 4096), dtype=torch.float16).pin_memory()
+    ids_dev = torch.empty_like(ids)
+    for _ in range(max(1, args.warmup // 2)):
+        ids_dev.copy_(ids_host, non_blocking=True)
+        model.forward(ids_dev, out=out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ids_dev.copy_(ids_host, non_blocking=True)
+        model.forward(ids_dev, out=out)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens / (e2e_ms / 1000.0)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    g = trace.get("lut6_gemm")
+    roofline = None
+    if g and g["ms"] > 0:
+        per_launch_flops = g["flops"] / g["launches"]
+        avg_ms = g["ms"] / g["launches"]
+        achieved = per_launch_flops / (avg_ms / 1000.0) / 1e12
+        peak = pk["tc_sust"]
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None, "kernel": "lut6_gemm",
+                    "peak_kind": f"bf16 dense sustained ({pk['source']}), fp16 same nominal rate",
+                    "algorithmic_flops_per_launch": per_launch_flops, "avg_launch_ms": avg_ms}
+    cpu_v, _ = cpu_oracle_sample(0, ids_np[0], 64)
+    step_total = sum(t["ms"] for t in trace.values()) / args.steps if trace else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16 activations, fp32 accumulate, LUT-6 weights",
+        "data": "synthetic (seeded random LUT-6 weights and token ids)",
+        "config": {"workload": wl["desc"], "global_batch": B * world, "seq_len": L, "layers": 32,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2 (5.2 GB of packed weights streamed per step)"},
+        "roofline": roofline,
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "oracle (fp64 numpy) on the first 64 positions: one GDN and one "
+                                   "attention layer timed, scaled to 24 + 8 layers"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(ids_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": int(sum(t["launches"] for t in trace.values())) if trace else None,
+        "clocks": clk,
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "kernels_ms_per_step": {k: round(v["ms"] / args.steps, 3) for k, v in sorted(trace.items(), key=lambda kv: -kv[1]["ms"])},
+        "kernel_time_sum_ms_per_step": step_total,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+import ctypes  # noqa: E402
+
+
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["clef", "reference"], default="clef")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="l16384")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_clef(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "lut6.cuh"
@@ -103,6 +104,45 @@ bool debug_should_fail() {
   return false;
 }
 
+// ---- per-kernel-class tracing ----
+struct TraceRec {
+  cudaEvent_t a, b;
+  const char* cls;
+  double flops, bytes;
+  bool used;
+};
+static std::mutex g_trace_mu;
+static bool g_trace = false;
+static std::vector<TraceRec> g_recs;
+static size_t g_next = 0;
+
+bool trace_on() { return g_trace; }
+
+int trace_start(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (!g_trace) return -1;
+  if (g_next == g_recs.size()) {
+    TraceRec r{};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return -1;
+    g_recs.push_back(r);
+  }
+  const int slot = (int)g_next++;
+  g_recs[slot].used = false;
+  cudaEventRecord(g_recs[slot].a, s);
+  return slot;
+}
+
+void trace_stop(int slot, cudaStream_t s, const char* cls, double flops, double bytes) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (slot < 0 || (size_t)slot >= g_recs.size()) return;
+  TraceRec& r = g_recs[slot];
+  cudaEventRecord(r.b, s);
+  r.cls = cls;
+  r.flops = flops;
+  r.bytes = bytes;
+  r.used = true;
+}
+
 }  // namespace clef
 
 using namespace clef;
@@ -114,6 +154,45 @@ extern "C" {
 const char* clef_last_error(void) { return g_err; }
 
 int32_t clef_version(void) { return (1 << 16) | 0; }
+
+clef_status clef_trace_begin(void) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  g_trace = true;
+  g_next = 0;
+  return CLEF_OK;
+}
+
+clef_status clef_trace_end(clef_trace_entry* entries, int32_t max_entries, int32_t* n_entries) {
+  if (!n_entries || (max_entries > 0 && !entries)) {
+    set_error("clef_trace_end: NULL output");
+    return CLEF_E_INVALID;
+  }
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  g_trace = false;
+  CLEF_CUDA_CHECK(cudaDeviceSynchronize());
+  int32_t n = 0;
+  for (size_t i = 0; i < g_next; ++i) {
+    const TraceRec& r = g_recs[i];
+    if (!r.used) continue;
+    float ms = 0.f;
+    CLEF_CUDA_CHECK(cudaEventElapsedTime(&ms, r.a, r.b));
+    int32_t j = 0;
+    while (j < n && strncmp(entries[j].name, r.cls, sizeof entries[j].name) != 0) ++j;
+    if (j == n) {
+      if (n == max_entries) continue;
+      memset(&entries[n], 0, sizeof entries[n]);
+      strncpy(entries[n].name, r.cls, sizeof entries[n].name - 1);
+      ++n;
+    }
+    entries[j].launches += 1;
+    entries[j].ms += ms;
+    entries[j].flops += r.flops;
+    entries[j].bytes += r.bytes;
+  }
+  g_next = 0;
+  *n_entries = n;
+  return CLEF_OK;
+}
 
 void clef_debug_fail_next(int32_t n_calls) {
   std::lock_guard<std::mutex> lock(g_fail_mu);

@@ -259,6 +259,7 @@ clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t l
                         const __half* kin, int64_t ldki, __half* kout, int64_t ldko, int64_t M,
                         int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
   attn::rope_kernel<<<(unsigned)M, 128, 0, stream>>>(qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
                                                      (int)L);
   CLEF_LAUNCH_CHECK();
@@ -277,6 +278,8 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
     attr = true;
   }
   dim3 grid((unsigned)((L + attn::POS - 1) / attn::POS), (unsigned)(B * attn::HKV));
+  TraceScope ts(stream, "flash_attn", 4.0 * attn::D * attn::HQ * (double)B * L * (L + 1) / 2.0,
+                (double)B * L * (16 + 4 + 4 + 16 + 16) * attn::D * 2.0);
   attn::flash_kernel<<<grid, attn::THREADS, sizeof(attn::FlashSmem), stream>>>(
       q, ldq, k, ldk, v, ldv, gate, ldg, out, ldo, (int)L);
   CLEF_LAUNCH_CHECK();

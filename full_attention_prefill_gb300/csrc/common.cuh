@@ -33,6 +33,24 @@ const char* set_error(const char* fmt, ...);
 int num_sms();
 bool debug_should_fail();            // host-side fault hook (clef_debug_fail_next)
 
+// Per-kernel-class device timing (clef_trace_begin / clef_trace_end).  A TraceScope around a
+// launch records a CUDA event before and after it on the launch stream while tracing is on, and
+// books the launch's algorithmic flops and bytes to its class.
+bool trace_on();
+int trace_start(cudaStream_t s);
+void trace_stop(int slot, cudaStream_t s, const char* cls, double flops, double bytes);
+struct TraceScope {
+  cudaStream_t s;
+  const char* cls;
+  double flops, bytes;
+  int slot;
+  TraceScope(cudaStream_t s_, const char* c, double f, double b)
+      : s(s_), cls(c), flops(f), bytes(b), slot(trace_on() ? trace_start(s_) : -1) {}
+  ~TraceScope() {
+    if (slot >= 0) trace_stop(slot, s, cls, flops, bytes);
+  }
+};
+
 #define CLEF_CUDA_CHECK(expr)                                                      \
   do {                                                                             \
     cudaError_t _e = (expr);                                                       \

@@ -663,6 +663,7 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const float* ab, co
                             __half* v, float* g, float* beta, int64_t M, int64_t L,
                             cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "gdn_prep", 0.0, M * (4.0 * 8192 * 2 + 8192 * 2 + 64 * 4 + 64 * 4));
   gdn::gdn_prep_kernel<<<(unsigned)M, 256, 0, stream>>>(proj, ldp, ab, conv_w, A_log, dt_bias, q, k,
                                                          v, g, beta, (int)L);
   CLEF_LAUNCH_CHECK();
@@ -687,16 +688,29 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     g = w.g;
   }
   dim3 g1((unsigned)(B * nch), gdn::HV);
-  gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(k, v, g, beta, w.gcum, w.W,
-                                                                      w.U1, (int)L, nch);
-  CLEF_LAUNCH_CHECK();
-  gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * (gdn::D / gdn::SL)), 128,
-                               sizeof(gdn::PassSmem), stream>>>(k, w.W, w.U1, w.gcum, s0, w.U, w.S0,
-                                                                s_out, (int)L, nch);
-  CLEF_LAUNCH_CHECK();
-  gdn::gdn_chunk_out_kernel<<<g1, 128, sizeof(gdn::OutSmem), stream>>>(
-      q, k, w.U, w.S0, w.gcum, z, ldz, o_norm, out, ldo, (int)L, nch);
-  CLEF_LAUNCH_CHECK();
+  const double C = gdn::C, D = gdn::D, HVd = gdn::HV, nchunks = (double)B * nch;
+  {
+    TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 6.0 * C * C * D,
+                  (double)M * HVd * D * (2 + 2 + 2 + 4));
+    gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(k, v, g, beta, w.gcum, w.W,
+                                                                        w.U1, (int)L, nch);
+    CLEF_LAUNCH_CHECK();
+  }
+  {
+    TraceScope ts(stream, "gdn_state_pass", nchunks * HVd * 4.0 * C * D * D,
+                  (double)M * HVd * D * (2 + 4 + 2) + (double)M * 16 * D * 2 + nchunks * HVd * D * D * 2);
+    gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * (gdn::D / gdn::SL)), 128,
+                                 sizeof(gdn::PassSmem), stream>>>(k, w.W, w.U1, w.gcum, s0, w.U,
+                                                                  w.S0, s_out, (int)L, nch);
+    CLEF_LAUNCH_CHECK();
+  }
+  {
+    TraceScope ts(stream, "gdn_chunk_out", nchunks * HVd * (4.0 * C * C * D + 2.0 * C * D * D),
+                  (double)M * HVd * D * (2 + 2 + 2) + (double)M * 32 * D * 2 * 2 + nchunks * HVd * D * D * 2);
+    gdn::gdn_chunk_out_kernel<<<g1, 128, sizeof(gdn::OutSmem), stream>>>(
+        q, k, w.U, w.S0, w.gcum, z, ldz, o_norm, out, ldo, (int)L, nch);
+    CLEF_LAUNCH_CHECK();
+  }
   return CLEF_OK;
 }
 

@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
 clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab, float* x,
                          int64_t M, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "embed", 0.0, M * (4096.0 * 2 + 4096.0 * 4));
   glue::embed_kernel<<<(unsigned)M, 256, 0, stream>>>(ids, table, vocab, x, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
@@ -156,6 +157,7 @@ clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab,
 clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
                            cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "rmsnorm", 0.0, M * (4096.0 * 4 + 4096.0 * 2));
   glue::rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(x, w, y);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
@@ -164,6 +166,7 @@ clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M
 clef_status ab_proj_launch(const __half* xn, const __half* w_ab, float* ab, int64_t M,
                            cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
   glue::ab_proj_kernel<<<(unsigned)((M + glue::AB_T - 1) / glue::AB_T), 128, 0, stream>>>(xn, w_ab,
                                                                                          ab, M);
   CLEF_LAUNCH_CHECK();

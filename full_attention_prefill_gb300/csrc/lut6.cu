@@ -329,6 +329,12 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* packed, const __hal
     attr_set = true;
   }
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  const double out_bytes = mode == EPI_F16 ? 2.0 * M * N
+                           : mode == EPI_F32 ? 4.0 * M * N
+                           : mode == EPI_ADD_F32 ? 8.0 * M * N
+                                                 : 1.0 * M * N;  // SwiGLU: fp16 [M, N/2]
+  TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
+                0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
   lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
       tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
   CLEF_LAUNCH_CHECK();
@@ -341,6 +347,7 @@ clef_status lut6_dequant_launch(const uint8_t* packed, const __half* lut, int64_
   if (quads == 0) return CLEF_OK;
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((quads + threads - 1) / threads, 65535LL * 8);
+  TraceScope ts(stream, "lut6_dequant", 0.0, 0.75 * n * k + 2.0 * n * k);
   lut::lut6_dequant_kernel<<<(unsigned)blocks, threads, 0, stream>>>(packed, lut, n, k, w);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;

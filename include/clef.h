@@ -208,6 +208,22 @@ CLEF_API clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64
    CLEF_E_DEVICE_TIMEOUT, CLEF_E_BAD_TOKEN or CLEF_E_CUDA. */
 CLEF_API clef_status clef_sync_status(clef_stream stream);
 
+/* Per-kernel-class device time.  Between clef_trace_begin() and clef_trace_end(), every kernel
+   the library launches (from any thread) is bracketed by CUDA events on its own stream.
+   clef_trace_end synchronises the device, then fills up to max_entries entries (one per kernel
+   class: launches, summed device milliseconds, and the summed algorithmic flops and bytes of
+   those launches) and writes their number to *n_entries.  Adds two event records per launch. */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double ms;
+  double flops;
+  double bytes;
+} clef_trace_entry;
+CLEF_API clef_status clef_trace_begin(void);
+CLEF_API clef_status clef_trace_end(clef_trace_entry* entries, int32_t max_entries,
+                                    int32_t* n_entries);
+
 /* Host-side fault hook for tests of the error paths: the next `n_calls` device entry points fail
    with CLEF_E_CUDA before launching anything.  Affects the calling process only. */
 CLEF_API void clef_debug_fail_next(int32_t n_calls);
