@@ -83,6 +83,8 @@ _SIGS = {
     "clef_gdn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int64, ctypes.c_int64,
                                                                   ctypes.c_void_p, ctypes.c_size_t,
                                                                   ctypes.c_void_p]),
+    "clef_gdn_prefill_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int64, ctypes.c_int64,
+                                                                          ctypes.c_void_p]),
     "clef_attn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "clef_gqa_attn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 +
                               [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),

@@ -127,6 +127,26 @@ CLEF_API clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, cons
                              float* s_out, int64_t B, int64_t L, void* workspace,
                              size_t workspace_bytes, clef_stream stream);
 
+/* The same scan for callers that cannot allocate device memory (no counterpart on the pages; an
+ * interface convenience).  Some hosts cannot call cudaMalloc: a plugin inside a runtime that owns
+ * the device allocator, or code that must not allocate once it is serving.  This call takes the
+ * same inputs and outputs as clef_gdn_prefill but no workspace: its scratch is one array of
+ * CLEF_GDN_NOALLOC_SCRATCH_BYTES (64 MiB) with static storage in the library, which every GPU
+ * that loads the library keeps reserved until the process exits.  Sizes whose scratch
+ * (clef_gdn_workspace_size(B, L), about 33 KB per position plus 1 MiB per 64-position chunk of
+ * each request) exceeds it are refused with CLEF_E_SHAPE; one request of up to 1,024 positions
+ * always fits.  The first call on a device looks up the array's device address (with that device
+ * current), so make that first call before any stream capture.  All calls share the one array
+ * and it keeps the last call's contents; nothing in it has to start at zero.  Two calls that run
+ * on the GPU at the same time (other streams, other threads) race on it: serialise them.
+ * Results equal clef_gdn_prefill's bit for bit. */
+#define CLEF_GDN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+CLEF_API clef_status clef_gdn_prefill_noalloc(const uint16_t* q, const uint16_t* k,
+                                              const uint16_t* v, const float* alpha,
+                                              const float* beta, const float* s0, uint16_t* o,
+                                              float* s_out, int64_t B, int64_t L,
+                                              clef_stream stream);
+
 /* ------------------------------------------------------------------------------------------
  * Causal GQA attention of a gated full-attention layer ("Clef-Flash-ANE-LUT6" section "Model
  * architecture": 16 query and 4 kv heads of 256; "clef-flash-LiteRT" section "Host contract"
