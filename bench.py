@@ -299,8 +299,69 @@ class TraceEntry(ctypes.Structure):
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
+def run_micro(args):
+    """One kernel entry point in a loop (CUDA events), for profiling and tuning.
+
+    gemm: clef_lut6_gemm at M x N x K (fp16 out); attn: clef_gqa_attn_prefill at L (gated);
+    gdn: clef_gdn_prefill at L.  Prints one JSON line; not the headline metric.
+    """
+    import numpy as np
+    import torch
+
+    import full_attention_prefill_gb300 as clef
+    import synth
+
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    if args.micro == "gemm":
+        M, N, K = args.m, args.n, args.k
+        x = torch.from_numpy(synth.normal_f16(0, "micro.x", 0, (M, K))).to(dev)
+        packed, lut = synth.lut6_weight(0, "micro.w", 0, N, K)
+        p, l = torch.from_numpy(packed).to(dev), torch.from_numpy(lut).to(dev)
+        y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        fn = lambda: clef.lut6_gemm(x, p, l, out=y)  # noqa: E731
+        flops, desc = 2.0 * M * N * K, f"lut6_gemm M={M} N={N} K={K}"
+    elif args.micro == "attn":
+        L = args.L
+        q = torch.from_numpy(synth.normal_f16(0, "q", 0, (1, L, 16, 256))).to(dev)
+        k = torch.from_numpy(synth.normal_f16(0, "k", 0, (1, L, 4, 256))).to(dev)
+        v = torch.from_numpy(synth.normal_f16(0, "v", 0, (1, L, 4, 256))).to(dev)
+        g = torch.from_numpy(synth.normal_f16(0, "g", 0, (1, L, 16, 256))).to(dev)
+        fn = lambda: clef.gqa_attn_prefill(q, k, v, g)  # noqa: E731
+        flops, desc = 4.0 * 256 * 16 * L * (L + 1) / 2, f"gqa_attn L={L}"
+    else:
+        L = args.L
+        q = torch.from_numpy(synth.normal_f16(0, "q", 0, (1, L, 16, 128))).to(dev)
+        k = torch.from_numpy(synth.normal_f16(0, "k", 0, (1, L, 16, 128))).to(dev)
+        q = q / q.float().norm(dim=-1, keepdim=True).half()
+        k = k / k.float().norm(dim=-1, keepdim=True).half()
+        v = torch.from_numpy(synth.normal_f16(0, "v", 0, (1, L, 32, 128))).to(dev)
+        a = torch.full((1, L, 32), 0.92, dtype=torch.float32, device=dev)
+        b = torch.full((1, L, 32), 0.5, dtype=torch.float32, device=dev)
+        fn = lambda: clef.gdn_prefill(q, k, v, a, b)  # noqa: E731
+        flops, desc = 6.0 * 128 * 128 * 32 * L, f"gdn_scan L={L}"
+    for _ in range(args.warmup):
+        fn()
+    clef.sync_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    clef.sync_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"micro": desc, "ms": ms, "tflops": flops / ms / 1e9,
+                      "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--micro", choices=["gemm", "attn", "gdn"], default=None)
+    ap.add_argument("--m", type=int, default=4096)
+    ap.add_argument("--n", type=int, default=24576)
+    ap.add_argument("--k", type=int, default=4096)
+    ap.add_argument("--L", type=int, default=4096)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
@@ -310,7 +371,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     wl = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.micro:
+        run_micro(args)
+    elif args.impl == "reference":
         run_reference(args, wl)
     else:
         run_clef(args, wl)
