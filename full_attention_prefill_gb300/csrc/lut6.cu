@@ -5,17 +5,19 @@
 // into three bytes as one little-endian (LSB-first) bit stream, rows of W in order, k fastest.
 //
 // GEMM design (sm_103a): Y[m, n] = sum_k X[m, k] * T[n/16][idx[n, k]].
-//   * one CTA per 128 (tokens) x 256 (output channels) tile, K walked in blocks of 64;
-//   * warp 0 issues TMA loads of the X tile (128-byte swizzle) and of the packed index tile
-//     (256 rows x 48 bytes) into a 3-stage ring;
+//   * one CTA per 256 (tokens) x 128 (output channels) tile, K walked in blocks of 64;
+//   * warp 0 issues TMA loads of the X tile (256 rows, 128-byte swizzle) and of the packed
+//     index tile (128 rows x 48 bytes) into a 4-stage ring;
 //   * warps 4..11 turn the packed tile into the fp16 weight tile in shared memory: each lane
-//     unpacks 16 indices from 12 bytes and looks them up in its group's 64-entry table, which
-//     sits in 128 bytes = one entry pair per bank, so a warp (8 rows of one 16-row group) never
-//     conflicts; the tile is written directly in the 128-byte-swizzled K-major layout;
-//   * warp 1 issues tcgen05.mma (M=128, N=256, K=16, fp16 x fp16 -> fp32) from the two shared
-//     tiles into a 128 x 256 fp32 accumulator in tensor memory;
-//   * warps 4..11 then read the accumulator with tcgen05.ld and run the fused epilogue (fp16 or
-//     fp32 store, fp32 residual add, or SwiGLU of an interleaved gate/up tile).
+//     unpacks 16 indices from 12 bytes (index*2 is cut out and OR'd into its table's address in
+//     one logic op) and looks them up in its group's 64-entry table, which sits in 128 bytes =
+//     one entry pair per bank, so a warp (8 rows of one 16-row group) never conflicts; the tile
+//     is written directly in the 128-byte-swizzled K-major layout;
+//   * warp 1 issues two tcgen05.mma per K=16 step (M=128 each, N=128, fp16 x fp16 -> fp32), one
+//     per 128-token half, both reading the same weight tile, into two 128 x 128 fp32
+//     accumulators in tensor memory: each dequantised weight serves 256 tokens;
+//   * warps 4..11 then read the accumulators with tcgen05.ld and run the fused epilogue (fp16
+//     or fp32 store, fp32 residual add, or SwiGLU of an interleaved gate/up tile).
 // The dense weight never reaches global memory.
 #include <stdarg.h>
 #include <stdio.h>
@@ -26,18 +28,18 @@
 namespace clef {
 namespace lut {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 256;                       // tokens per tile: two M = 128 MMAs
+constexpr int BN = 128;                       // output channels per tile
 constexpr int BK = 64;
-constexpr int STAGES = 3;
-constexpr int X_BYTES = BM * BK * 2;          // 16 KB
-constexpr int W_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGES = 4;
+constexpr int X_BYTES = BM * BK * 2;          // 32 KB
+constexpr int W_BYTES = BN * BK * 2;          // 16 KB
 constexpr int P_ROW = BK * 3 / 4;             // 48 packed bytes per row per k-block
-constexpr int P_BYTES = BN * P_ROW;           // 12 KB
-constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 2 KB: the 16 tables of the tile's rows
+constexpr int P_BYTES = BN * P_ROW;           // 6 KB
+constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the tile's rows
 constexpr int NUM_DQ_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (4 + NUM_DQ_WARPS);
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 256;                // two 128-column fp32 accumulators
 
 constexpr int OFF_X = 0;
 constexpr int OFF_W = OFF_X + STAGES * X_BYTES;
@@ -47,14 +49,11 @@ constexpr int OFF_BAR = OFF_T + TBL_BYTES;
 constexpr int OFF_SLOT = OFF_BAR + 16 * 8;
 constexpr int SMEM_USED = OFF_SLOT + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(BN == 2 * CLEF_SWIGLU_BLOCK, "a SwiGLU tile holds one gate block and its up block");
 
 static_assert(OFF_W % 1024 == 0 && OFF_P % 1024 == 0, "tile alignment");
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -70,24 +69,39 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// 16 indices of 6 bits from 96 bits (w0 | w1 << 32 | w2 << 64), LSB first.
-__device__ __forceinline__ void unpack16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&ix)[16]) {
-  ix[0] = w0 & 63u;
-  ix[1] = (w0 >> 6) & 63u;
-  ix[2] = (w0 >> 12) & 63u;
-  ix[3] = (w0 >> 18) & 63u;
-  ix[4] = (w0 >> 24) & 63u;
-  ix[5] = __funnelshift_r(w0, w1, 30) & 63u;
-  ix[6] = (w1 >> 4) & 63u;
-  ix[7] = (w1 >> 10) & 63u;
-  ix[8] = (w1 >> 16) & 63u;
-  ix[9] = (w1 >> 22) & 63u;
-  ix[10] = __funnelshift_r(w1, w2, 28) & 63u;
-  ix[11] = (w2 >> 2) & 63u;
-  ix[12] = (w2 >> 8) & 63u;
-  ix[13] = (w2 >> 14) & 63u;
-  ix[14] = (w2 >> 20) & 63u;
-  ix[15] = (w2 >> 26) & 63u;
+// Table addresses of 16 indices of 6 bits taken from 96 bits (w0 | w1 << 32 | w2 << 64), LSB
+// first: index i sits at bits 6i..6i+5; (index * 2) is cut out and OR'd into the table base tb
+// (128-byte aligned), one shift and one logic op per index.
+__device__ __forceinline__ void table_addrs16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t tb,
+                                              uint32_t (&a)[16]) {
+  a[0] = ((w0 << 1) & 0x7Eu) | tb;
+  a[1] = ((w0 >> 5) & 0x7Eu) | tb;
+  a[2] = ((w0 >> 11) & 0x7Eu) | tb;
+  a[3] = ((w0 >> 17) & 0x7Eu) | tb;
+  a[4] = ((w0 >> 23) & 0x7Eu) | tb;
+  a[5] = (__funnelshift_r(w0, w1, 29) & 0x7Eu) | tb;
+  a[6] = ((w1 >> 3) & 0x7Eu) | tb;
+  a[7] = ((w1 >> 9) & 0x7Eu) | tb;
+  a[8] = ((w1 >> 15) & 0x7Eu) | tb;
+  a[9] = ((w1 >> 21) & 0x7Eu) | tb;
+  a[10] = (__funnelshift_r(w1, w2, 27) & 0x7Eu) | tb;
+  a[11] = ((w2 >> 1) & 0x7Eu) | tb;
+  a[12] = ((w2 >> 7) & 0x7Eu) | tb;
+  a[13] = ((w2 >> 13) & 0x7Eu) | tb;
+  a[14] = ((w2 >> 19) & 0x7Eu) | tb;
+  a[15] = ((w2 >> 25) & 0x7Eu) | tb;
+}
+// Two fp16 table entries packed into one 32-bit word (first in the low half).
+__device__ __forceinline__ uint32_t lds_pair(uint32_t a0, uint32_t a1) {
+  uint32_t v;
+  asm volatile(
+      "{\n\t.reg .b16 lo, hi;\n\t"
+      "ld.shared.b16 lo, [%1];\n\t"
+      "ld.shared.b16 hi, [%2];\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(v)
+      : "r"(a0), "r"(a1));
+  return v;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+      constexpr uint32_t idesc = idesc_f16_f32(128, BN);
       bool ok = true;
       for (int kb = 0; kb < num_kb && ok; ++kb) {
         const int s = kb % STAGES;
@@ -157,9 +171,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = sdesc_k_sw128(sb + OFF_X + s * X_BYTES + kk * 32);
           const uint64_t bd = sdesc_k_sw128(sb + OFF_W + s * W_BYTES + kk * 32);
-          tc_mma_f16_ss(tmem, ad, bd, idesc, (kb | kk) != 0);
+          const uint64_t a0 = sdesc_k_sw128(sb + OFF_X + s * X_BYTES + kk * 32);
+          const uint64_t a1 = sdesc_k_sw128(sb + OFF_X + s * X_BYTES + 16384 + kk * 32);
+          tc_mma_f16_ss(tmem, a0, bd, idesc, (kb | kk) != 0);
+          tc_mma_f16_ss(tmem + BN, a1, bd, idesc, (kb | kk) != 0);
         }
         tc_commit(bar_empty + 8 * s);
       }
@@ -170,12 +186,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int dq = warp - 4;              // 0..7
     const int t = threadIdx.x - 128;      // 0..255
     {
-      // the tile's 16 tables (rows n0 .. n0+255); groups past N read as zero
-      const int e = t * 4;
+      // the tile's 8 tables (rows n0 .. n0+127); groups past N read as zero
+      const int e = t * 2;
       const int g = n0 / 16 + e / 64;
-      uint2 v = make_uint2(0u, 0u);
-      if (g < N / 16) v = *reinterpret_cast<const uint2*>(lut + (size_t)g * 64 + (e & 63));
-      *reinterpret_cast<uint2*>(smem + OFF_T + e * 2) = v;
+      uint32_t v = 0u;
+      if (g < N / 16) v = *reinterpret_cast<const uint32_t*>(lut + (size_t)g * 64 + (e & 63));
+      *reinterpret_cast<uint32_t*>(smem + OFF_T + e * 2) = v;
     }
     named_bar_sync(1, 32 * NUM_DQ_WARPS);
     const int rsub = lane >> 2;  // row inside the 8-row task
@@ -194,16 +210,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t wbase = sb + OFF_W + s * W_BYTES;
 #pragma unroll
       for (int it = 0; it < BN / 8 / NUM_DQ_WARPS; ++it) {
-        const int row = (dq + NUM_DQ_WARPS * it) * 8 + rsub;  // 0..255
+        const int row = (dq + NUM_DQ_WARPS * it) * 8 + rsub;  // 0..127
         const uint32_t pa = pbase + row * P_ROW + q4 * 12;
         const uint32_t w0 = lds_u32(pa), w1 = lds_u32(pa + 4), w2 = lds_u32(pa + 8);
-        uint32_t ix[16];
-        unpack16(w0, w1, w2, ix);
-        const uint32_t tb = sb + OFF_T + (row >> 4) * 128;
+        uint32_t a[16];
+        table_addrs16(w0, w1, w2, sb + OFF_T + (row >> 4) * 128, a);
         uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[i] = lds_u16(tb + ix[2 * i] * 2) | (lds_u16(tb + ix[2 * i + 1] * 2) << 16);
+        for (int i = 0; i < 8; ++i) o[i] = lds_pair(a[2 * i], a[2 * i + 1]);
         const uint32_t wrow = wbase + (row >> 3) * 1024 + (row & 7) * 128;
         sts_v4(wrow + (((2 * q4) ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
         sts_v4(wrow + (((2 * q4 + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
@@ -212,20 +226,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_wready + 8 * s);
     }
-    // ---- epilogue
+    // ---- epilogue: warps 4..7 drain accumulator 0 (tokens 0..127), warps 8..11 accumulator 1
     if (ok && mbar_wait(bar_acc, 0, status, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
       const int quarter = warp & 3;
       const int half = dq >> 2;
-      const int row = m0 + quarter * 32 + lane;
-      const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+      const int row = m0 + half * 128 + quarter * 32 + lane;
+      const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + half * BN;
       if (mode == EPI_SWIGLU_F16) {
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
-          const int j0 = half * 64 + c * 32;
+          const int j0 = c * 32;
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(tl + j0, g);
-          tmem_ld_32x32b_x32(tl + 128 + j0, u);
+          tmem_ld_32x32b_x32(tl + BN / 2 + j0, u);
           tc_wait_ld();
           if (row < M) {
             __half* out = reinterpret_cast<__half*>(y) + (int64_t)row * ldy + n0 / 2 + j0;
@@ -246,8 +260,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const int col0 = half * 128 + c * 32;
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = c * 32;
           uint32_t r[32];
           tmem_ld_32x32b_x32(tl + col0, r);
           tc_wait_ld();

@@ -8,11 +8,11 @@ enum Epilogue : int {
   EPI_F16 = 0,        // y fp16 = acc
   EPI_F32 = 1,        // y fp32 = acc
   EPI_ADD_F32 = 2,    // y fp32 += acc (residual add, in place)
-  EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up of a gate/up tile interleaved by 128 rows
+  EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up of a gate/up tile interleaved by 64 rows
 };
 
 // y[m, n] (row stride ldy elements) = x[m, k] . W^T.  Requires n % 16 == 0, k % 64 == 0
-// (and n % 256 == 0 for EPI_SWIGLU_F16); x packed [m, k].
+// (and n % 128 == 0 for EPI_SWIGLU_F16); x packed [m, k].
 clef_status lut6_gemm_launch(const __half* x, const uint8_t* packed, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
                              cudaStream_t stream);

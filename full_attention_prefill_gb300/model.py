@@ -2,7 +2,7 @@
 
 The layout is the C ABI's (include/clef.h, clef_layer / clef_model): per layer one fused input
 projection (GDN: q | k | v | z rows; attention: query | gate | k | v rows), the output
-projection, the MLP gate and up rows interleaved in blocks of 128, and the down projection, all
+projection, the MLP gate and up rows interleaved in blocks of 64, and the down projection, all
 LUT-6; GDN small weights fp16.  Building a layer only moves bytes (row blocks of the packed
 indices and their tables are concatenated or interleaved); no weight value changes.
 """

@@ -54,3 +54,21 @@ def test_host_pack_rejects_bad_input(lib):
 
 def test_version(lib):
     assert lib.clef_version() >> 16 == 1
+
+
+def test_gate_up_interleave_layout():
+    from full_attention_prefill_gb300 import SWIGLU_BLOCK
+    from full_attention_prefill_gb300.model import interleave_gate_up
+    b = SWIGLU_BLOCK
+    n = 4 * b
+    gp = np.arange(n * 3, dtype=np.int64).reshape(n, 3).astype(np.uint8)
+    up = (gp.astype(np.int64) + 101).astype(np.uint8)
+    gl = np.arange(n // 16 * 64, dtype=np.float32).reshape(n // 16, 64).astype(np.float16)
+    ul = gl + np.float16(1000)
+    p, l = interleave_gate_up((gp, gl), (up, ul))
+    for j in range(n // b):
+        assert np.array_equal(p[2 * j * b:(2 * j + 1) * b], gp[j * b:(j + 1) * b])
+        assert np.array_equal(p[(2 * j + 1) * b:(2 * j + 2) * b], up[j * b:(j + 1) * b])
+        t = b // 16
+        assert np.array_equal(l[2 * j * t:(2 * j + 1) * t], gl[j * t:(j + 1) * t])
+        assert np.array_equal(l[(2 * j + 1) * t:(2 * j + 2) * t], ul[j * t:(j + 1) * t])
