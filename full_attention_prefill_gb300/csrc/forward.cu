@@ -32,7 +32,6 @@ struct FwdWs {
   float* x;
   __half* xn;
   __half* proj;
-  float* ab;
   __half* q;
   __half* k;
   __half* v;
@@ -56,7 +55,6 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
   t.x = static_cast<float*>(take(M * H * 4));
   t.xn = static_cast<__half*>(take(M * H * 2));
   t.proj = static_cast<__half*>(take(M * GDN_PROJ * 2));
-  t.ab = static_cast<float*>(take(M * 64 * 4));
   t.q = static_cast<__half*>(take(M * 2048 * 2));
   t.k = static_cast<__half*>(take(M * 2048 * 2));
   t.v = static_cast<__half*>(take(M * 4096 * 2));
@@ -84,11 +82,11 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
   if (ly.kind == CLEF_LAYER_GDN) {
     CLEF_TRY(lut6_gemm_launch(w.xn, ly.in_proj.packed, in_lut, w.proj, GDN_PROJ, M, GDN_PROJ, H,
                               EPI_F16, s));
-    CLEF_TRY(ab_proj_launch(w.xn, reinterpret_cast<const __half*>(ly.ab_w), w.ab, M, s));
-    CLEF_TRY(gdn_prep_launch(w.proj, GDN_PROJ, w.ab, reinterpret_cast<const __half*>(ly.conv_w),
-                             reinterpret_cast<const __half*>(ly.A_log),
-                             reinterpret_cast<const __half*>(ly.dt_bias), w.q, w.k, w.v, w.g,
-                             w.beta, M, L, s));
+    CLEF_TRY(ab_proj_launch(w.xn, reinterpret_cast<const __half*>(ly.ab_w),
+                            reinterpret_cast<const __half*>(ly.A_log),
+                            reinterpret_cast<const __half*>(ly.dt_bias), w.g, w.beta, M, s));
+    CLEF_TRY(gdn_prep_launch(w.proj, GDN_PROJ, reinterpret_cast<const __half*>(ly.conv_w), w.q,
+                             w.k, w.v, M, L, s));
     CLEF_TRY(gdn_scan_launch(w.q, w.k, w.v, w.g, nullptr, w.beta, nullptr, nullptr,
                              w.proj + 8192, GDN_PROJ, reinterpret_cast<const __half*>(ly.o_norm),
                              w.mix, H, B, L, w.scan, s));

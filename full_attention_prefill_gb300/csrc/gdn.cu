@@ -13,7 +13,7 @@
 //     S_C = exp(g_C) S0 + U^T diag(exp(g_C - g)) K
 // Three kernels:
 //   gdn_chunk_wy    (parallel over chunks x heads): g, T by forward substitution, W and U'
-//   gdn_state_pass  (sequential over chunks, parallel over heads x 4 slices of 32 value rows):
+//   gdn_state_pass  (sequential over chunks, parallel over heads x 8 slices of 16 value rows):
 //                   U and the state entering every chunk; the state stays in registers
 //   gdn_chunk_out   (parallel over chunks x heads): O, with the z-gated RMSNorm fused in
 // All products run on tensor cores (mma.sync m16n8k16, fp16 inputs, fp32 accumulation); the
@@ -35,86 +35,84 @@ constexpr int LDH = D + 8;     // padded fp16 row (272 bytes) for conflict-free 
 constexpr float kLogAlphaMin = -30.0f;
 
 // ------------------------------------------------------------------------------------------
-// Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels,
-// per-head L2 norm of q and k, and the gates g = log(alpha) = -exp(A_log) softplus(a + dt_bias),
-// beta = sigmoid(b).  One CTA (256 threads x 32 channels) per token.
-// proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..);  ab [M, 64] fp32.
+// Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels and
+// the per-head L2 norm of q and k.  A CTA walks 64 consecutive tokens for 2048 channels (256
+// threads x 8 channels); each thread keeps the last three inputs of its channels in registers,
+// so every input is read once.  The gates come from the a/b projection's epilogue.
+// proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..).
 // ------------------------------------------------------------------------------------------
+constexpr int PREP_T = 64;
 __global__ void __launch_bounds__(256) gdn_prep_kernel(
-    const __half* __restrict__ proj, int64_t ldp, const float* __restrict__ ab,
-    const __half* __restrict__ conv_w, const __half* __restrict__ A_log,
-    const __half* __restrict__ dt_bias, __half* __restrict__ q, __half* __restrict__ k,
-    __half* __restrict__ v, float* __restrict__ g, float* __restrict__ beta, int L) {
-  const int64_t tok = blockIdx.x;
-  const int t = (int)(tok % L);  // position inside its request (conv history resets per request)
+    const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
+    __half* __restrict__ q, __half* __restrict__ k, __half* __restrict__ v, int64_t M, int L) {
   const int tid = threadIdx.x;
-  const int ch0 = tid * 32;
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  // conv weights of these 32 channels: [32][4] fp16 = 256 bytes
-  float w[32][4];
+  const int ch0 = blockIdx.x * 2048 + tid * 8;
+  const int64_t tok0 = (int64_t)blockIdx.y * PREP_T;
+  float w[8][4];
   {
     const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (int64_t)ch0 * 4);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4; ++i) {
       uint4 u = wp[i];
       const __half* hh = reinterpret_cast<const __half*>(&u);
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[(i * 8 + j) / 4][(i * 8 + j) % 4] = __half2float(hh[j]);
     }
   }
+  auto load8 = [&](int64_t tok, float (&x)[8]) {
+    uint4 u = *reinterpret_cast<const uint4*>(proj + tok * ldp + ch0);
+    const __half2* h2 = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
-  for (int tap = 0; tap < 4; ++tap) {
-    const int back = 3 - tap;  // tap j multiplies x[t - 3 + j]
-    if (t - back < 0) continue;
-    const uint4* xp = reinterpret_cast<const uint4*>(proj + (tok - back) * ldp + ch0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 u = xp[i];
-      const __half* hh = reinterpret_cast<const __half*>(&u);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i * 8 + j] += w[i * 8 + j][tap] * __half2float(hh[j]);
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(h2[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
     }
+  };
+  // history x[t-1], x[t-2], x[t-3] of the first token (zero before its request's start)
+  float h1[8], h2[8], h3[8];
+  {
+    const int pos0 = (int)(tok0 % L);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) h1[c] = h2[c] = h3[c] = 0.f;
+    if (pos0 >= 1) load8(tok0 - 1, h1);
+    if (pos0 >= 2) load8(tok0 - 2, h2);
+    if (pos0 >= 3) load8(tok0 - 3, h3);
   }
+  const int64_t tend = (tok0 + PREP_T < M) ? tok0 + PREP_T : M;
+  for (int64_t tok = tok0; tok < tend; ++tok) {
+    if (tok % L == 0) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = silu_f(acc[i]);
-  if (ch0 < 4096) {
-    // q or k: a head is 128 channels = 4 consecutive threads
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ss += acc[i] * acc[i];
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float r = rsqrtf(ss + 1e-6f);
-    __half* dst = (ch0 < 2048 ? q + tok * 2048 + ch0 : k + tok * 2048 + (ch0 - 2048));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 u;
-      u.x = h2u(acc[8 * i + 0] * r, acc[8 * i + 1] * r);
-      u.y = h2u(acc[8 * i + 2] * r, acc[8 * i + 3] * r);
-      u.z = h2u(acc[8 * i + 4] * r, acc[8 * i + 5] * r);
-      u.w = h2u(acc[8 * i + 6] * r, acc[8 * i + 7] * r);
-      reinterpret_cast<uint4*>(dst)[i] = u;
+      for (int c = 0; c < 8; ++c) h1[c] = h2[c] = h3[c] = 0.f;
     }
-  } else {
-    __half* dst = v + tok * 4096 + (ch0 - 4096);
+    float x[8], y[8];
+    load8(tok, x);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 u;
-      u.x = h2u(acc[8 * i + 0], acc[8 * i + 1]);
-      u.y = h2u(acc[8 * i + 2], acc[8 * i + 3]);
-      u.z = h2u(acc[8 * i + 4], acc[8 * i + 5]);
-      u.w = h2u(acc[8 * i + 6], acc[8 * i + 7]);
-      reinterpret_cast<uint4*>(dst)[i] = u;
+    for (int c = 0; c < 8; ++c) {
+      // tap j multiplies x[t - 3 + j]
+      const float pre = w[c][0] * h3[c] + w[c][1] * h2[c] + w[c][2] * h1[c] + w[c][3] * x[c];
+      y[c] = silu_f(pre);
+      h3[c] = h2[c];
+      h2[c] = h1[c];
+      h1[c] = x[c];
     }
-  }
-  if (tid < HV) {
-    const float a = ab[tok * 64 + tid] + __half2float(dt_bias[tid]);
-    const float sp = a > 20.f ? a : log1pf(__expf(a));
-    const float gl = -__expf(__half2float(A_log[tid])) * sp;
-    g[tok * HV + tid] = fmaxf(gl, kLogAlphaMin);
-    beta[tok * HV + tid] = sigmoid_f(ab[tok * 64 + 32 + tid]);
+    __half* dst;
+    if (ch0 < 4096) {
+      // q or k: a head is 128 channels = 16 consecutive threads
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ss += y[c] * y[c];
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) y[c] *= r;
+      dst = ch0 < 2048 ? q + tok * 2048 + ch0 : k + tok * 2048 + (ch0 - 2048);
+    } else {
+      dst = v + tok * 4096 + (ch0 - 4096);
+    }
+    *reinterpret_cast<uint4*>(dst) =
+        make_uint4(h2u(y[0], y[1]), h2u(y[2], y[3]), h2u(y[4], y[5]), h2u(y[6], y[7]));
   }
 }
 
@@ -137,8 +135,7 @@ struct WySmem {
   __half KB[C][LDH];   // beta * exp(g) * K
   __half VB[C][LDH];   // beta * V
   __half T[C][C + 8];  // (I + A)^-1 in fp16 for the products
-  float A[C][C + 1];
-  float Tf[C][C + 1];
+  float A[C][C + 4];    // 16-byte aligned rows for broadcast float4 reads
   float gc[C];
   float bt[C];
 };
@@ -146,7 +143,7 @@ struct WySmem {
 __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const __half* __restrict__ kk, const __half* __restrict__ vv, const float* __restrict__ g,
     const float* __restrict__ beta, float* __restrict__ gcum, __half* __restrict__ Wout,
-    float* __restrict__ Uout, int L, int nch) {
+    float* __restrict__ Uout, __half* __restrict__ Ktout, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
   WySmem& s = *reinterpret_cast<WySmem*>(smraw);
   const int cg = blockIdx.x;           // global chunk index = b * nch + c
@@ -219,24 +216,46 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
       }
     }
   }
-  // scaled operands for W and U'
-  for (int i = tid; i < C * D; i += 128) {
-    const int r = i / D, cc = i % D;
+  // scaled operands for W and U', and the decayed keys exp(g_C - g_r) k_r the state pass uses
+  const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
+  for (int i = tid; i < C * (D / 2); i += 128) {
+    const int r = i / (D / 2), c2 = (i % (D / 2)) * 2;
     const float eb = s.bt[r] * __expf(s.gc[r]);
-    s.KB[r][cc] = __float2half_rn(eb * __half2float(s.K[r][cc]));
-    s.VB[r][cc] = __float2half_rn(s.bt[r] * __half2float(s.V[r][cc]));
+    const float ed = __expf(gC - s.gc[r]);
+    const float2 kf = __half22float2(*reinterpret_cast<const __half2*>(&s.K[r][c2]));
+    const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&s.V[r][c2]));
+    *reinterpret_cast<__half2*>(&s.KB[r][c2]) = __floats2half2_rn(eb * kf.x, eb * kf.y);
+    *reinterpret_cast<__half2*>(&s.VB[r][c2]) = __floats2half2_rn(s.bt[r] * vf.x, s.bt[r] * vf.y);
+    if (r < nvalid)
+      *reinterpret_cast<__half2*>(Ktout + ((t0 + r) * HV + h) * D + c2) =
+          __floats2half2_rn(ed * kf.x, ed * kf.y);
   }
   __syncthreads();
-  // T = (I + A)^-1: column sc only depends on earlier rows of the same column
+  // T = (I + A)^-1 by forward substitution: T[r][sc] = -sum_{j<r} A[r][j] T[j][sc] (r > sc).
+  // Column sc depends only on earlier rows of the same column: thread sc keeps its column in
+  // registers and all 64 threads read each A row as the same (broadcast) float4s.  A is zero on
+  // and above the diagonal, so whole float4s can be read past j = r.
   if (tid < C) {
     const int sc = tid;
-    for (int r = 0; r < C; ++r) s.Tf[r][sc] = (r == sc) ? 1.f : 0.f;
-    for (int r = sc + 1; r < C; ++r) {
-      float acc = 0.f;
-      for (int j = sc; j < r; ++j) acc += s.A[r][j] * s.Tf[j][sc];
-      s.Tf[r][sc] = -acc;
+    float tcol[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) tcol[r] = (r == sc) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < C; ++r) {
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; j += 4) {
+        const float4 av = *reinterpret_cast<const float4*>(&s.A[r][j]);
+        a0 += av.x * tcol[j];
+        a1 += av.y * tcol[j + 1];
+        a2 += av.z * tcol[j + 2];
+        a3 += av.w * tcol[j + 3];
+      }
+      const float val = -((a0 + a1) + (a2 + a3));
+      tcol[r] = (r > sc) ? val : tcol[r];
     }
-    for (int r = 0; r < C; ++r) s.T[r][sc] = __float2half_rn(s.Tf[r][sc]);
+#pragma unroll
+    for (int r = 0; r < C; ++r) s.T[r][sc] = __float2half_rn(tcol[r]);
   }
   __syncthreads();
   // W = T KB and U' = T VB  (rows 16w.., all 128 columns)
@@ -279,16 +298,16 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
-// Phase 2: the state pass.  One CTA per (request, value head, slice of 32 value rows); the
-// 32 x 128 fp32 state slice lives in mma accumulators (warp w: value rows 16(w&1).., key
-// columns 64(w>>1)..).  Per chunk: U = U' - W S0^T for the slice, then
-// S <- exp(g_C) S + U^T diag(exp(g_C - g)) K.  The next chunk's W, K, U' are prefetched with
-// cp.async while the current one is processed.
+// Phase 2: the state pass.  One CTA per (request, value head, slice of 16 value rows); the
+// 16 x 128 fp32 state slice lives in mma accumulators (warp w: key columns 32w..32w+31).  Per
+// chunk: U = U' - W S0^T for the slice, then S <- exp(g_C) S + U^T Kd with the decayed keys
+// Kd = diag(exp(g_C - g)) K written by phase 1.  Everything a chunk needs (W, Kd, U', g) is
+// prefetched with cp.async while the previous chunk is processed.
 // ------------------------------------------------------------------------------------------
-constexpr int SL = 32;  // value rows per CTA
+constexpr int SL = 16;  // value rows per CTA
 struct PassBuf {
   __half W[C][LDH];
-  __half K[C][LDH];
+  __half K[C][LDH];      // decayed keys
   float U[C][SL + 4];
   float gc[C];
 };
@@ -299,15 +318,16 @@ struct PassSmem {
 };
 
 __device__ __forceinline__ void pass_prefetch(PassBuf& pb, const __half* __restrict__ Wg,
-                                              const __half* __restrict__ kk,
-                                              const float* __restrict__ Ug, int64_t t0,
+                                              const __half* __restrict__ Kt,
+                                              const float* __restrict__ Ug,
+                                              const float* __restrict__ gcum, int64_t t0,
                                               int nvalid, int h, int sl, int tid) {
   for (int i = tid; i < C * (D / 8); i += 128) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < nvalid;
     const int64_t rr = ok ? (t0 + r) : t0;
     cp_async16(smem_u32(&pb.W[r][c8]), Wg + (rr * HV + h) * D + c8, ok);
-    cp_async16(smem_u32(&pb.K[r][c8]), kk + rr * (HK * D) + (h >> 1) * D + c8, ok);
+    cp_async16(smem_u32(&pb.K[r][c8]), Kt + (rr * HV + h) * D + c8, ok);
   }
   for (int i = tid; i < C * (SL / 4); i += 128) {
     const int r = i / (SL / 4), c4 = (i % (SL / 4)) * 4;
@@ -315,11 +335,18 @@ __device__ __forceinline__ void pass_prefetch(PassBuf& pb, const __half* __restr
     const int64_t rr = ok ? (t0 + r) : t0;
     cp_async16(smem_u32(&pb.U[r][c4]), Ug + (rr * HV + h) * D + sl * SL + c4, ok);
   }
+  if (tid < C) {
+    // rows past the end repeat the last valid g
+    const int64_t rr = t0 + min(tid, nvalid - 1);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&pb.gc[tid])),
+                 "l"(gcum + rr * HV + h)
+                 : "memory");
+  }
   cp_async_commit();
 }
 
 __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
-    const __half* __restrict__ kk, const __half* __restrict__ Wg, const float* __restrict__ Ug,
+    const __half* __restrict__ Kt, const __half* __restrict__ Wg, const float* __restrict__ Ug,
     const float* __restrict__ gcum, const float* __restrict__ s0, __half* __restrict__ Vnew,
     __half* __restrict__ S0out, float* __restrict__ s_out, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
@@ -329,17 +356,16 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
   const int b = blockIdx.x / ((D / SL) * HV);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int mrow = (warp & 1) * 16;      // value rows of this warp's state tiles
-  const int ncol = (warp >> 1) * 64;     // key columns of this warp's state tiles
+  const int ncol = warp * 32;            // key columns of this warp's state tiles
 
-  float S[8][4];
+  float S[4][4];
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
+  for (int n = 0; n < 4; ++n) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float v0 = 0.f;
       if (s0) {
-        const int r = sl * SL + mrow + gq + (e >= 2 ? 8 : 0);
+        const int r = sl * SL + gq + (e >= 2 ? 8 : 0);
         const int col = ncol + n * 8 + 2 * tq + (e & 1);
         v0 = s0[(((int64_t)b * HV + h) * D + r) * D + col];
       }
@@ -347,7 +373,7 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
     }
   }
   const int64_t tb = (int64_t)b * L;
-  pass_prefetch(s.buf[0], Wg, kk, Ug, tb, min(C, L), h, sl, tid);
+  pass_prefetch(s.buf[0], Wg, Kt, Ug, gcum, tb, min(C, L), h, sl, tid);
 
   for (int c = 0; c < nch; ++c) {
     const int64_t t0 = tb + (int64_t)c * C;
@@ -355,10 +381,10 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
     PassBuf& pb = s.buf[c & 1];
     // entering state: fp16 copy to shared (for W S0^T) and to global (for the output phase)
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+    for (int n = 0; n < 4; ++n) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int r = mrow + gq + hf * 8;
+        const int r = gq + hf * 8;
         const int col = ncol + n * 8 + 2 * tq;
         const uint32_t pk = h2u(S[n][2 * hf], S[n][2 * hf + 1]);
         *reinterpret_cast<uint32_t*>(&s.S[r][col]) = pk;
@@ -367,38 +393,33 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
       }
     }
     if (c + 1 < nch)
-      pass_prefetch(s.buf[(c + 1) & 1], Wg, kk, Ug, t0 + C, min(C, L - (c + 1) * C), h, sl, tid);
+      pass_prefetch(s.buf[(c + 1) & 1], Wg, Kt, Ug, gcum, t0 + C, min(C, L - (c + 1) * C), h, sl,
+                    tid);
     else
       cp_async_commit();
     cp_async_wait<1>();
-    // g of this chunk (rows past the end repeat the last valid value)
-    if (tid < C) pb.gc[tid] = gcum[(t0 + min(tid, nvalid - 1)) * HV + h];
     __syncthreads();
-    const float gC = pb.gc[C - 1];
-    // U = U' - W S0^T  (tokens 16w.., 32 value rows)
+    const float eC = __expf(pb.gc[C - 1]);
+    // U = U' - W S0^T  (tokens 16w.., 16 value rows)
     {
-      float acc[4][4];
+      float acc[2][4];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+      for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
       const uint32_t sW = smem_u32(&pb.W[0][0]);
       const uint32_t sS = smem_u32(&s.S[0][0]);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a[4];
+        uint32_t a[4], bq[4];
         ldsm_x4(a, a_addr(sW, LDH, warp * 16, ks * 16, lane));
-#pragma unroll
-        for (int n = 0; n < 4; n += 2) {
-          uint32_t bq[4];
-          ldsm_x4(bq, bn_addr(sS, LDH, n * 8, ks * 16, lane));
-          mma16816(acc[n], a, bq[0], bq[1]);
-          mma16816(acc[n + 1], a, bq[2], bq[3]);
-        }
+        ldsm_x4(bq, bn_addr(sS, LDH, 0, ks * 16, lane));
+        mma16816(acc[0], a, bq[0], bq[1]);
+        mma16816(acc[1], a, bq[2], bq[3]);
       }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = warp * 16 + gq + hf * 8;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
+        for (int n = 0; n < 2; ++n) {
           const int col = n * 8 + 2 * tq;
           const float u0 = pb.U[r][col] - acc[n][2 * hf];
           const float u1 = pb.U[r][col + 1] - acc[n][2 * hf + 1];
@@ -409,20 +430,11 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
         }
       }
     }
-    // K~ = exp(g_C - g) K, in place
-    for (int i = tid; i < C * (D / 2); i += 128) {
-      const int r = i / (D / 2), c2 = (i % (D / 2)) * 2;
-      const float f = __expf(gC - pb.gc[r]);
-      __half2 kv = *reinterpret_cast<__half2*>(&pb.K[r][c2]);
-      const float2 kf = __half22float2(kv);
-      *reinterpret_cast<__half2*>(&pb.K[r][c2]) = __floats2half2_rn(kf.x * f, kf.y * f);
-    }
     __syncthreads();
-    // S <- exp(g_C) S + U^T K~
+    // S <- exp(g_C) S + U^T Kd
     {
-      const float eC = __expf(gC);
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         S[n][0] *= eC; S[n][1] *= eC; S[n][2] *= eC; S[n][3] *= eC;
       }
       const uint32_t sV = smem_u32(&s.Vn[0][0]);
@@ -430,9 +442,9 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4_t(a, at_addr(sV, SL + 8, mrow, ks * 16, lane));
+        ldsm_x4_t(a, at_addr(sV, SL + 8, 0, ks * 16, lane));
 #pragma unroll
-        for (int n = 0; n < 8; n += 2) {
+        for (int n = 0; n < 4; n += 2) {
           uint32_t bq[4];
           ldsm_x4_t(bq, bk_addr(sK, LDH, ncol + n * 8, ks * 16, lane));
           mma16816(S[n], a, bq[0], bq[1]);
@@ -445,10 +457,10 @@ __global__ void __launch_bounds__(128) gdn_state_pass_kernel(
   cp_async_wait<0>();
   if (s_out) {
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+    for (int n = 0; n < 4; ++n) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = sl * SL + mrow + gq + (e >= 2 ? 8 : 0);
+        const int r = sl * SL + gq + (e >= 2 ? 8 : 0);
         const int col = ncol + n * 8 + 2 * tq + (e & 1);
         s_out[(((int64_t)b * HV + h) * D + r) * D + col] = S[n][e];
       }
@@ -620,6 +632,7 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L) {
   n += al256g(M * gdn::HV * gdn::D * 2);                // W
   n += al256g(M * gdn::HV * gdn::D * 4);                // U'
   n += al256g(M * gdn::HV * gdn::D * 2);                // U
+  n += al256g(M * gdn::HV * gdn::D * 2);                // decayed keys
   n += al256g(B * nch * gdn::HV * gdn::D * gdn::D * 2); // entering states
   return n;
 }
@@ -630,6 +643,7 @@ struct GdnWs {
   __half* W;
   float* U1;
   __half* U;
+  __half* Kt;
   __half* S0;
 };
 static GdnWs carve(void* ws, int64_t B, int64_t L) {
@@ -641,6 +655,7 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   w.W = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
   w.U1 = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * gdn::D * 4);
   w.U = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
+  w.Kt = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
   w.S0 = reinterpret_cast<__half*>(p);
   return w;
 }
@@ -658,14 +673,12 @@ static clef_status gdn_set_attrs() {
   return CLEF_OK;
 }
 
-clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const float* ab, const __half* conv_w,
-                            const __half* A_log, const __half* dt_bias, __half* q, __half* k,
-                            __half* v, float* g, float* beta, int64_t M, int64_t L,
-                            cudaStream_t stream) {
+clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
+                            __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
-  TraceScope ts(stream, "gdn_prep", 0.0, M * (4.0 * 8192 * 2 + 8192 * 2 + 64 * 4 + 64 * 4));
-  gdn::gdn_prep_kernel<<<(unsigned)M, 256, 0, stream>>>(proj, ldp, ab, conv_w, A_log, dt_bias, q, k,
-                                                         v, g, beta, (int)L);
+  TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
+  dim3 grid(4, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
+  gdn::gdn_prep_kernel<<<grid, 256, 0, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
@@ -693,14 +706,14 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 6.0 * C * C * D,
                   (double)M * HVd * D * (2 + 2 + 2 + 4));
     gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(k, v, g, beta, w.gcum, w.W,
-                                                                        w.U1, (int)L, nch);
+                                                                        w.U1, w.Kt, (int)L, nch);
     CLEF_LAUNCH_CHECK();
   }
   {
     TraceScope ts(stream, "gdn_state_pass", nchunks * HVd * 4.0 * C * D * D,
                   (double)M * HVd * D * (2 + 4 + 2) + (double)M * 16 * D * 2 + nchunks * HVd * D * D * 2);
     gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * (gdn::D / gdn::SL)), 128,
-                                 sizeof(gdn::PassSmem), stream>>>(k, w.W, w.U1, w.gcum, s0, w.U,
+                                 sizeof(gdn::PassSmem), stream>>>(w.Kt, w.W, w.U1, w.gcum, s0, w.U,
                                                                   w.S0, s_out, (int)L, nch);
     CLEF_LAUNCH_CHECK();
   }

@@ -4,11 +4,9 @@
 
 namespace clef {
 
-// conv(4) + SiLU + q/k L2 norm + gates, for M tokens of requests of L positions.
-clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const float* ab, const __half* conv_w,
-                            const __half* A_log, const __half* dt_bias, __half* q, __half* k,
-                            __half* v, float* g, float* beta, int64_t M, int64_t L,
-                            cudaStream_t stream);
+// conv(4) + SiLU + q/k L2 norm, for M tokens of requests of L positions.
+clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
+                            __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream);
 
 size_t gdn_scan_workspace_bytes(int64_t B, int64_t L);
 

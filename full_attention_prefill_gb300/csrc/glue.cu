@@ -1,5 +1,5 @@
 // Memory-bound glue of the decoder: embedding gather, RMSNorm, and the small fp16 gate
-// projections a, b of the Gated DeltaNet layers.
+// projections a, b of the Gated DeltaNet layers with the gates computed in their epilogue.
 //
 // "clef-flash-LiteRT" README, "Host contract" step 4: the input rows are the embedding table's
 // rows at the request's ids; step 6: the output is the hidden state after the final RMSNorm.
@@ -93,7 +93,10 @@ struct AbSmem {
 
 __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__ xn,
                                                       const __half* __restrict__ wab,
-                                                      float* __restrict__ ab, int64_t M) {
+                                                      const __half* __restrict__ A_log,
+                                                      const __half* __restrict__ dt_bias,
+                                                      float* __restrict__ g,
+                                                      float* __restrict__ beta, int64_t M) {
   __shared__ __align__(16) AbSmem s;
   const int64_t t0 = (int64_t)blockIdx.x * AB_T;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -132,14 +135,27 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
   }
   cp_async_wait<0>();
   const int gq = lane >> 2, tq = lane & 3;
+  // gates of the 32 value heads: columns 0..31 are a, 32..63 are b
+  //   g = log(alpha) = -exp(A_log) softplus(a + dt_bias) (clamped at -30),  beta = sigmoid(b)
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     const int64_t tok = t0 + warp * 16 + gq + hf * 8;
     if (tok >= M) continue;
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
-      *reinterpret_cast<float2*>(ab + tok * 64 + n * 8 + 2 * tq) =
-          make_float2(acc[n][2 * hf], acc[n][2 * hf + 1]);
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = n * 8 + 2 * tq + e;
+        const float v = acc[n][2 * hf + e];
+        if (col < 32) {
+          const float a = v + __half2float(dt_bias[col]);
+          const float sp = a > 20.f ? a : log1pf(__expf(a));
+          g[tok * 32 + col] = fmaxf(-__expf(__half2float(A_log[col])) * sp, -30.f);
+        } else {
+          beta[tok * 32 + col - 32] = sigmoid_f(v);
+        }
+      }
+    }
   }
 }
 
@@ -163,12 +179,13 @@ clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M
   return CLEF_OK;
 }
 
-clef_status ab_proj_launch(const __half* xn, const __half* w_ab, float* ab, int64_t M,
+clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A_log,
+                           const __half* dt_bias, float* g, float* beta, int64_t M,
                            cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
-  glue::ab_proj_kernel<<<(unsigned)((M + glue::AB_T - 1) / glue::AB_T), 128, 0, stream>>>(xn, w_ab,
-                                                                                         ab, M);
+  glue::ab_proj_kernel<<<(unsigned)((M + glue::AB_T - 1) / glue::AB_T), 128, 0, stream>>>(
+      xn, w_ab, A_log, dt_bias, g, beta, M);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

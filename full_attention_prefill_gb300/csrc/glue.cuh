@@ -13,8 +13,10 @@ clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab,
 clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
                            cudaStream_t stream);
 
-// ab [M, 64] fp32 = xn [M, 4096] . W_ab^T, W_ab [64, 4096] fp16 (tensor cores).
-clef_status ab_proj_launch(const __half* xn, const __half* w_ab, float* ab, int64_t M,
+// [a | b] = xn [M, 4096] . W_ab^T, W_ab [64, 4096] fp16 (tensor cores), then the GDN gates
+// g [M, 32] = log(alpha) = -exp(A_log) softplus(a + dt_bias) (>= -30), beta [M, 32] = sigmoid(b).
+clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A_log,
+                           const __half* dt_bias, float* g, float* beta, int64_t M,
                            cudaStream_t stream);
 
 }  // namespace clef
