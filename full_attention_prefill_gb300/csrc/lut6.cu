@@ -8,7 +8,7 @@
 //   * one CTA per 256 (tokens) x 128 (output channels) tile, K walked in blocks of 64;
 //   * warp 0 issues TMA loads of the X tile (256 rows, 128-byte swizzle) and of the packed
 //     index tile (128 rows x 48 bytes) into a 4-stage ring;
-//   * warps 4..11 turn the packed tile into the fp16 weight tile in shared memory: each lane
+//   * warps 4..19 turn the packed tile into the fp16 weight tile in shared memory: each lane
 //     unpacks 16 indices from 12 bytes (index*2 is cut out and OR'd into its table's address in
 //     one logic op) and looks them up in its group's 64-entry table, which sits in 128 bytes =
 //     one entry pair per bank, so a warp (8 rows of one 16-row group) never conflicts; the tile
@@ -16,7 +16,7 @@
 //   * warp 1 issues two tcgen05.mma per K=16 step (M=128 each, N=128, fp16 x fp16 -> fp32), one
 //     per 128-token half, both reading the same weight tile, into two 128 x 128 fp32
 //     accumulators in tensor memory: each dequantised weight serves 256 tokens;
-//   * warps 4..11 then read the accumulators with tcgen05.ld and run the fused epilogue (fp16
+//   * warps 4..19 then read the accumulators with tcgen05.ld and run the fused epilogue (fp16
 //     or fp32 store, fp32 residual add, or SwiGLU of an interleaved gate/up tile).
 // The dense weight never reaches global memory.
 #include <stdarg.h>
@@ -37,7 +37,7 @@ constexpr int W_BYTES = BN * BK * 2;          // 16 KB
 constexpr int P_ROW = BK * 3 / 4;             // 48 packed bytes per row per k-block
 constexpr int P_BYTES = BN * P_ROW;           // 6 KB
 constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the tile's rows
-constexpr int NUM_DQ_WARPS = 8;
+constexpr int NUM_DQ_WARPS = 16;
 constexpr int NUM_THREADS = 32 * (4 + NUM_DQ_WARPS);
 constexpr int TMEM_COLS = 256;                // two 128-column fp32 accumulators
 
@@ -183,9 +183,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- dequant, then epilogue
-    const int dq = warp - 4;              // 0..7
-    const int t = threadIdx.x - 128;      // 0..255
-    {
+    const int dq = warp - 4;              // 0..15
+    const int t = threadIdx.x - 128;      // 0..511
+    if (t < 256) {
       // the tile's 8 tables (rows n0 .. n0+127); groups past N read as zero
       const int e = t * 2;
       const int g = n0 / 16 + e / 64;
@@ -226,17 +226,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_wready + 8 * s);
     }
-    // ---- epilogue: warps 4..7 drain accumulator 0 (tokens 0..127), warps 8..11 accumulator 1
+    // ---- epilogue: warp dq drains accumulator (dq >> 2) & 1 (tokens 0..127 or 128..255),
+    //      TMEM lanes 32 (dq & 3).., columns 64 (dq >> 3) .. +63
     if (ok && mbar_wait(bar_acc, 0, status, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
       const int quarter = warp & 3;
-      const int half = dq >> 2;
+      const int half = (dq >> 2) & 1;
+      const int chalf = dq >> 3;
       const int row = m0 + half * 128 + quarter * 32 + lane;
       const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + half * BN;
       if (mode == EPI_SWIGLU_F16) {
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int j0 = c * 32;
+        {
+          const int j0 = chalf * 32;
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(tl + j0, g);
           tmem_ld_32x32b_x32(tl + BN / 2 + j0, u);
@@ -260,8 +261,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = c * 32;
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = chalf * 64 + c * 32;
           uint32_t r[32];
           tmem_ld_32x32b_x32(tl + col0, r);
           tc_wait_ld();
