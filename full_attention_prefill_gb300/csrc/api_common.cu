@@ -67,28 +67,41 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-cudaError_t tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
-                          uint32_t box_outer, CUtensorMapSwizzle swz) {
+cudaError_t tma_encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return cudaErrorNotSupported;
   }
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_stride_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t d[5];
+  cuuint64_t st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    set_error("cuTensorMapEncodeTiled failed (%d): dims %llu x %llu, stride %llu, box %u x %u", (int)r,
-              (unsigned long long)inner, (unsigned long long)outer,
-              (unsigned long long)row_stride_bytes, box_inner, box_outer);
+    set_error("cuTensorMapEncodeTiled failed (%d): rank %d, dims %llu x %llu, box %u x %u", (int)r,
+              rank, (unsigned long long)dims[0], (unsigned long long)dims[1], box[0], box[1]);
     return cudaErrorInvalidValue;
   }
   return cudaSuccess;
+}
+
+cudaError_t tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                          uint32_t box_outer, CUtensorMapSwizzle swz) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {row_stride_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return tma_encode(map, dt, 2, base, dims, strides, box, swz);
 }
 
 // host-side fault hook (tests of error paths without any GPU fault)

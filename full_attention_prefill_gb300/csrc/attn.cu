@@ -8,12 +8,11 @@
 //
 //   rope_kernel   rotates dims 0..63 of every q and k head (rotate-half pairs (j, j+32), angle
 //                 pos * 1e7^(-j/32), computed in fp64), in place or into a copy.
-//   flash_kernel  one CTA = 32 positions x the 4 query heads of one kv head (128 rows), so each
-//                 K/V tile is read once for the group; online softmax over 64-key tiles
-//                 (tensor-core mma.sync, fp32 accumulation); epilogue o * sigmoid(gate).
+//   flash_tc_kernel  one CTA = 32 positions x the 4 query heads of one kv head (128 rows), so
+//                 each K/V tile is read once for the group; tcgen05 MMAs with S and O in tensor
+//                 memory; online softmax over 64-key tiles; epilogue o * sigmoid(gate).
 #include "attn.cuh"
 #include "common.cuh"
-#include "mma.cuh"
 
 namespace clef {
 namespace attn {
@@ -22,9 +21,6 @@ constexpr int D = 256;
 constexpr int HQ = 16, HKV = 4;
 constexpr int BM = 128;            // rows per CTA = 32 positions x 4 heads
 constexpr int POS = BM / 4;        // positions per CTA
-constexpr int BN = 64;             // keys per tile
-constexpr int LDS = D + 8;         // padded smem row (528 bytes)
-constexpr int THREADS = 256;
 
 __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qin, int64_t ldqi,
                                                    __half* __restrict__ qout, int64_t ldqo,
@@ -77,179 +73,246 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
   }
 }
 
-struct FlashSmem {
-  __half Q[BM][LDS];
-  __half K[2][BN][LDS];
-  __half V[2][BN][LDS];
-};
+// ------------------------------------------------------------------------------------------
+// tcgen05 flash attention.  CTA = 128 rows (32 positions x the 4 query heads of kv head g), keys
+// in tiles of 64, two K/V stages.
+//   warp 0   TMA: Q once (4 boxes of 64 dims, 128-byte swizzle), then K and V tiles
+//   warp 1   MMA: S_j = Q K_j^T (M=128, N=64, 16 steps of K=16) into one of two 64-column
+//            TMEM buffers; O += P_{j-1} V_{j-1} (M=128, N=256, K=64) with P read from TMEM and
+//            V an MN-major shared operand; O is a 256-column fp32 TMEM accumulator
+//   warps 4-7 softmax, one thread per row: read S, mask, online max/sum in base 2, write P
+//            (fp16) over the first 32 columns of its S buffer.  O is rescaled (in TMEM) only
+//            when a row's max grows by more than 2^8, so P stays below 256; the final O is
+//            divided by the row sum, multiplied by sigmoid(gate) and stored.
+// ------------------------------------------------------------------------------------------
+constexpr int TBN = 64;                   // keys per tile
+constexpr int Q_BYTES = BM * D * 2;       // 64 KB: 4 blocks [128 rows][64 dims]
+constexpr int KV_BYTES = TBN * D * 2;     // 32 KB: 4 blocks [64 keys][64 dims]
+constexpr int KV_BLOCK = TBN * 128;       // 8 KB
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+constexpr int OFF_SLOT = OFF_BAR + 16 * 8;
+constexpr int FLASH_SMEM = OFF_SLOT + 16 + 1024;
+constexpr int FLASH_THREADS = 256;
+constexpr uint32_t S_COL = 256;           // S/P buffers at TMEM columns 256 and 320
+constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 units)
 
-__device__ __forceinline__ void load_kv(FlashSmem& s, int buf, const __half* __restrict__ k,
-                                        int64_t ldk, const __half* __restrict__ v, int64_t ldv,
-                                        int64_t tb, int key0, int L, int g, int tid) {
-  for (int i = tid; i < BN * (D / 8); i += THREADS) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    const int key = key0 + r;
-    const bool ok = key < L;
-    const int64_t row = tb + (ok ? key : 0);
-    cp_async16(smem_u32(&s.K[buf][r][c8]), k + row * ldk + g * D + c8, ok);
-    cp_async16(smem_u32(&s.V[buf][r][c8]), v + row * ldv + g * D + c8, ok);
-  }
-  cp_async_commit();
-}
-
-__global__ void __launch_bounds__(THREADS, 1) flash_kernel(
-    const __half* __restrict__ q, int64_t ldq, const __half* __restrict__ k, int64_t ldk,
-    const __half* __restrict__ v, int64_t ldv, const __half* __restrict__ gate, int64_t ldg,
-    __half* __restrict__ out, int64_t ldo, int L) {
-  extern __shared__ __align__(16) uint8_t smraw[];
-  FlashSmem& s = *reinterpret_cast<FlashSmem*>(smraw);
-  // heavy (late) position blocks first
-  const int pblk = gridDim.x - 1 - blockIdx.x;
+__global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __grid_constant__ CUtensorMap tv, const __half* __restrict__ gate, int64_t ldg,
+    __half* __restrict__ out, int64_t ldo, int L, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pblk = gridDim.x - 1 - blockIdx.x;  // heavy (late) position blocks first
   const int p0 = pblk * POS;
   const int g = blockIdx.y % HKV;
   const int b = blockIdx.y / HKV;
-  const int64_t tb = (int64_t)b * L;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-
-  // Q rows: row r = 4 * (position - p0) + (query head - 4g)
-  for (int i = tid; i < BM * (D / 8); i += THREADS) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    const int p = p0 + (r >> 2);
-    const bool ok = p < L;
-    const int64_t row = tb + (ok ? p : 0);
-    cp_async16(smem_u32(&s.Q[r][c8]), q + row * ldq + (4 * g + (r & 3)) * D + c8, ok);
-  }
-  cp_async_commit();
+  const int tb = b * L;
   const int last_pos = min(p0 + POS, L) - 1;
-  const int ntiles = last_pos / BN + 1;
-  load_kv(s, 0, k, ldk, v, ldv, tb, 0, L, g, tid);
+  const int nt = last_pos / TBN + 1;
 
-  // this thread's two rows
-  const int r_lo = warp * 16 + gq, r_hi = r_lo + 8;
-  const int pos_lo = p0 + (r_lo >> 2), pos_hi = p0 + (r_hi >> 2);
-  const float sl2 = 0.0625f * 1.4426950408889634f;  // softmax scale 1/sqrt(256), base 2
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  float o[32][4];
-#pragma unroll
-  for (int n = 0; n < 32; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  const uint32_t sQ = smem_u32(&s.Q[0][0]);
+  const uint32_t bar_q = sb + OFF_BAR;
+  const uint32_t bar_k = bar_q + 8;         // [2]
+  const uint32_t bar_v = bar_q + 24;        // [2]
+  const uint32_t bar_empty = bar_q + 40;    // [2]
+  const uint32_t bar_s = bar_q + 56;        // [2]
+  const uint32_t bar_p = bar_q + 72;        // [2]
+  const uint32_t bar_o = bar_q + 88;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
-  for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < ntiles)
-      load_kv(s, buf ^ 1, k, ldk, v, ldv, tb, (t + 1) * BN, L, g, tid);
-    else
-      cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const int key0 = t * BN;
-    const uint32_t sK = smem_u32(&s.K[buf][0][0]);
-    const uint32_t sV = smem_u32(&s.V[buf][0][0]);
-    // S = Q K^T for this warp's 16 rows x 64 keys
-    float sc[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(a, a_addr(sQ, LDS, warp * 16, ks * 16, lane));
-#pragma unroll
-      for (int n = 0; n < 8; n += 2) {
-        uint32_t bq[4];
-        ldsm_x4(bq, bn_addr(sK, LDS, n * 8, ks * 16, lane));
-        mma16816(sc[n], a, bq[0], bq[1]);
-        mma16816(sc[n + 1], a, bq[2], bq[3]);
-      }
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_k + 8 * i, 1);
+      mbar_init(bar_v + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
+      mbar_init(bar_s + 8 * i, 1);
+      mbar_init(bar_p + 8 * i, 4);
     }
-    // causal mask + online softmax (base-2 exponent, scale folded in)
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int key = key0 + n * 8 + 2 * tq;
-      sc[n][0] = (key <= pos_lo) ? sc[n][0] * sl2 : -INFINITY;
-      sc[n][1] = (key + 1 <= pos_lo) ? sc[n][1] * sl2 : -INFINITY;
-      sc[n][2] = (key <= pos_hi) ? sc[n][2] * sl2 : -INFINITY;
-      sc[n][3] = (key + 1 <= pos_hi) ? sc[n][3] * sl2 : -INFINITY;
-      mx_lo = fmaxf(mx_lo, fmaxf(sc[n][0], sc[n][1]));
-      mx_hi = fmaxf(mx_hi, fmaxf(sc[n][2], sc[n][3]));
-    }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-    // rows whose keys are all masked so far keep m = -inf; use 0 as the reference then
-    const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-    const float ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-    const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    float rs_lo = 0.f, rs_hi = 0.f;
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const float e0 = exp2f(sc[n][0] - ref_lo), e1 = exp2f(sc[n][1] - ref_lo);
-      const float e2 = exp2f(sc[n][2] - ref_hi), e3 = exp2f(sc[n][3] - ref_hi);
-      rs_lo += e0 + e1;
-      rs_hi += e2 + e3;
-      const int j = n >> 1;
-      if ((n & 1) == 0) {
-        pa[j][0] = h2u(e0, e1);
-        pa[j][1] = h2u(e2, e3);
-      } else {
-        pa[j][2] = h2u(e0, e1);
-        pa[j][3] = h2u(e2, e3);
-      }
-    }
-    l_lo = l_lo * al_lo + rs_lo;
-    l_hi = l_hi * al_hi + rs_hi;
-#pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      o[n][0] *= al_lo; o[n][1] *= al_lo;
-      o[n][2] *= al_hi; o[n][3] *= al_hi;
-    }
-    // O += P V
-#pragma unroll
-    for (int ks = 0; ks < BN / 16; ++ks) {
-#pragma unroll
-      for (int n = 0; n < 32; n += 2) {
-        uint32_t bq[4];
-        ldsm_x4_t(bq, bk_addr(sV, LDS, n * 8, ks * 16, lane));
-        mma16816(o[n], pa[ks], bq[0], bq[1]);
-        mma16816(o[n + 1], pa[ks], bq[2], bq[3]);
-      }
-    }
-    __syncthreads();
+    mbar_init(bar_o, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
   }
-  cp_async_wait<0>();
-  // epilogue: normalise, gate, store
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
-  const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int r = hf ? r_hi : r_lo;
-    const int p = hf ? pos_hi : pos_lo;
-    if (p >= L) continue;
-    const float inv = hf ? inv_hi : inv_lo;
-    const int hq = 4 * g + (r & 3);
-    const int64_t row = tb + p;
-#pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      const int col = n * 8 + 2 * tq;
-      float a0 = o[n][2 * hf] * inv, a1 = o[n][2 * hf + 1] * inv;
-      if (gate) {
-        const float2 gf =
-            __half22float2(*reinterpret_cast<const __half2*>(gate + row * ldg + hq * D + col));
-        a0 *= sigmoid_f(gf.x);
-        a1 *= sigmoid_f(gf.y);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, Q_BYTES);
+      for (int blk = 0; blk < 4; ++blk)
+        tma_load_3d(sb + OFF_Q + blk * (BM * 128), &tq, bar_q, blk * 64, 4 * g, tb + p0);
+      for (int j = 0; j < nt; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(bar_empty + 8 * s, ((j >> 1) & 1) ^ 1, status, DEV_TIMEOUT_TMA))
+          break;
+        mbar_arrive_expect_tx(bar_k + 8 * s, KV_BYTES);
+        for (int blk = 0; blk < 4; ++blk)
+          tma_load_3d(sb + OFF_K + s * KV_BYTES + blk * KV_BLOCK, &tk, bar_k + 8 * s, blk * 64, g,
+                      tb + j * TBN);
+        mbar_arrive_expect_tx(bar_v + 8 * s, KV_BYTES);
+        for (int blk = 0; blk < 4; ++blk)
+          tma_load_3d(sb + OFF_V + s * KV_BYTES + blk * KV_BLOCK, &tv, bar_v + 8 * s, blk * 64, g,
+                      tb + j * TBN);
       }
-      *reinterpret_cast<uint32_t*>(out + row * ldo + hq * D + col) = h2u(a0, a1);
     }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16_f32(128, TBN);
+      constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
+      bool ok = mbar_wait(bar_q, 0, status, DEV_TIMEOUT_MMA);
+      auto issue_pv = [&](int jj) -> bool {
+        const int sp = jj & 1;
+        if (!mbar_wait(bar_p + 8 * sp, (jj >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
+            !mbar_wait(bar_v + 8 * sp, (jj >> 1) & 1, status, DEV_TIMEOUT_MMA))
+          return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TBN / 16; ++kk) {
+          const uint64_t bd = sdesc_mn_sw128(sb + OFF_V + sp * KV_BYTES + kk * 16 * 128, KV_BLOCK, 1024);
+          tc_mma_f16_ts(tmem, tmem + S_COL + sp * TBN + kk * 8, bd, idesc_o, (jj | kk) != 0);
+        }
+        tc_commit(bar_o);
+        tc_commit(bar_empty + 8 * sp);
+        return true;
+      };
+      for (int j = 0; j < nt && ok; ++j) {
+        const int s = j & 1;
+        ok = mbar_wait(bar_k + 8 * s, (j >> 1) & 1, status, DEV_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = sdesc_k_sw128(sb + OFF_Q + (kk >> 2) * (BM * 128) + (kk & 3) * 32);
+          const uint64_t bd =
+              sdesc_k_sw128(sb + OFF_K + s * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32);
+          tc_mma_f16_ss(tmem + S_COL + s * TBN, ad, bd, idesc_s, kk != 0);
+        }
+        tc_commit(bar_s + 8 * s);
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(nt - 1);
+    }
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // row of this thread
+    const int pos = p0 + (r >> 2);
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const float sl2 = 0.0625f * 1.4426950408889634f;  // 1/sqrt(256) in base 2
+    float m_ref = -INFINITY, lsum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(bar_s + 8 * s, (j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[64];
+      {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN, lo);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + 32, hi);
+      }
+      tc_wait_ld();
+      const int key0 = j * TBN;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TBN; ++c) {
+        float v = __uint_as_float(sv[c]) * sl2;
+        v = (key0 + c <= pos) ? v : -INFINITY;
+        sv[c] = __float_as_uint(v);
+        mt = fmaxf(mt, v);
+      }
+      const float m_new = fmaxf(m_ref, mt);
+      const bool need = m_new > m_ref + kRescale;
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // rescale this warp's O rows once the previous P V has landed
+        if (!mbar_wait(bar_o, (j - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = need ? exp2f(m_ref - m_new) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(tl + c0, ov);
+          tc_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * f);
+          tmem_st_32x32b_x32(tl + c0, ov);
+        }
+        tc_wait_st();
+        lsum *= f;
+      }
+      if (need) m_ref = m_new;
+      uint32_t pk[32];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < TBN / 2; ++c) {
+        const float e0 = exp2f(__uint_as_float(sv[2 * c]) - m_ref);
+        const float e1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_ref);
+        rs += e0 + e1;
+        pk[c] = pack_half2(e0, e1);
+      }
+      lsum += rs;
+      tmem_st_32x32b_x32(tl + S_COL + s * TBN, pk);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p + 8 * s);
+    }
+    // epilogue: wait for the last P V, then O / l * sigmoid(gate)
+    if (ok && mbar_wait(bar_o, (nt - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+      tc_fence_after();
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const int hq = 4 * g + (r & 3);
+      const int64_t row = (int64_t)tb + pos;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tl + c0, ov);
+        tc_wait_ld();
+        if (pos < L) {
+          uint32_t pkd[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float a0 = __uint_as_float(ov[2 * c]) * inv, a1 = __uint_as_float(ov[2 * c + 1]) * inv;
+            if (gate) {
+              const float2 gf = __half22float2(
+                  *reinterpret_cast<const __half2*>(gate + row * ldg + hq * D + c0 + 2 * c));
+              a0 *= sigmoid_f(gf.x);
+              a1 *= sigmoid_f(gf.y);
+            }
+            pkd[c] = pack_half2(a0, a1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(out + row * ldo + hq * D + c0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -272,16 +335,37 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
   if (B == 0 || L == 0) return CLEF_OK;
   static bool attr = false;
   if (!attr) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(attn::flash_kernel,
+    CLEF_CUDA_CHECK(cudaFuncSetAttribute(attn::flash_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         sizeof(attn::FlashSmem)));
+                                         attn::FLASH_SMEM));
     attr = true;
+  }
+  const uint64_t M = (uint64_t)(B * L);
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[3] = {256, 16, M};
+    const uint64_t st[2] = {512, (uint64_t)ldq * 2};
+    const uint32_t box[3] = {64, 4, attn::POS};
+    if (tma_encode(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, st, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+      return CLEF_E_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {256, 4, M};
+    const uint32_t box[3] = {64, 1, attn::TBN};
+    const uint64_t stk[2] = {512, (uint64_t)ldk * 2};
+    const uint64_t stv[2] = {512, (uint64_t)ldv * 2};
+    if (tma_encode(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, stk, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+        tma_encode(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v, dims, stv, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+      return CLEF_E_CUDA;
   }
   dim3 grid((unsigned)((L + attn::POS - 1) / attn::POS), (unsigned)(B * attn::HKV));
   TraceScope ts(stream, "flash_attn", 4.0 * attn::D * attn::HQ * (double)B * L * (L + 1) / 2.0,
                 (double)B * L * (16 + 4 + 4 + 16 + 16) * attn::D * 2.0);
-  attn::flash_kernel<<<grid, attn::THREADS, sizeof(attn::FlashSmem), stream>>>(
-      q, ldq, k, ldk, v, ldv, gate, ldg, out, ldo, (int)L);
+  attn::flash_tc_kernel<<<grid, attn::FLASH_THREADS, attn::FLASH_SMEM, stream>>>(
+      mq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

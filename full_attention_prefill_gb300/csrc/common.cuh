@@ -29,6 +29,10 @@ unsigned* status_word_ptr();          // device address of the status word (host
 cudaError_t tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                           uint32_t box_outer, CUtensorMapSwizzle swz);
+// rank-N tiled tensor map (dims innermost first; strides_bytes[i] = stride of dim i+1)
+cudaError_t tma_encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swz);
 const char* set_error(const char* fmt, ...);
 int num_sms();
 bool debug_should_fail();            // host-side fault hook (clef_debug_fail_next)
@@ -228,6 +232,19 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+// 32 lanes x 32 consecutive 32-bit columns written from registers.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 // 32 lanes x 16 consecutive 32-bit columns written from registers.
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
