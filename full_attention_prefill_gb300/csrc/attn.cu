@@ -239,13 +239,17 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       }
       const float m_new = fmaxf(m_ref, mt);
       const bool need = m_new > m_ref + kRescale;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale this warp's O rows once the previous P V has landed
+      // P_j may only be published once P_{j-1} V_{j-1} has landed in O (tested: publishing it
+      // while that MMA is in flight corrupts O)
+      if (j > 0) {
         if (!mbar_wait(bar_o, (j - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
           ok = false;
           break;
         }
         tc_fence_after();
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // rescale this warp's O rows
         const float f = need ? exp2f(m_ref - m_new) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
