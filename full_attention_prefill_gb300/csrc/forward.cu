@@ -37,6 +37,7 @@ struct FwdWs {
   __half* v;
   float* g;
   float* beta;
+  float* abpart;
   __half* mix;
   __half* h;
   void* scan;
@@ -60,6 +61,7 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
   t.v = static_cast<__half*>(take(M * 4096 * 2));
   t.g = static_cast<float*>(take(M * 32 * 4));
   t.beta = static_cast<float*>(take(M * 32 * 4));
+  t.abpart = static_cast<float*>(take(ab_proj_scratch_bytes(M)));
   t.mix = static_cast<__half*>(take(M * H * 2));
   t.h = static_cast<__half*>(take(M * I * 2));
   t.scan = take(gdn_scan_workspace_bytes(B, L));
@@ -84,7 +86,8 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
                               EPI_F16, s));
     CLEF_TRY(ab_proj_launch(w.xn, reinterpret_cast<const __half*>(ly.ab_w),
                             reinterpret_cast<const __half*>(ly.A_log),
-                            reinterpret_cast<const __half*>(ly.dt_bias), w.g, w.beta, M, s));
+                            reinterpret_cast<const __half*>(ly.dt_bias), w.g, w.beta, w.abpart, M,
+                            s));
     CLEF_TRY(gdn_prep_launch(w.proj, GDN_PROJ, reinterpret_cast<const __half*>(ly.conv_w), w.q,
                              w.k, w.v, M, L, s));
     CLEF_TRY(gdn_scan_launch(w.q, w.k, w.v, w.g, nullptr, w.beta, nullptr, nullptr,

@@ -36,12 +36,12 @@ constexpr float kLogAlphaMin = -30.0f;
 
 // ------------------------------------------------------------------------------------------
 // Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels and
-// the per-head L2 norm of q and k.  A CTA walks 64 consecutive tokens for 2048 channels (256
-// threads x 8 channels); each thread keeps the last three inputs of its channels in registers,
-// so every input is read once.  The gates come from the a/b projection's epilogue.
+// the per-head L2 norm of q and k.  A CTA covers 16 consecutive tokens for 2048 channels (256
+// threads x 8 channels); each thread issues the loads of all 19 rows it needs at once and keeps
+// them in registers.  The gates come from the a/b projection's epilogue.
 // proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..).
 // ------------------------------------------------------------------------------------------
-constexpr int PREP_T = 64;
+constexpr int PREP_T = 16;
 __global__ void __launch_bounds__(256) gdn_prep_kernel(
     const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
     __half* __restrict__ q, __half* __restrict__ k, __half* __restrict__ v, int64_t M, int L) {
@@ -59,42 +59,39 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
       for (int j = 0; j < 8; ++j) w[(i * 8 + j) / 4][(i * 8 + j) % 4] = __half2float(hh[j]);
     }
   }
-  auto load8 = [&](int64_t tok, float (&x)[8]) {
-    uint4 u = *reinterpret_cast<const uint4*>(proj + tok * ldp + ch0);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+  // rows tok0 - 3 .. tok0 + PREP_T - 1, all loads in flight at once; rows before the start of
+  // their request or past M are zero
+  uint4 xr[PREP_T + 3];
+  const int pos0 = (int)(tok0 % L);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __half22float2(h2[j]);
-      x[2 * j] = f.x;
-      x[2 * j + 1] = f.y;
-    }
-  };
-  // history x[t-1], x[t-2], x[t-3] of the first token (zero before its request's start)
-  float h1[8], h2[8], h3[8];
-  {
-    const int pos0 = (int)(tok0 % L);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) h1[c] = h2[c] = h3[c] = 0.f;
-    if (pos0 >= 1) load8(tok0 - 1, h1);
-    if (pos0 >= 2) load8(tok0 - 2, h2);
-    if (pos0 >= 3) load8(tok0 - 3, h3);
+  for (int i = 0; i < PREP_T + 3; ++i) {
+    const int64_t tok = tok0 - 3 + i;
+    const bool ok = (i >= 3 || pos0 >= 3 - i) && tok < M;
+    xr[i] = ok ? *reinterpret_cast<const uint4*>(proj + tok * ldp + ch0) : make_uint4(0, 0, 0, 0);
   }
-  const int64_t tend = (tok0 + PREP_T < M) ? tok0 + PREP_T : M;
-  for (int64_t tok = tok0; tok < tend; ++tok) {
-    if (tok % L == 0) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) h1[c] = h2[c] = h3[c] = 0.f;
-    }
-    float x[8], y[8];
-    load8(tok, x);
+  for (int i = 0; i < PREP_T; ++i) {
+    const int64_t tok = tok0 + i;
+    if (tok >= M) break;
+    const int pos = (int)(tok % L);
+    float y[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      // tap j multiplies x[t - 3 + j]
-      const float pre = w[c][0] * h3[c] + w[c][1] * h2[c] + w[c][2] * h1[c] + w[c][3] * x[c];
-      y[c] = silu_f(pre);
-      h3[c] = h2[c];
-      h2[c] = h1[c];
-      h1[c] = x[c];
+    for (int c2 = 0; c2 < 4; ++c2) {
+      float2 xs[4];
+#pragma unroll
+      for (int tap = 0; tap < 4; ++tap) {
+        // tap j multiplies x[t - 3 + j]; positions before the request's start are zero
+        const uint4 u = xr[i + tap];
+        const __half2 hv = reinterpret_cast<const __half2*>(&u)[c2];
+        xs[tap] = (pos - 3 + tap >= 0) ? __half22float2(hv) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = 2 * c2 + e;
+        const float pre = w[c][0] * (e ? xs[0].y : xs[0].x) + w[c][1] * (e ? xs[1].y : xs[1].x) +
+                          w[c][2] * (e ? xs[2].y : xs[2].x) + w[c][3] * (e ? xs[3].y : xs[3].x);
+        y[c] = silu_f(pre);
+      }
     }
     __half* dst;
     if (ch0 < 4096) {
@@ -138,6 +135,8 @@ struct WySmem {
   float A[C][C + 4];    // 16-byte aligned rows for broadcast float4 reads
   float gc[C];
   float bt[C];
+  float eb[C];         // beta_r exp(g_r)
+  float ed[C];         // exp(g_C - g_r)
 };
 
 __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
@@ -218,10 +217,15 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   }
   // scaled operands for W and U', and the decayed keys exp(g_C - g_r) k_r the state pass uses
   const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
+  if (tid < C) {
+    s.eb[tid] = s.bt[tid] * __expf(s.gc[tid]);
+    s.ed[tid] = __expf(gC - s.gc[tid]);
+  }
+  __syncthreads();
   for (int i = tid; i < C * (D / 2); i += 128) {
     const int r = i / (D / 2), c2 = (i % (D / 2)) * 2;
-    const float eb = s.bt[r] * __expf(s.gc[r]);
-    const float ed = __expf(gC - s.gc[r]);
+    const float eb = s.eb[r];
+    const float ed = s.ed[r];
     const float2 kf = __half22float2(*reinterpret_cast<const __half2*>(&s.K[r][c2]));
     const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&s.V[r][c2]));
     *reinterpret_cast<__half2*>(&s.KB[r][c2]) = __floats2half2_rn(eb * kf.x, eb * kf.y);

@@ -91,14 +91,32 @@ struct AbSmem {
   __half W[2][64][AB_LD];
 };
 
+// Gates from the summed projections: g = -exp(A_log) softplus(a + dt_bias) (>= -30), beta = sigmoid(b).
+__device__ __forceinline__ void write_gate(int64_t tok, int col, float v, const __half* A_log,
+                                           const __half* dt_bias, float* g, float* beta) {
+  if (col < 32) {
+    const float a = v + __half2float(dt_bias[col]);
+    const float sp = a > 20.f ? a : log1pf(__expf(a));
+    g[tok * 32 + col] = fmaxf(-__expf(__half2float(A_log[col])) * sp, -30.f);
+  } else {
+    beta[tok * 32 + col - 32] = sigmoid_f(v);
+  }
+}
+
+// blockIdx.y = slice of K (gridDim.y slices).  With one slice the epilogue computes the gates;
+// otherwise it writes its partial sums to part [slice][M][64] for ab_gates_kernel.
 __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__ xn,
                                                       const __half* __restrict__ wab,
                                                       const __half* __restrict__ A_log,
                                                       const __half* __restrict__ dt_bias,
                                                       float* __restrict__ g,
-                                                      float* __restrict__ beta, int64_t M) {
+                                                      float* __restrict__ beta,
+                                                      float* __restrict__ part, int64_t M) {
   __shared__ __align__(16) AbSmem s;
   const int64_t t0 = (int64_t)blockIdx.x * AB_T;
+  const int nkb_all = H / AB_K;
+  const int kb0 = blockIdx.y * nkb_all / gridDim.y;
+  const int kb1 = (blockIdx.y + 1) * nkb_all / gridDim.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto load = [&](int buf, int kb) {
     for (int i = tid; i < AB_T * (AB_K / 8); i += 128) {
@@ -112,13 +130,13 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
   float acc[8][4];
 #pragma unroll
   for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  constexpr int NKB = H / AB_K;
-  load(0, 0);
-  for (int kb = 0; kb < NKB; ++kb) {
-    if (kb + 1 < NKB) load((kb + 1) & 1, kb + 1); else cp_async_commit();
+  load(0, kb0);
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const int buf = (kb - kb0) & 1;
+    if (kb + 1 < kb1) load(buf ^ 1, kb + 1); else cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
-    const uint32_t sX = smem_u32(&s.X[kb & 1][0][0]), sW = smem_u32(&s.W[kb & 1][0][0]);
+    const uint32_t sX = smem_u32(&s.X[buf][0][0]), sW = smem_u32(&s.W[buf][0][0]);
 #pragma unroll
     for (int ks = 0; ks < AB_K / 16; ++ks) {
       uint32_t a[4];
@@ -136,27 +154,33 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
   cp_async_wait<0>();
   const int gq = lane >> 2, tq = lane & 3;
   // gates of the 32 value heads: columns 0..31 are a, 32..63 are b
-  //   g = log(alpha) = -exp(A_log) softplus(a + dt_bias) (clamped at -30),  beta = sigmoid(b)
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     const int64_t tok = t0 + warp * 16 + gq + hf * 8;
     if (tok >= M) continue;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = n * 8 + 2 * tq + e;
-        const float v = acc[n][2 * hf + e];
-        if (col < 32) {
-          const float a = v + __half2float(dt_bias[col]);
-          const float sp = a > 20.f ? a : log1pf(__expf(a));
-          g[tok * 32 + col] = fmaxf(-__expf(__half2float(A_log[col])) * sp, -30.f);
-        } else {
-          beta[tok * 32 + col - 32] = sigmoid_f(v);
-        }
+      const int col = n * 8 + 2 * tq;
+      if (gridDim.y == 1) {
+        write_gate(tok, col, acc[n][2 * hf], A_log, dt_bias, g, beta);
+        write_gate(tok, col + 1, acc[n][2 * hf + 1], A_log, dt_bias, g, beta);
+      } else {
+        *reinterpret_cast<float2*>(part + ((int64_t)blockIdx.y * M + tok) * 64 + col) =
+            make_float2(acc[n][2 * hf], acc[n][2 * hf + 1]);
       }
     }
   }
+}
+
+// Sums the K-slice partials in slice order (deterministic) and writes the gates.
+__global__ void ab_gates_kernel(const float* __restrict__ part, int slices,
+                                const __half* __restrict__ A_log, const __half* __restrict__ dt_bias,
+                                float* __restrict__ g, float* __restrict__ beta, int64_t M) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= M * 64) return;
+  float v = 0.f;
+  for (int sl = 0; sl < slices; ++sl) v += part[sl * M * 64 + i];
+  write_gate(i / 64, (int)(i % 64), v, A_log, dt_bias, g, beta);
 }
 
 }  // namespace glue
@@ -179,14 +203,25 @@ clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M
   return CLEF_OK;
 }
 
+size_t ab_proj_scratch_bytes(int64_t M) { return (size_t)kAbMaxSlices * M * 64 * 4; }
+
 clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A_log,
-                           const __half* dt_bias, float* g, float* beta, int64_t M,
+                           const __half* dt_bias, float* g, float* beta, float* part, int64_t M,
                            cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
+  const int64_t ctas = (M + glue::AB_T - 1) / glue::AB_T;
+  // split K when there are too few token blocks to fill the GPU (partials summed in order)
+  int slices = 1;
+  while (slices < kAbMaxSlices && ctas * slices * 2 <= num_sms()) slices *= 2;
   TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
-  glue::ab_proj_kernel<<<(unsigned)((M + glue::AB_T - 1) / glue::AB_T), 128, 0, stream>>>(
-      xn, w_ab, A_log, dt_bias, g, beta, M);
+  glue::ab_proj_kernel<<<dim3((unsigned)ctas, (unsigned)slices), 128, 0, stream>>>(
+      xn, w_ab, A_log, dt_bias, g, beta, part, M);
   CLEF_LAUNCH_CHECK();
+  if (slices > 1) {
+    glue::ab_gates_kernel<<<(unsigned)((M * 64 + 255) / 256), 256, 0, stream>>>(part, slices, A_log,
+                                                                              dt_bias, g, beta, M);
+    CLEF_LAUNCH_CHECK();
+  }
   return CLEF_OK;
 }
 

@@ -15,8 +15,12 @@ clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M
 
 // [a | b] = xn [M, 4096] . W_ab^T, W_ab [64, 4096] fp16 (tensor cores), then the GDN gates
 // g [M, 32] = log(alpha) = -exp(A_log) softplus(a + dt_bias) (>= -30), beta [M, 32] = sigmoid(b).
+// When M is small the K dimension is split over up to kAbMaxSlices CTAs per token block; their
+// partial sums go to `part` (ab_proj_scratch_bytes(M) bytes) and are added in a fixed order.
+constexpr int kAbMaxSlices = 8;
+size_t ab_proj_scratch_bytes(int64_t M);
 clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A_log,
-                           const __half* dt_bias, float* g, float* beta, int64_t M,
+                           const __half* dt_bias, float* g, float* beta, float* part, int64_t M,
                            cudaStream_t stream);
 
 }  // namespace clef
