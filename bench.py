@@ -318,8 +318,9 @@ def run_micro(args):
         x = torch.from_numpy(synth.normal_f16(0, "micro.x", 0, (M, K))).to(dev)
         packed, lut = synth.lut6_weight(0, "micro.w", 0, N, K)
         p, l = torch.from_numpy(packed).to(dev), torch.from_numpy(lut).to(dev)
+        p = clef.lut6_tile(p, K)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        fn = lambda: clef.lut6_gemm(x, p, l, out=y)  # noqa: E731
+        fn = lambda: clef.lut6_gemm(x, p, l, out=y, tiled=True)  # noqa: E731
         flops, desc = 2.0 * M * N * K, f"lut6_gemm M={M} N={N} K={K}"
     elif args.micro == "attn":
         L = args.L

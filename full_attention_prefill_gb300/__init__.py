@@ -76,6 +76,8 @@ _SIGS = {
     "clef_lut6_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "clef_lut6_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_void_p, ctypes.c_void_p]),
+    "clef_lut6_tile": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_void_p]),
     "clef_lut6_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p]),
@@ -171,11 +173,25 @@ def lut6_dequant(packed, lut, k, stream=None):
     return w
 
 
-def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None):
-    """Device: y = x . W^T for fp16 x [m, k] and LUT-6 W [n, k]; y fp16 (or fp32) [m, n]."""
+def lut6_tile(packed, k, stream=None):
+    """Device: the GEMM's tiled layout of a canonical packed LUT-6 weight [n, k*3/4]."""
+    _need_cuda(packed)
+    n = packed.shape[0]
+    tiled = torch.empty_like(packed)
+    _check(lib().clef_lut6_tile(_ptr(packed), n, k, _ptr(tiled), _stream(stream)), "clef_lut6_tile")
+    return tiled
+
+
+def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None, tiled=False):
+    """Device: y = x . W^T for fp16 x [m, k] and LUT-6 W [n, k]; y fp16 (or fp32) [m, n].
+
+    `packed` is the canonical [n, k*3/4] stream, tiled here first, or (tiled=True) already in
+    the GEMM layout of lut6_tile."""
     _need_cuda(x, packed, lut)
     m, k = x.shape
     n = lut.shape[0] * 16
+    if not tiled and k % 64 == 0 and n % 16 == 0:
+        packed = lut6_tile(packed, k, stream)
     if out is None:
         out = torch.empty((m, n), dtype=torch.float32 if out_fp32 else torch.float16, device=x.device)
     _check(lib().clef_lut6_gemm(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out), 1 if out_fp32 else 0,

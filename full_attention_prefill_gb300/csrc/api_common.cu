@@ -294,6 +294,21 @@ clef_status clef_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_
                              reinterpret_cast<__half*>(w), static_cast<cudaStream_t>(stream));
 }
 
+clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
+                           clef_stream stream) {
+  if (!packed || !tiled || n < 0 || k < 0) {
+    set_error("clef_lut6_tile: NULL pointer or negative size");
+    return CLEF_E_INVALID;
+  }
+  if (n % 16 || k % 64) {
+    set_error("clef_lut6_tile: need n %% 16 == 0 and k %% 64 == 0 (n=%lld k=%lld)", (long long)n,
+              (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  return lut6_tile_launch(packed, n, k, tiled, static_cast<cudaStream_t>(stream));
+}
+
 clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,
                            int32_t y_is_fp32, int64_t m, int64_t n, int64_t k, clef_stream stream) {
   if (m < 0 || n <= 0 || k <= 0 || (y_is_fp32 != 0 && y_is_fp32 != 1)) {

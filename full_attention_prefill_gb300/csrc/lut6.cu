@@ -8,14 +8,15 @@
 // transposed product D[n, m] = W X^T so that the weights are the MMA's A operand, held in tensor
 // memory, and never pass through shared memory:
 //   * one CTA per 128 (output channels) x 256 (tokens) tile, K walked in blocks of 64;
-//   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and of the packed
-//     index tile (128 rows x 48 bytes) into a 4-stage ring;
+//   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and bulk copies
+//     of the 8 packed 768-byte blocks of the tile's rows (tiled layout, see clef_lut6_tile) into
+//     a 4-stage ring;
 //   * warps 4..11 dequantise: each warp owns one 16-row table group and writes its 16 x 64
 //     weights straight into a tensor-memory A stage with one tcgen05.st.16x256b.x4; every
 //     lookup of a warp hits the same 64-entry table (128 bytes, one entry pair per bank), so the
-//     lookups never conflict; each lane takes the packed quadruples its fragment needs out of
-//     two aligned words with one funnel shift, and cuts index*2 into the table address with one
-//     logic op per index;
+//     lookups never conflict; in the tiled layout the 32 indices a lane's fragment needs are 24
+//     contiguous bytes (three 8-byte loads), and index*2 is cut into the table address with one
+//     shift and one logic op per index;
 //   * warp 1 issues tcgen05.mma (M=128 channels from tensor memory, N=256 tokens from shared
 //     memory, K=16) into a 128 x 256 fp32 accumulator in tensor memory;
 //   * the epilogue (warps 4..11) drains the accumulator with tcgen05.ld into shared memory in
@@ -36,8 +37,8 @@ constexpr int BT = 256;                       // tokens per tile: MMA N (B opera
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int X_BYTES = BT * BK * 2;          // 32 KB
-constexpr int P_ROW = BK * 3 / 4;             // 48 packed bytes per row per k-block
-constexpr int P_BYTES = BN * P_ROW;           // 6 KB
+constexpr int P_BLOCK = 768;                  // packed bytes of one 16-row group per k-block
+constexpr int P_BYTES = (BN / 16) * P_BLOCK;  // 6 KB
 constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the tile's rows
 constexpr int NUM_DQ_WARPS = 8;               // one per 16-row group
 constexpr int NUM_THREADS = 32 * (4 + NUM_DQ_WARPS);
@@ -96,22 +97,42 @@ __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_
       : "memory");
 }
 
-// The packed quadruple q (indices 4q..4q+3 of a row, 24 bits at byte 3q) of a row starting at
-// shared address `row`, as four table addresses (index * 2 OR'd into the 128-byte aligned tb).
-__device__ __forceinline__ void quad_addrs(uint32_t row, int q, uint32_t tb, uint32_t (&a)[4]) {
-  const int off = 3 * q;
-  const uint32_t wa = row + (off & ~3);
-  const uint32_t lo = lds_u32(wa), hi = lds_u32(wa + 4);
-  const uint32_t w = __funnelshift_r(lo, hi, (off & 3) * 8);
-  a[0] = ((w << 1) & 0x7Eu) | tb;
-  a[1] = ((w >> 5) & 0x7Eu) | tb;
-  a[2] = ((w >> 11) & 0x7Eu) | tb;
-  a[3] = ((w >> 17) & 0x7Eu) | tb;
+// Table addresses of 16 indices of 6 bits taken from 96 bits (w0 | w1 << 32 | w2 << 64), LSB
+// first: index i sits at bits 6i..6i+5; (index * 2) is cut out and OR'd into the table base tb
+// (128-byte aligned), one shift and one logic op per index.
+__device__ __forceinline__ void table_addrs16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t tb,
+                                              uint32_t (&a)[16]) {
+  a[0] = ((w0 << 1) & 0x7Eu) | tb;
+  a[1] = ((w0 >> 5) & 0x7Eu) | tb;
+  a[2] = ((w0 >> 11) & 0x7Eu) | tb;
+  a[3] = ((w0 >> 17) & 0x7Eu) | tb;
+  a[4] = ((w0 >> 23) & 0x7Eu) | tb;
+  a[5] = (__funnelshift_r(w0, w1, 29) & 0x7Eu) | tb;
+  a[6] = ((w1 >> 3) & 0x7Eu) | tb;
+  a[7] = ((w1 >> 9) & 0x7Eu) | tb;
+  a[8] = ((w1 >> 15) & 0x7Eu) | tb;
+  a[9] = ((w1 >> 21) & 0x7Eu) | tb;
+  a[10] = (__funnelshift_r(w1, w2, 27) & 0x7Eu) | tb;
+  a[11] = ((w2 >> 1) & 0x7Eu) | tb;
+  a[12] = ((w2 >> 7) & 0x7Eu) | tb;
+  a[13] = ((w2 >> 13) & 0x7Eu) | tb;
+  a[14] = ((w2 >> 19) & 0x7Eu) | tb;
+  a[15] = ((w2 >> 25) & 0x7Eu) | tb;
+}
+__device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                     const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
+                     const uint8_t* __restrict__ tiled, const __half* __restrict__ lut,
                      void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
                      unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -139,7 +160,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_acc, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_x);
-    tma_prefetch_desc(&tmap_p);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -153,13 +173,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      const int ngroups = min(BN / 16, N / 16 - n0 / 16);  // groups of this tile inside N
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1;
         if (kb >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1, status, DEV_TIMEOUT_TMA)) break;
-        mbar_arrive_expect_tx(bar_full + 8 * s, X_BYTES + P_BYTES);
+        mbar_arrive_expect_tx(bar_full + 8 * s, X_BYTES + ngroups * P_BLOCK);
         tma_load_2d(sb + OFF_X + s * X_BYTES, &tmap_x, bar_full + 8 * s, kb * BK, m0);
-        tma_load_2d(sb + OFF_P + s * P_BYTES, &tmap_p, bar_full + 8 * s, kb * P_ROW, n0);
+        for (int gi = 0; gi < ngroups; ++gi)
+          bulk_load(sb + OFF_P + s * P_BYTES + gi * P_BLOCK,
+                    tiled + ((size_t)(n0 / 16 + gi) * num_kb + kb) * P_BLOCK, P_BLOCK,
+                    bar_full + 8 * s);
       }
     }
   } else if (warp == 1) {
@@ -198,8 +222,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     named_bar_sync(1, 32 * NUM_DQ_WARPS);
     const int quarter = warp & 3;         // TMEM lanes 32*quarter .. (this warp's access window)
     const int grp = 2 * quarter + (dq >> 2);          // 16-row group of this warp
-    const int r0 = grp * 16 + (lane >> 2);            // rows r0 and r0 + 8 of the group
-    const int u = lane & 3;
     const uint32_t tb = sb + OFF_T + grp * 128;
     const uint32_t tl = tmem + ((uint32_t)(grp * 16) << 16) + A_COL;
     bool ok = true;
@@ -212,19 +234,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = false;
         break;
       }
-      const uint32_t prow0 = sb + OFF_P + s * P_BYTES + r0 * P_ROW;
-      const uint32_t prow1 = prow0 + 8 * P_ROW;
+      // this lane's 24 bytes: quadruples j = 0..3 of row r0, then of row r0 + 8
+      const uint32_t pa = sb + OFF_P + s * P_BYTES + (grp & 7) * P_BLOCK + lane * 24;
+      uint32_t w[6];
+      lds_v2(pa, w[0], w[1]);
+      lds_v2(pa + 8, w[2], w[3]);
+      lds_v2(pa + 16, w[4], w[5]);
+      uint32_t a0[16], a1[16];
+      table_addrs16(w[0], w[1], w[2], tb, a0);
+      table_addrs16(w[3], w[4], w[5], tb, a1);
       uint32_t rg[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        // fragment block j holds k = 16j + 4u .. 16j + 4u + 3: packed quadruple 4j + u
-        uint32_t a0[4], a1[4];
-        quad_addrs(prow0, 4 * j + u, tb, a0);
-        quad_addrs(prow1, 4 * j + u, tb, a1);
-        rg[4 * j + 0] = lds_pair(a0[0], a0[1]);
-        rg[4 * j + 1] = lds_pair(a0[2], a0[3]);
-        rg[4 * j + 2] = lds_pair(a1[0], a1[1]);
-        rg[4 * j + 3] = lds_pair(a1[2], a1[3]);
+        // fragment block j holds k = 16j + 4u .. 16j + 4u + 3 of rows r0 and r0 + 8
+        rg[4 * j + 0] = lds_pair(a0[4 * j], a0[4 * j + 1]);
+        rg[4 * j + 1] = lds_pair(a0[4 * j + 2], a0[4 * j + 3]);
+        rg[4 * j + 2] = lds_pair(a1[4 * j], a1[4 * j + 1]);
+        rg[4 * j + 3] = lds_pair(a1[4 * j + 2], a1[4 * j + 3]);
       }
       tmem_st_16x256b_x4(tl + s * 32, rg);
       tc_wait_st();
@@ -320,19 +346,39 @@ __global__ void lut6_dequant_kernel(const uint8_t* __restrict__ packed, const __
   }
 }
 
+// Canonical packed [n, k*3/4] -> tiled: one thread per 3-byte quadruple of the output.
+//   tiled[((G * (k/64) + kb) * 32 + t) * 24 + 3 * (4h + j) + b]
+//     = packed[16G + t/4 + 8h][3 * (16kb + 4j + t%4) + b]
+__global__ void lut6_tile_kernel(const uint8_t* __restrict__ packed, int64_t n, int64_t k,
+                                 uint8_t* __restrict__ tiled) {
+  const int64_t quads = n * (k / 4);
+  const int64_t kbs = k / 64;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < quads;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int hj = (int)(q % 8);
+    const int t = (int)((q / 8) % 32);
+    const int64_t blk = q / 256;  // G * kbs + kb
+    const int64_t kb = blk % kbs, G = blk / kbs;
+    const int h = hj >> 2, j = hj & 3;
+    const int64_t row = 16 * G + t / 4 + 8 * h;
+    const int64_t src = row * (k / 4 * 3) + 3 * (16 * kb + 4 * j + t % 4);
+    uint8_t* d = tiled + q * 3;
+    d[0] = packed[src];
+    d[1] = packed[src + 1];
+    d[2] = packed[src + 2];
+  }
+}
+
 }  // namespace lut
 
-clef_status lut6_gemm_launch(const __half* x, const uint8_t* packed, const __half* lut, void* y,
+clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
                              cudaStream_t stream) {
   using namespace lut;
   if (M == 0) return CLEF_OK;
-  CUtensorMap tx, tp;
+  CUtensorMap tx;
   if (tma_encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)K, (uint64_t)M,
                     (uint64_t)K * 2, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
-    return CLEF_E_CUDA;
-  if (tma_encode_2d(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K * 3 / 4, (uint64_t)N,
-                    (uint64_t)K * 3 / 4, P_ROW, BN, CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
     return CLEF_E_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
@@ -348,7 +394,18 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* packed, const __hal
   TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
                 0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
   lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
+      tx, tiled, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status lut6_tile_launch(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
+                             cudaStream_t stream) {
+  const int64_t quads = n * (k / 4);
+  if (quads == 0) return CLEF_OK;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((quads + threads - 1) / threads, 65535LL * 8);
+  lut::lut6_tile_kernel<<<(unsigned)blocks, threads, 0, stream>>>(packed, n, k, tiled);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

@@ -11,10 +11,15 @@ enum Epilogue : int {
   EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up of a gate/up tile interleaved by 64 rows
 };
 
-// y[m, n] (row stride ldy elements) = x[m, k] . W^T.  Requires n % 16 == 0, k % 64 == 0
-// (and n % 128 == 0 for EPI_SWIGLU_F16); x packed [m, k].
-clef_status lut6_gemm_launch(const __half* x, const uint8_t* packed, const __half* lut, void* y,
+// y[m, n] (row stride ldy elements) = x[m, k] . W^T with W in the tiled layout
+// (clef_lut6_tile).  Requires n % 16 == 0, k % 64 == 0 (and n % 128 == 0 for EPI_SWIGLU_F16);
+// x packed [m, k].
+clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
+                             cudaStream_t stream);
+
+// canonical packed [n, k*3/4] -> tiled layout of the GEMM (same size)
+clef_status lut6_tile_launch(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
                              cudaStream_t stream);
 
 clef_status lut6_dequant_launch(const uint8_t* packed, const __half* lut, int64_t n, int64_t k,

@@ -3,8 +3,9 @@
 The layout is the C ABI's (include/clef.h, clef_layer / clef_model): per layer one fused input
 projection (GDN: q | k | v | z rows; attention: query | gate | k | v rows), the output
 projection, the MLP gate and up rows interleaved in blocks of 64, and the down projection, all
-LUT-6; GDN small weights fp16.  Building a layer only moves bytes (row blocks of the packed
-indices and their tables are concatenated or interleaved); no weight value changes.
+LUT-6 in the GEMM's tiled layout (clef_lut6_tile); GDN small weights fp16.  Building a layer only
+moves bytes (row blocks of the packed indices and their tables are concatenated or interleaved,
+then the quadruples are tiled); no weight value changes.
 """
 from __future__ import annotations
 
@@ -14,7 +15,7 @@ import numpy as np
 import torch
 
 from . import (HIDDEN, SWIGLU_BLOCK, Layer, Lut6, Model, _check, _ptr, _stream, _workspace, lib,
-               prefill_workspace_size)
+               lut6_tile, prefill_workspace_size)
 
 GDN, ATTENTION = 0, 1
 
@@ -52,7 +53,12 @@ class DeviceLayer:
 
         def lut6(pair):
             packed, lut = pair
-            return Lut6(_ptr(dev(packed)), _ptr(dev(lut)))
+            k = packed.shape[1] * 4 // 3
+            canon = torch.from_numpy(np.ascontiguousarray(packed)).to(device)
+            tiled = lut6_tile(canon, k)      # the GEMM's operand layout (same bytes, moved)
+            self._keep.append(tiled)
+            del canon
+            return Lut6(_ptr(tiled), _ptr(dev(lut)))
 
         st = Layer()
         st.kind = kind

@@ -100,14 +100,23 @@ CLEF_API clef_status clef_lut6_unpack(const uint8_t* packed, int64_t n, int64_t 
 CLEF_API clef_status clef_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_t n, int64_t k,
                               uint16_t* w, clef_stream stream);
 
+/* device: tiled [n, k*3/4] = the same bytes as `packed` rearranged into the LUT-6 GEMM's operand
+   layout (n % 16 == 0, k % 64 == 0; CLEF_E_SHAPE otherwise).  For each 16-row group G and each
+   64-wide block kb of k, a 768-byte block at ((G * k/64) + kb) * 768 holds, for t = 0..31, the
+   24 bytes t*24 ..: the 3-byte quadruples (16kb + 4j + t%4, j = 0..3) of row 16G + t/4, then of
+   row 16G + t/4 + 8.  No bit changes; only whole quadruples move.  Done once per weight. */
+CLEF_API clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
+                                    clef_stream stream);
+
 /* device: y [m, n] = x [m, k] . W^T, fp32 accumulation; y is fp16 (y_is_fp32 = 0) or fp32
-   (y_is_fp32 = 1).  The LUT-6 weight is dequantised in shared memory and fed to tcgen05
-   tensor-core MMAs; W is never written to global memory.  Requirements: m >= 0 (m == 0 is a
-   no-op and x, y may then be NULL), n % 16 == 0, k % 64 == 0, k > 0 (CLEF_E_SHAPE otherwise).
-   x, packed, lut, y device,
-   16-byte aligned. */
-CLEF_API clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,
-                           int32_t y_is_fp32, int64_t m, int64_t n, int64_t k, clef_stream stream);
+   (y_is_fp32 = 1); W given as `tiled` (clef_lut6_tile) and lut.  The weights are dequantised
+   into tensor memory and used there as the A operand of tcgen05 MMAs (Y^T = W X^T); W is never
+   written to global memory.  Requirements: m >= 0 (m == 0 is a no-op and x, y may then be NULL),
+   n % 16 == 0, k % 64 == 0, k > 0 (CLEF_E_SHAPE otherwise).  x, tiled, lut, y device, 16-byte
+   aligned. */
+CLEF_API clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* tiled, const uint16_t* lut,
+                                    void* y, int32_t y_is_fp32, int64_t m, int64_t n, int64_t k,
+                                    clef_stream stream);
 
 /* ------------------------------------------------------------------------------------------
  * Gated DeltaNet scan ("Clef-Flash-ANE-LUT6" section "Model architecture"; "clef-flash - Core
@@ -170,7 +179,7 @@ CLEF_API clef_status clef_gqa_attn_prefill(const uint16_t* q, const uint16_t* k,
  * The model.  All pointers are device pointers except `layers` (a host array).
  * ------------------------------------------------------------------------------------------ */
 typedef struct {
-  const uint8_t* packed; /* [n, k*3/4] */
+  const uint8_t* packed; /* [n, k*3/4] in the tiled layout of clef_lut6_tile */
   const uint16_t* lut;   /* [n/16, 64] fp16 */
 } clef_lut6;
 

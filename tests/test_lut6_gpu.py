@@ -73,3 +73,19 @@ def test_gemm_deterministic():
     a = clef.lut6_gemm(x, p, l)
     b = clef.lut6_gemm(x, p, l)
     assert torch.equal(a, b)
+
+
+def test_tile_layout_moves_whole_quadruples():
+    # the tiled layout documented in clef.h, restated with numpy index arithmetic
+    n, k = 48, 192
+    packed = synth.random_bytes(5, "tile", 0, (n, k * 3 // 4))
+    tiled = clef.lut6_tile(_dev(packed), k).cpu().numpy().reshape(-1)
+    trip = packed.reshape(n, k // 4, 3)
+    expect = np.empty((n // 16, k // 64, 32, 2, 4, 3), dtype=np.uint8)
+    for G in range(n // 16):
+        for kb in range(k // 64):
+            for t in range(32):
+                for h in range(2):
+                    for j in range(4):
+                        expect[G, kb, t, h, j] = trip[16 * G + t // 4 + 8 * h, 16 * kb + 4 * j + t % 4]
+    assert np.array_equal(tiled, expect.reshape(-1))
