@@ -8,9 +8,9 @@
 // transposed product D[n, m] = W X^T so that the weights are the MMA's A operand, held in tensor
 // memory, and never pass through shared memory:
 //   * one CTA per 128 (output channels) x 256 (tokens) tile, K walked in blocks of 64;
-//   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and bulk copies
-//     of the 8 packed 768-byte blocks of the tile's rows (tiled layout, see clef_lut6_tile) into
-//     a 4-stage ring;
+//   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and of the 8
+//     packed 768-byte blocks of the tile's rows (tiled layout, see clef_lut6_tile) into a 4-stage
+//     ring;
 //   * warps 4..11 dequantise: each warp owns one 16-row table group and writes its 16 x 64
 //     weights straight into a tensor-memory A stage with one tcgen05.st.16x256b.x4; every
 //     lookup of a warp hits the same 64-entry table (128 bytes, one entry pair per bank), so the
@@ -132,7 +132,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                     const uint8_t* __restrict__ tiled, const __half* __restrict__ lut,
+                     const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
                      void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
                      unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_acc, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_p);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -173,17 +174,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const int ngroups = min(BN / 16, N / 16 - n0 / 16);  // groups of this tile inside N
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1;
         if (kb >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1, status, DEV_TIMEOUT_TMA)) break;
-        mbar_arrive_expect_tx(bar_full + 8 * s, X_BYTES + ngroups * P_BLOCK);
+        mbar_arrive_expect_tx(bar_full + 8 * s, X_BYTES + P_BYTES);
         tma_load_2d(sb + OFF_X + s * X_BYTES, &tmap_x, bar_full + 8 * s, kb * BK, m0);
-        for (int gi = 0; gi < ngroups; ++gi)
-          bulk_load(sb + OFF_P + s * P_BYTES + gi * P_BLOCK,
-                    tiled + ((size_t)(n0 / 16 + gi) * num_kb + kb) * P_BLOCK, P_BLOCK,
-                    bar_full + 8 * s);
+        // the 8 groups' 768-byte blocks of k-block kb: box {256 B, 3, 8 groups}
+        tma_load_3d(sb + OFF_P + s * P_BYTES, &tmap_p, bar_full + 8 * s, 0, 3 * kb, n0 / 16);
       }
     }
   } else if (warp == 1) {
@@ -376,10 +374,19 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
                              cudaStream_t stream) {
   using namespace lut;
   if (M == 0) return CLEF_OK;
-  CUtensorMap tx;
+  CUtensorMap tx, tp;
   if (tma_encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)K, (uint64_t)M,
                     (uint64_t)K * 2, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
     return CLEF_E_CUDA;
+  {
+    // tiled weights as [N/16 groups][3 * K/64][256 bytes]; groups past N read as zero
+    const uint64_t dims[3] = {256, (uint64_t)(3 * (K / BK)), (uint64_t)(N / 16)};
+    const uint64_t st[2] = {256, (uint64_t)(K / BK) * P_BLOCK};
+    const uint32_t box[3] = {256, 3, BN / 16};
+    if (tma_encode(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, tiled, dims, st, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+      return CLEF_E_CUDA;
+  }
   static bool attr_set = false;
   if (!attr_set) {
     CLEF_CUDA_CHECK(cudaFuncSetAttribute(lut6_gemm_kernel,
@@ -394,7 +401,7 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
                 0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
   lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      tx, tiled, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
+      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
