@@ -36,17 +36,17 @@ constexpr float kLogAlphaMin = -30.0f;
 
 // ------------------------------------------------------------------------------------------
 // Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels and
-// the per-head L2 norm of q and k.  A CTA covers 16 consecutive tokens for 2048 channels (256
+// the per-head L2 norm of q and k.  A CTA covers 16 consecutive tokens for 1024 channels (128
 // threads x 8 channels); each thread issues the loads of all 19 rows it needs at once and keeps
 // them in registers.  The gates come from the a/b projection's epilogue.
 // proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..).
 // ------------------------------------------------------------------------------------------
 constexpr int PREP_T = 16;
-__global__ void __launch_bounds__(256) gdn_prep_kernel(
+__global__ void __launch_bounds__(128) gdn_prep_kernel(
     const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
     __half* __restrict__ q, __half* __restrict__ k, __half* __restrict__ v, int64_t M, int L) {
   const int tid = threadIdx.x;
-  const int ch0 = blockIdx.x * 2048 + tid * 8;
+  const int ch0 = blockIdx.x * 1024 + tid * 8;
   const int64_t tok0 = (int64_t)blockIdx.y * PREP_T;
   float w[8][4];
   {
@@ -681,8 +681,8 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
                             __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
-  dim3 grid(4, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
-  gdn::gdn_prep_kernel<<<grid, 256, 0, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
+  dim3 grid(8, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
+  gdn::gdn_prep_kernel<<<grid, 128, 0, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
