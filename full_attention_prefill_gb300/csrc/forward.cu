@@ -64,7 +64,7 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
   t.abpart = static_cast<float*>(take(ab_proj_scratch_bytes(M)));
   t.mix = static_cast<__half*>(take(M * H * 2));
   t.h = static_cast<__half*>(take(M * I * 2));
-  t.scan = take(gdn_scan_workspace_bytes(B, L));
+  t.scan = take(gdn_scan_workspace_bytes(B, L, true));
   if (w) *w = t;
   return off;
 }
@@ -172,7 +172,7 @@ extern "C" {
 
 size_t clef_gdn_workspace_size(int64_t B, int64_t L) {
   if (B < 1 || L < 1) return 0;
-  return gdn_scan_workspace_bytes(B, L);
+  return gdn_scan_workspace_bytes(B, L, false);
 }
 
 clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -190,9 +190,9 @@ clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, const uint16_
     set_error("clef_gdn_prefill: s0 / s_out not 16-byte aligned");
     return CLEF_E_ALIGN;
   }
-  if (workspace_bytes < gdn_scan_workspace_bytes(B, L)) {
+  if (workspace_bytes < gdn_scan_workspace_bytes(B, L, false)) {
     set_error("clef_gdn_prefill: workspace of %zu bytes, need %zu", workspace_bytes,
-              gdn_scan_workspace_bytes(B, L));
+              gdn_scan_workspace_bytes(B, L, false));
     return CLEF_E_WORKSPACE;
   }
   if (debug_should_fail()) return CLEF_E_CUDA;

@@ -11,11 +11,15 @@
 //     W = T diag(beta exp(g)) K,   U' = T diag(beta) V,   U = U' - W S0^T
 //     O = (diag(exp(g)) Q S0^T + (tril(Q K^T) o exp(g_r - g_s)) U) / sqrt(128)
 //     S_C = exp(g_C) S0 + U^T diag(exp(g_C - g)) K
-// Three kernels:
-//   gdn_chunk_wy    (parallel over chunks x heads): g, T by forward substitution, W and U'
-//   gdn_state_pass  (sequential over chunks, parallel over heads x 8 slices of 16 value rows):
-//                   U and the state entering every chunk; the state stays in registers
-//   gdn_chunk_out   (parallel over chunks x heads): O, with the z-gated RMSNorm fused in
+// Kernels:
+//   gdn_chunk_wy    (parallel over chunks x heads): cumulative g, T by forward substitution,
+//                   W, U', the decayed keys exp(g_C - g) k and the intra-chunk matrix
+//                   Aqk = tril(Q K^T) o exp(g_r - g_s) / sqrt(128)
+//   gdn_state_pass  (sequential over chunks; one warp per 16 value rows of a head): the state
+//                   slice stays in mma accumulators and is reused in registers as the fp16
+//                   operand S0^T; per chunk U = U' - W S0^T, O = exp(g) Q S0^T / sqrt(128) + Aqk U,
+//                   S <- exp(g_C) S + U^T Kd, with U transposed in registers (movmatrix)
+//   gdn_gated_norm  (decoder layer only): y = RMSNorm_128(O) * w_o * SiLU(z)
 // All products run on tensor cores (mma.sync m16n8k16, fp16 inputs, fp32 accumulation); the
 // state and the scalars stay fp32.
 #include <algorithm>
@@ -127,12 +131,11 @@ __global__ void log_alpha_kernel(const float* __restrict__ alpha, float* __restr
 // U' = T diag(beta) V.  128 threads; warp w owns rows 16w .. 16w+15 of every 64-row product.
 // ------------------------------------------------------------------------------------------
 struct WySmem {
-  __half K[C][LDH];
-  __half V[C][LDH];
-  __half KB[C][LDH];   // beta * exp(g) * K
-  __half VB[C][LDH];   // beta * V
+  __half Q[C][LDH];
+  __half K[C][LDH];    // K, then beta * exp(g) * K in place
+  __half V[C][LDH];    // V, then beta * V in place
   __half T[C][C + 8];  // (I + A)^-1 in fp16 for the products
-  float A[C][C + 4];    // 16-byte aligned rows for broadcast float4 reads
+  float A[C][C + 4];   // 16-byte aligned rows for broadcast float4 reads
   float gc[C];
   float bt[C];
   float eb[C];         // beta_r exp(g_r)
@@ -140,9 +143,10 @@ struct WySmem {
 };
 
 __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
-    const __half* __restrict__ kk, const __half* __restrict__ vv, const float* __restrict__ g,
-    const float* __restrict__ beta, float* __restrict__ gcum, __half* __restrict__ Wout,
-    float* __restrict__ Uout, __half* __restrict__ Ktout, int L, int nch) {
+    const __half* __restrict__ qq, const __half* __restrict__ kk, const __half* __restrict__ vv,
+    const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ gcum,
+    __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Ktout,
+    __half* __restrict__ Aqk, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
   WySmem& s = *reinterpret_cast<WySmem*>(smraw);
   const int cg = blockIdx.x;           // global chunk index = b * nch + c
@@ -151,18 +155,18 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   const int64_t t0 = (int64_t)b * L + (int64_t)c * C;
   const int nvalid = min(C, L - c * C);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
 
-  // load K (key head h/2) and V (head h) rows, zero past the request's end
+  // Q, K (key head h/2) and V (head h) rows, zero past the request's end
   for (int i = tid; i < C * (D / 8); i += 128) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    uint4 ku = make_uint4(0, 0, 0, 0), vu = make_uint4(0, 0, 0, 0);
-    if (r < nvalid) {
-      ku = *reinterpret_cast<const uint4*>(kk + (t0 + r) * (HK * D) + (h >> 1) * D + c8);
-      vu = *reinterpret_cast<const uint4*>(vv + (t0 + r) * (HV * D) + h * D + c8);
-    }
-    *reinterpret_cast<uint4*>(&s.K[r][c8]) = ku;
-    *reinterpret_cast<uint4*>(&s.V[r][c8]) = vu;
+    const bool ok = r < nvalid;
+    const int64_t rr = ok ? t0 + r : t0;
+    cp_async16(smem_u32(&s.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
+    cp_async16(smem_u32(&s.K[r][c8]), kk + rr * (HK * D) + (h >> 1) * D + c8, ok);
+    cp_async16(smem_u32(&s.V[r][c8]), vv + rr * (HV * D) + h * D + c8, ok);
   }
+  cp_async_commit();
   if (warp == 0) {
     // inclusive prefix sum of g over the chunk (2 rows per lane)
     const int r0 = 2 * lane, r1 = 2 * lane + 1;
@@ -181,19 +185,28 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     s.bt[r0] = r0 < nvalid ? beta[(t0 + r0) * HV + h] : 0.f;
     s.bt[r1] = r1 < nvalid ? beta[(t0 + r1) * HV + h] : 0.f;
   }
+  cp_async_wait<0>();
   __syncthreads();
   if (tid < C && tid < nvalid) gcum[(t0 + tid) * HV + h] = s.gc[tid];
+  const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
+  if (tid < C) {
+    s.eb[tid] = s.bt[tid] * __expf(s.gc[tid]);
+    s.ed[tid] = __expf(gC - s.gc[tid]);
+  }
 
   const uint32_t sK = smem_u32(&s.K[0][0]);
-  // A = strict_tril(beta_r e^{g_r - g_s} k_r . k_s)
-  {
+  const uint32_t sQ = smem_u32(&s.Q[0][0]);
+  // A = strict_tril(beta_r e^{g_r - g_s} k_r . k_s) and Aqk = tril(q_r . k_s e^{g_r - g_s}) / sqrt(128)
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t sA = which == 0 ? sK : sQ;
     float acc[8][4];
 #pragma unroll
     for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t a[4];
-      ldsm_x4(a, a_addr(sK, LDH, warp * 16, ks * 16, lane));
+      ldsm_x4(a, a_addr(sA, LDH, warp * 16, ks * 16, lane));
 #pragma unroll
       for (int n = 0; n < 8; n += 2) {
         uint32_t bq[4];
@@ -202,34 +215,34 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
         mma16816(acc[n + 1], a, bq[2], bq[3]);
       }
     }
-    const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = warp * 16 + gq + (e >= 2 ? 8 : 0);
-        const int col = n * 8 + 2 * tq + (e & 1);
-        float val = 0.f;
-        if (col < r) val = s.bt[r] * __expf(s.gc[r] - s.gc[col]) * acc[n][e];
-        s.A[r][col] = val;
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = warp * 16 + gq + hf * 8;
+        const int col = n * 8 + 2 * tq;
+        const float d0 = __expf(s.gc[r] - s.gc[col]), d1 = __expf(s.gc[r] - s.gc[col + 1]);
+        if (which == 0) {
+          s.A[r][col] = (col < r) ? s.bt[r] * d0 * acc[n][2 * hf] : 0.f;
+          s.A[r][col + 1] = (col + 1 < r) ? s.bt[r] * d1 * acc[n][2 * hf + 1] : 0.f;
+        } else {
+          const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
+          const float v0 = (col <= r) ? d0 * acc[n][2 * hf] * scale : 0.f;
+          const float v1 = (col + 1 <= r) ? d1 * acc[n][2 * hf + 1] * scale : 0.f;
+          *reinterpret_cast<uint32_t*>(Aqk + (((int64_t)cg * HV + h) * C + r) * C + col) = h2u(v0, v1);
+        }
       }
     }
   }
-  // scaled operands for W and U', and the decayed keys exp(g_C - g_r) k_r the state pass uses
-  const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
-  if (tid < C) {
-    s.eb[tid] = s.bt[tid] * __expf(s.gc[tid]);
-    s.ed[tid] = __expf(gC - s.gc[tid]);
-  }
   __syncthreads();
+  // decayed keys to global; K -> beta e^g K and V -> beta V in place
   for (int i = tid; i < C * (D / 2); i += 128) {
     const int r = i / (D / 2), c2 = (i % (D / 2)) * 2;
-    const float eb = s.eb[r];
-    const float ed = s.ed[r];
+    const float eb = s.eb[r], ed = s.ed[r];
     const float2 kf = __half22float2(*reinterpret_cast<const __half2*>(&s.K[r][c2]));
     const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&s.V[r][c2]));
-    *reinterpret_cast<__half2*>(&s.KB[r][c2]) = __floats2half2_rn(eb * kf.x, eb * kf.y);
-    *reinterpret_cast<__half2*>(&s.VB[r][c2]) = __floats2half2_rn(s.bt[r] * vf.x, s.bt[r] * vf.y);
+    *reinterpret_cast<__half2*>(&s.K[r][c2]) = __floats2half2_rn(eb * kf.x, eb * kf.y);
+    *reinterpret_cast<__half2*>(&s.V[r][c2]) = __floats2half2_rn(s.bt[r] * vf.x, s.bt[r] * vf.y);
     if (r < nvalid)
       *reinterpret_cast<__half2*>(Ktout + ((t0 + r) * HV + h) * D + c2) =
           __floats2half2_rn(ed * kf.x, ed * kf.y);
@@ -264,10 +277,9 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   __syncthreads();
   // W = T KB and U' = T VB  (rows 16w.., all 128 columns)
   const uint32_t sT = smem_u32(&s.T[0][0]);
-  const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
-    const uint32_t sB = smem_u32(which == 0 ? &s.KB[0][0] : &s.VB[0][0]);
+    const uint32_t sB = smem_u32(which == 0 ? &s.K[0][0] : &s.V[0][0]);
     float acc[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
@@ -302,42 +314,58 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
-// Phase 2: the state pass.  One CTA per (request, value head, slice of 16 value rows); the
-// 16 x 128 fp32 state slice lives in mma accumulators (warp w: key columns 32w..32w+31).  Per
-// chunk: U = U' - W S0^T for the slice, then S <- exp(g_C) S + U^T Kd with the decayed keys
-// Kd = diag(exp(g_C - g)) K written by phase 1.  Everything a chunk needs (W, Kd, U', g) is
-// prefetched with cp.async while the previous chunk is processed.
+// Phase 2: the fused state pass.  CTA = (request, value head, 32 value rows); warp w owns value
+// rows 16w.. of that slice.  Per chunk (all data prefetched by cp.async one chunk ahead):
+//   SB   = fp16 B fragments of S0^T, taken straight from the fp32 state accumulators
+//   U    = U' - W S0^T                               (rows past the end set to zero)
+//   UT   = U transposed in registers (movmatrix): A fragments of U^T, B fragments of U
+//   O    = exp(g) / sqrt(128) * (Q S0^T) + Aqk U     -> out
+//   S   <- exp(g_C) S + U^T Kd
+// One barrier per chunk (the two warps share the prefetched tiles).
 // ------------------------------------------------------------------------------------------
-constexpr int SL = 16;  // value rows per CTA
+constexpr int SW = 2;              // warps (16-row value slices) per CTA
 struct PassBuf {
   __half W[C][LDH];
-  __half K[C][LDH];      // decayed keys
-  float U[C][SL + 4];
+  __half Q[C][LDH];
+  __half K[C][LDH];       // decayed keys
+  __half Aq[C][C + 8];
+  float U[SW][C][16 + 4];
   float gc[C];
 };
 struct PassSmem {
   PassBuf buf[2];
-  __half S[SL][LDH];       // fp16 copy of the entering state slice (value row, key col)
-  __half Vn[C][SL + 8];    // U for the slice (token, value row)
 };
 
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void pass_prefetch(PassBuf& pb, const __half* __restrict__ Wg,
+                                              const __half* __restrict__ qq,
                                               const __half* __restrict__ Kt,
+                                              const __half* __restrict__ Aqk,
                                               const float* __restrict__ Ug,
                                               const float* __restrict__ gcum, int64_t t0,
-                                              int nvalid, int h, int sl, int tid) {
-  for (int i = tid; i < C * (D / 8); i += 128) {
+                                              int64_t cgi, int nvalid, int h, int dv0, int tid) {
+  for (int i = tid; i < C * (D / 8); i += 32 * SW) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < nvalid;
     const int64_t rr = ok ? (t0 + r) : t0;
     cp_async16(smem_u32(&pb.W[r][c8]), Wg + (rr * HV + h) * D + c8, ok);
+    cp_async16(smem_u32(&pb.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
     cp_async16(smem_u32(&pb.K[r][c8]), Kt + (rr * HV + h) * D + c8, ok);
   }
-  for (int i = tid; i < C * (SL / 4); i += 128) {
-    const int r = i / (SL / 4), c4 = (i % (SL / 4)) * 4;
+  for (int i = tid; i < C * (C / 8); i += 32 * SW) {
+    const int r = i / (C / 8), c8 = (i % (C / 8)) * 8;
+    cp_async16(smem_u32(&pb.Aq[r][c8]), Aqk + ((cgi * HV + h) * C + r) * C + c8, true);
+  }
+  for (int i = tid; i < SW * C * 4; i += 32 * SW) {
+    const int w = i / (C * 4), r = (i / 4) % C, c4 = (i % 4) * 4;
     const bool ok = r < nvalid;
     const int64_t rr = ok ? (t0 + r) : t0;
-    cp_async16(smem_u32(&pb.U[r][c4]), Ug + (rr * HV + h) * D + sl * SL + c4, ok);
+    cp_async16(smem_u32(&pb.U[w][r][c4]), Ug + (rr * HV + h) * D + dv0 + 16 * w + c4, ok);
   }
   if (tid < C) {
     // rows past the end repeat the last valid g
@@ -349,295 +377,216 @@ __device__ __forceinline__ void pass_prefetch(PassBuf& pb, const __half* __restr
   cp_async_commit();
 }
 
-__global__ void __launch_bounds__(128) gdn_state_pass_kernel(
-    const __half* __restrict__ Kt, const __half* __restrict__ Wg, const float* __restrict__ Ug,
-    const float* __restrict__ gcum, const float* __restrict__ s0, __half* __restrict__ Vnew,
-    __half* __restrict__ S0out, float* __restrict__ s_out, int L, int nch) {
+__global__ void __launch_bounds__(32 * SW) gdn_state_pass_kernel(
+    const __half* __restrict__ qq, const __half* __restrict__ Kt, const __half* __restrict__ Wg,
+    const float* __restrict__ Ug, const __half* __restrict__ Aqk, const float* __restrict__ gcum,
+    const float* __restrict__ s0, __half* __restrict__ out, int64_t ldo,
+    float* __restrict__ s_out, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
   PassSmem& s = *reinterpret_cast<PassSmem*>(smraw);
-  const int sl = blockIdx.x % (D / SL);
-  const int h = (blockIdx.x / (D / SL)) % HV;
-  const int b = blockIdx.x / ((D / SL) * HV);
+  constexpr int NSL = D / (16 * SW);     // CTAs per head
+  const int sl = blockIdx.x % NSL;
+  const int h = (blockIdx.x / NSL) % HV;
+  const int b = blockIdx.x / (NSL * HV);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int ncol = warp * 32;            // key columns of this warp's state tiles
+  const int dv0 = sl * 16 * SW;          // first value row of the CTA
+  const int dvw = dv0 + 16 * warp;       // first value row of this warp
 
-  float S[4][4];
+  // state slice [16 value rows x 128 key cols]: n-tile nt covers key columns 8nt..8nt+7
+  float S[16][4];
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
+  for (int nt = 0; nt < 16; ++nt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float v0 = 0.f;
       if (s0) {
-        const int r = sl * SL + gq + (e >= 2 ? 8 : 0);
-        const int col = ncol + n * 8 + 2 * tq + (e & 1);
+        const int r = dvw + gq + (e >= 2 ? 8 : 0);
+        const int col = nt * 8 + 2 * tq + (e & 1);
         v0 = s0[(((int64_t)b * HV + h) * D + r) * D + col];
       }
-      S[n][e] = v0;
+      S[nt][e] = v0;
     }
   }
   const int64_t tb = (int64_t)b * L;
-  pass_prefetch(s.buf[0], Wg, Kt, Ug, gcum, tb, min(C, L), h, sl, tid);
+  pass_prefetch(s.buf[0], Wg, qq, Kt, Aqk, Ug, gcum, tb, (int64_t)b * nch, min(C, L), h, dv0, tid);
+  const float inv_sqrt_d = 0.08838834764831845f;
 
   for (int c = 0; c < nch; ++c) {
     const int64_t t0 = tb + (int64_t)c * C;
     const int nvalid = min(C, L - c * C);
     PassBuf& pb = s.buf[c & 1];
-    // entering state: fp16 copy to shared (for W S0^T) and to global (for the output phase)
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = gq + hf * 8;
-        const int col = ncol + n * 8 + 2 * tq;
-        const uint32_t pk = h2u(S[n][2 * hf], S[n][2 * hf + 1]);
-        *reinterpret_cast<uint32_t*>(&s.S[r][col]) = pk;
-        *reinterpret_cast<uint32_t*>(
-            S0out + ((((int64_t)b * nch + c) * HV + h) * D + sl * SL + r) * D + col) = pk;
-      }
-    }
+    cp_async_wait<0>();
+    __syncthreads();  // chunk c landed for both warps; both are done with chunk c-1's buffer
     if (c + 1 < nch)
-      pass_prefetch(s.buf[(c + 1) & 1], Wg, Kt, Ug, gcum, t0 + C, min(C, L - (c + 1) * C), h, sl,
-                    tid);
-    else
-      cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const float eC = __expf(pb.gc[C - 1]);
-    // U = U' - W S0^T  (tokens 16w.., 16 value rows)
-    {
+      pass_prefetch(s.buf[(c + 1) & 1], Wg, qq, Kt, Aqk, Ug, gcum, t0 + C, (int64_t)b * nch + c + 1,
+                    min(C, L - (c + 1) * C), h, dv0, tid);
+    // SB[ks][nv]: B fragments of S0^T for key step ks (16 columns) and value n-tile nv
+    uint32_t SB[8][2][2];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      SB[ks][0][0] = h2u(S[2 * ks][0], S[2 * ks][1]);
+      SB[ks][0][1] = h2u(S[2 * ks + 1][0], S[2 * ks + 1][1]);
+      SB[ks][1][0] = h2u(S[2 * ks][2], S[2 * ks][3]);
+      SB[ks][1][1] = h2u(S[2 * ks + 1][2], S[2 * ks + 1][3]);
+    }
+    const uint32_t sW = smem_u32(&pb.W[0][0]), sQ = smem_u32(&pb.Q[0][0]);
+    const uint32_t sK = smem_u32(&pb.K[0][0]), sA = smem_u32(&pb.Aq[0][0]);
+    // U = U' - W S0^T, transposed into UT[mt][nv][2] (fp16): rows tok 16mt.., value rows 8nv..
+    uint32_t UT[4][2][2];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
       float acc[2][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-      const uint32_t sW = smem_u32(&pb.W[0][0]);
-      const uint32_t sS = smem_u32(&s.S[0][0]);
+      for (int nv = 0; nv < 2; ++nv) acc[nv][0] = acc[nv][1] = acc[nv][2] = acc[nv][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a[4], bq[4];
-        ldsm_x4(a, a_addr(sW, LDH, warp * 16, ks * 16, lane));
-        ldsm_x4(bq, bn_addr(sS, LDH, 0, ks * 16, lane));
-        mma16816(acc[0], a, bq[0], bq[1]);
-        mma16816(acc[1], a, bq[2], bq[3]);
-      }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = warp * 16 + gq + hf * 8;
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const int col = n * 8 + 2 * tq;
-          const float u0 = pb.U[r][col] - acc[n][2 * hf];
-          const float u1 = pb.U[r][col + 1] - acc[n][2 * hf + 1];
-          const uint32_t pk = (r < nvalid) ? h2u(u0, u1) : 0u;
-          *reinterpret_cast<uint32_t*>(&s.Vn[r][col]) = pk;
-          if (r < nvalid)
-            *reinterpret_cast<uint32_t*>(Vnew + ((t0 + r) * HV + h) * D + sl * SL + col) = pk;
-        }
-      }
-    }
-    __syncthreads();
-    // S <- exp(g_C) S + U^T Kd
-    {
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        S[n][0] *= eC; S[n][1] *= eC; S[n][2] *= eC; S[n][3] *= eC;
-      }
-      const uint32_t sV = smem_u32(&s.Vn[0][0]);
-      const uint32_t sK = smem_u32(&pb.K[0][0]);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) {
+      for (int ks = 0; ks < 8; ++ks) {
         uint32_t a[4];
-        ldsm_x4_t(a, at_addr(sV, SL + 8, 0, ks * 16, lane));
+        ldsm_x4(a, a_addr(sW, LDH, mt * 16, ks * 16, lane));
+        mma16816(acc[0], a, SB[ks][0][0], SB[ks][0][1]);
+        mma16816(acc[1], a, SB[ks][1][0], SB[ks][1][1]);
+      }
 #pragma unroll
-        for (int n = 0; n < 4; n += 2) {
-          uint32_t bq[4];
-          ldsm_x4_t(bq, bk_addr(sK, LDH, ncol + n * 8, ks * 16, lane));
-          mma16816(S[n], a, bq[0], bq[1]);
-          mma16816(S[n + 1], a, bq[2], bq[3]);
-        }
+      for (int nv = 0; nv < 2; ++nv) {
+        const int r0 = mt * 16 + gq, r1 = r0 + 8;
+        const int col = nv * 8 + 2 * tq;
+        const float u00 = r0 < nvalid ? pb.U[warp][r0][col] - acc[nv][0] : 0.f;
+        const float u01 = r0 < nvalid ? pb.U[warp][r0][col + 1] - acc[nv][1] : 0.f;
+        const float u10 = r1 < nvalid ? pb.U[warp][r1][col] - acc[nv][2] : 0.f;
+        const float u11 = r1 < nvalid ? pb.U[warp][r1][col + 1] - acc[nv][3] : 0.f;
+        UT[mt][nv][0] = movmatrix_t(h2u(u00, u01));
+        UT[mt][nv][1] = movmatrix_t(h2u(u10, u11));
       }
     }
-    __syncthreads();  // buffers of this chunk are free for the prefetch two chunks ahead
+    // O = e^g / sqrt(128) * (Q S0^T) + Aqk U
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      float acc[2][4];
+#pragma unroll
+      for (int nv = 0; nv < 2; ++nv) acc[nv][0] = acc[nv][1] = acc[nv][2] = acc[nv][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, a_addr(sQ, LDH, mt * 16, ks * 16, lane));
+        mma16816(acc[0], a, SB[ks][0][0], SB[ks][0][1]);
+        mma16816(acc[1], a, SB[ks][1][0], SB[ks][1][1]);
+      }
+      const int r0 = mt * 16 + gq, r1 = r0 + 8;
+      const float f0 = __expf(pb.gc[r0]) * inv_sqrt_d, f1 = __expf(pb.gc[r1]) * inv_sqrt_d;
+#pragma unroll
+      for (int nv = 0; nv < 2; ++nv) {
+        acc[nv][0] *= f0; acc[nv][1] *= f0; acc[nv][2] *= f1; acc[nv][3] *= f1;
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, a_addr(sA, C + 8, mt * 16, ks * 16, lane));
+        mma16816(acc[0], a, UT[ks][0][0], UT[ks][0][1]);
+        mma16816(acc[1], a, UT[ks][1][0], UT[ks][1][1]);
+      }
+#pragma unroll
+      for (int nv = 0; nv < 2; ++nv) {
+        const int col = dvw + nv * 8 + 2 * tq;
+        if (r0 < nvalid)
+          *reinterpret_cast<uint32_t*>(out + (t0 + r0) * ldo + h * D + col) = h2u(acc[nv][0], acc[nv][1]);
+        if (r1 < nvalid)
+          *reinterpret_cast<uint32_t*>(out + (t0 + r1) * ldo + h * D + col) = h2u(acc[nv][2], acc[nv][3]);
+      }
+    }
+    // S <- e^{g_C} S + U^T Kd
+    const float eC = __expf(pb.gc[C - 1]);
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      S[nt][0] *= eC; S[nt][1] *= eC; S[nt][2] *= eC; S[nt][3] *= eC;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint32_t a[4] = {UT[ks][0][0], UT[ks][1][0], UT[ks][0][1], UT[ks][1][1]};
+#pragma unroll
+      for (int nt = 0; nt < 16; nt += 2) {
+        uint32_t bq[4];
+        ldsm_x4_t(bq, bk_addr(sK, LDH, nt * 8, ks * 16, lane));
+        mma16816(S[nt], a, bq[0], bq[1]);
+        mma16816(S[nt + 1], a, bq[2], bq[3]);
+      }
+    }
   }
-  cp_async_wait<0>();
   if (s_out) {
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
+    for (int nt = 0; nt < 16; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = sl * SL + gq + (e >= 2 ? 8 : 0);
-        const int col = ncol + n * 8 + 2 * tq + (e & 1);
-        s_out[(((int64_t)b * HV + h) * D + r) * D + col] = S[n][e];
+        const int r = dvw + gq + (e >= 2 ? 8 : 0);
+        const int col = nt * 8 + 2 * tq + (e & 1);
+        s_out[(((int64_t)b * HV + h) * D + r) * D + col] = S[nt][e];
       }
     }
   }
 }
 
 // ------------------------------------------------------------------------------------------
-// Phase 3: outputs of a (chunk, value head): O = (diag(e^g) Q S0^T + (tril(QK^T) o Gamma) U)
-// / sqrt(128); then either a plain fp16 store or the z-gated RMSNorm
-//   y = RMSNorm_128(O) * w_o * SiLU(z)  stored at out[token, h*128 + dv].
+// Output gate of the decoder layer: y[t, h*128 + i] = RMSNorm_128(o[t, h, :])_i * w_i * SiLU(z).
+// One CTA (256 threads) per token; 8 threads x 16 values per head.
 // ------------------------------------------------------------------------------------------
-struct OutSmem {
-  __half Q[C][LDH];
-  __half K[C][LDH];
-  __half U[C][LDH];
-  __half S[D][LDH];  // entering state (value row, key col)
-  float gc[C];
-};
-
-__global__ void __launch_bounds__(128) gdn_chunk_out_kernel(
-    const __half* __restrict__ qq, const __half* __restrict__ kk, const __half* __restrict__ Vnew,
-    const __half* __restrict__ S0g, const float* __restrict__ gcum, const __half* __restrict__ z,
-    int64_t ldz, const __half* __restrict__ o_norm, __half* __restrict__ out, int64_t ldo, int L,
-    int nch) {
-  extern __shared__ __align__(16) uint8_t smraw[];
-  OutSmem& s = *reinterpret_cast<OutSmem*>(smraw);
-  const int cg = blockIdx.x, h = blockIdx.y;
-  const int b = cg / nch, c = cg % nch;
-  const int64_t t0 = (int64_t)b * L + (int64_t)c * C;
-  const int nvalid = min(C, L - c * C);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-
-  for (int i = tid; i < C * (D / 8); i += 128) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    const bool ok = r < nvalid;
-    const int64_t rr = ok ? t0 + r : t0;
-    cp_async16(smem_u32(&s.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
-    cp_async16(smem_u32(&s.K[r][c8]), kk + rr * (HK * D) + (h >> 1) * D + c8, ok);
-    cp_async16(smem_u32(&s.U[r][c8]), Vnew + (rr * HV + h) * D + c8, ok);
-  }
-  const __half* Sg = S0g + (((int64_t)cg) * HV + h) * D * D;
-  for (int i = tid; i < D * (D / 8); i += 128) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    cp_async16(smem_u32(&s.S[r][c8]), Sg + r * D + c8, true);
-  }
-  cp_async_commit();
-  if (tid < C) s.gc[tid] = gcum[(t0 + min(tid, nvalid - 1)) * HV + h];
-  cp_async_wait<0>();
-  __syncthreads();
-
-  const uint32_t sQ = smem_u32(&s.Q[0][0]), sK = smem_u32(&s.K[0][0]);
-  const uint32_t sU = smem_u32(&s.U[0][0]), sS = smem_u32(&s.S[0][0]);
-  // P = Q K^T for rows 16w..16w+15, masked and decayed
-  uint32_t pa[4][4];  // P as A fragments, 4 k-steps of 16 keys
+__global__ void __launch_bounds__(256) gdn_gated_norm_kernel(const __half* __restrict__ o,
+                                                             const __half* __restrict__ z,
+                                                             int64_t ldz,
+                                                             const __half* __restrict__ w,
+                                                             __half* __restrict__ y, int64_t ldy) {
+  const int64_t tok = blockIdx.x;
+  const int c0 = threadIdx.x * 16;            // 16 consecutive values of head c0 / 128
+  float ov[16], zv[16];
   {
-    float acc[8][4];
+    const uint4* op = reinterpret_cast<const uint4*>(o + tok * (HV * D) + c0);
+    const uint4* zp = reinterpret_cast<const uint4*>(z + tok * ldz + c0);
 #pragma unroll
-    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int i = 0; i < 2; ++i) {
+      uint4 a = op[i], bz = zp[i];
+      const __half2* ah = reinterpret_cast<const __half2*>(&a);
+      const __half2* zh = reinterpret_cast<const __half2*>(&bz);
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(a, a_addr(sQ, LDH, warp * 16, ks * 16, lane));
-#pragma unroll
-      for (int n = 0; n < 8; n += 2) {
-        uint32_t bq[4];
-        ldsm_x4(bq, bn_addr(sK, LDH, n * 8, ks * 16, lane));
-        mma16816(acc[n], a, bq[0], bq[1]);
-        mma16816(acc[n + 1], a, bq[2], bq[3]);
+      for (int j = 0; j < 4; ++j) {
+        const float2 fa = __half22float2(ah[j]), fz = __half22float2(zh[j]);
+        ov[8 * i + 2 * j] = fa.x; ov[8 * i + 2 * j + 1] = fa.y;
+        zv[8 * i + 2 * j] = fz.x; zv[8 * i + 2 * j + 1] = fz.y;
       }
     }
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = warp * 16 + gq + (e >= 2 ? 8 : 0);
-        const int col = n * 8 + 2 * tq + (e & 1);
-        acc[n][e] = (col <= r) ? acc[n][e] * __expf(s.gc[r] - s.gc[col]) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pa[j][0] = h2u(acc[2 * j][0], acc[2 * j][1]);
-      pa[j][1] = h2u(acc[2 * j][2], acc[2 * j][3]);
-      pa[j][2] = h2u(acc[2 * j + 1][0], acc[2 * j + 1][1]);
-      pa[j][3] = h2u(acc[2 * j + 1][2], acc[2 * j + 1][3]);
-    }
   }
-  // scale this warp's own Q rows by e^{g_r} (only this warp reads them)
-  __syncwarp();
-  for (int i = lane; i < 16 * (D / 2); i += 32) {
-    const int r = warp * 16 + i / (D / 2), c2 = (i % (D / 2)) * 2;
-    const float f = __expf(s.gc[r]);
-    const float2 qf = __half22float2(*reinterpret_cast<__half2*>(&s.Q[r][c2]));
-    *reinterpret_cast<__half2*>(&s.Q[r][c2]) = __floats2half2_rn(qf.x * f, qf.y * f);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss += ov[i] * ov[i];
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+  const float inv = rsqrtf(ss * (1.f / D) + 1e-6f);
+  const int wi = c0 % D;
+  uint32_t pk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(w + wi + 2 * j));
+    pk[j] = h2u(ov[2 * j] * inv * wf.x * silu_f(zv[2 * j]),
+                ov[2 * j + 1] * inv * wf.y * silu_f(zv[2 * j + 1]));
   }
-  __syncwarp();
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  // O = P U
-#pragma unroll
-  for (int ks = 0; ks < C / 16; ++ks) {
-#pragma unroll
-    for (int n = 0; n < 16; n += 2) {
-      uint32_t bq[4];
-      ldsm_x4_t(bq, bk_addr(sU, LDH, n * 8, ks * 16, lane));
-      mma16816(o[n], pa[ks], bq[0], bq[1]);
-      mma16816(o[n + 1], pa[ks], bq[2], bq[3]);
-    }
-  }
-  // O += (e^g Q) S0^T
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(a, a_addr(sQ, LDH, warp * 16, ks * 16, lane));
-#pragma unroll
-    for (int n = 0; n < 16; n += 2) {
-      uint32_t bq[4];
-      ldsm_x4(bq, bn_addr(sS, LDH, n * 8, ks * 16, lane));
-      mma16816(o[n], a, bq[0], bq[1]);
-      mma16816(o[n + 1], a, bq[2], bq[3]);
-    }
-  }
-  const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int r = warp * 16 + gq + hf * 8;
-    float inv = 1.f;
-    if (z) {
-      float ss = 0.f;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        const float a0 = o[n][2 * hf] * scale, a1 = o[n][2 * hf + 1] * scale;
-        ss += a0 * a0 + a1 * a1;
-      }
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      inv = rsqrtf(ss * (1.f / D) + 1e-6f);
-    }
-    if (r >= nvalid) continue;
-    const int64_t tok = t0 + r;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int col = n * 8 + 2 * tq;
-      float a0 = o[n][2 * hf] * scale, a1 = o[n][2 * hf + 1] * scale;
-      if (z) {
-        const float2 zf = __half22float2(*reinterpret_cast<const __half2*>(z + tok * ldz + h * D + col));
-        const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(o_norm + col));
-        a0 = a0 * inv * wf.x * silu_f(zf.x);
-        a1 = a1 * inv * wf.y * silu_f(zf.y);
-      }
-      *reinterpret_cast<uint32_t*>(out + tok * ldo + h * D + col) = h2u(a0, a1);
-    }
-  }
+  uint4* yp = reinterpret_cast<uint4*>(y + tok * ldy + c0);
+  yp[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  yp[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
 }  // namespace gdn
 
 static inline size_t al256g(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t gdn_scan_workspace_bytes(int64_t B, int64_t L) {
+size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   const int64_t M = B * L;
   const int64_t nch = (L + gdn::C - 1) / gdn::C;
   size_t n = 0;
-  n += al256g(M * gdn::HV * 4);                         // g (from alpha)
-  n += al256g(M * gdn::HV * 4);                         // gcum
-  n += al256g(M * gdn::HV * gdn::D * 2);                // W
-  n += al256g(M * gdn::HV * gdn::D * 4);                // U'
-  n += al256g(M * gdn::HV * gdn::D * 2);                // U
-  n += al256g(M * gdn::HV * gdn::D * 2);                // decayed keys
-  n += al256g(B * nch * gdn::HV * gdn::D * gdn::D * 2); // entering states
+  n += al256g(M * gdn::HV * 4);                          // g (from alpha)
+  n += al256g(M * gdn::HV * 4);                          // gcum
+  n += al256g(M * gdn::HV * gdn::D * 2);                 // W
+  n += al256g(M * gdn::HV * gdn::D * 4);                 // U'
+  n += al256g(M * gdn::HV * gdn::D * 2);                 // decayed keys
+  n += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);  // Aqk
+  if (with_norm) n += al256g(M * gdn::HV * gdn::D * 2);  // o before the output gate
   return n;
 }
 
@@ -646,21 +595,22 @@ struct GdnWs {
   float* gcum;
   __half* W;
   float* U1;
-  __half* U;
   __half* Kt;
-  __half* S0;
+  __half* Aqk;
+  __half* o;
 };
 static GdnWs carve(void* ws, int64_t B, int64_t L) {
   const int64_t M = B * L;
+  const int64_t nch = (L + gdn::C - 1) / gdn::C;
   uint8_t* p = static_cast<uint8_t*>(ws);
   GdnWs w;
   w.g = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * 4);
   w.gcum = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * 4);
   w.W = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
   w.U1 = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * gdn::D * 4);
-  w.U = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
   w.Kt = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
-  w.S0 = reinterpret_cast<__half*>(p);
+  w.Aqk = reinterpret_cast<__half*>(p); p += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);
+  w.o = reinterpret_cast<__half*>(p);
   return w;
 }
 
@@ -671,8 +621,6 @@ static clef_status gdn_set_attrs() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::WySmem)));
   CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_state_pass_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::PassSmem)));
-  CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_chunk_out_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::OutSmem)));
   g_gdn_attr = true;
   return CLEF_OK;
 }
@@ -707,25 +655,29 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
   dim3 g1((unsigned)(B * nch), gdn::HV);
   const double C = gdn::C, D = gdn::D, HVd = gdn::HV, nchunks = (double)B * nch;
   {
-    TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 6.0 * C * C * D,
-                  (double)M * HVd * D * (2 + 2 + 2 + 4));
-    gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(k, v, g, beta, w.gcum, w.W,
-                                                                        w.U1, w.Kt, (int)L, nch);
+    TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 8.0 * C * C * D,
+                  (double)M * HVd * D * (2 + 2 + 2 + 2 + 4) + nchunks * HVd * C * C * 2);
+    gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(
+        q, k, v, g, beta, w.gcum, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch);
     CLEF_LAUNCH_CHECK();
   }
+  __half* o = z ? w.o : out;
+  const int64_t ldo_pass = z ? (int64_t)gdn::HV * gdn::D : ldo;
   {
-    TraceScope ts(stream, "gdn_state_pass", nchunks * HVd * 4.0 * C * D * D,
-                  (double)M * HVd * D * (2 + 4 + 2) + (double)M * 16 * D * 2 + nchunks * HVd * D * D * 2);
-    gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * (gdn::D / gdn::SL)), 128,
-                                 sizeof(gdn::PassSmem), stream>>>(w.Kt, w.W, w.U1, w.gcum, s0, w.U,
-                                                                  w.S0, s_out, (int)L, nch);
+    TraceScope ts(stream, "gdn_state_pass",
+                  nchunks * HVd * (6.0 * C * D * D + 2.0 * C * C * D),
+                  (double)M * HVd * D * (2 + 2 + 4 + 2) + (double)M * 16 * D * 2 +
+                      nchunks * HVd * C * C * 2);
+    constexpr int nsl = gdn::D / (16 * gdn::SW);
+    gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * nsl), 32 * gdn::SW,
+                                 sizeof(gdn::PassSmem), stream>>>(q, w.Kt, w.W, w.U1, w.Aqk, w.gcum,
+                                                                  s0, o, ldo_pass, s_out, (int)L,
+                                                                  nch);
     CLEF_LAUNCH_CHECK();
   }
-  {
-    TraceScope ts(stream, "gdn_chunk_out", nchunks * HVd * (4.0 * C * C * D + 2.0 * C * D * D),
-                  (double)M * HVd * D * (2 + 2 + 2) + (double)M * 32 * D * 2 * 2 + nchunks * HVd * D * D * 2);
-    gdn::gdn_chunk_out_kernel<<<g1, 128, sizeof(gdn::OutSmem), stream>>>(
-        q, k, w.U, w.S0, w.gcum, z, ldz, o_norm, out, ldo, (int)L, nch);
+  if (z) {
+    TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);
+    gdn::gdn_gated_norm_kernel<<<(unsigned)M, 256, 0, stream>>>(o, z, ldz, o_norm, out, ldo);
     CLEF_LAUNCH_CHECK();
   }
   return CLEF_OK;

@@ -8,7 +8,8 @@ namespace clef {
 clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
                             __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream);
 
-size_t gdn_scan_workspace_bytes(int64_t B, int64_t L);
+// with_norm: room for o before the output gate (decoder layer path, z != NULL)
+size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm);
 
 // The chunked scan.  Exactly one of g (log alpha) / alpha is non-NULL.  With z != NULL the
 // output is the z-gated RMSNorm (weight o_norm) of o; otherwise o itself.  out [M, ldo] fp16.

@@ -63,7 +63,7 @@ clef_status clef_gdn_prefill_noalloc(const uint16_t* q, const uint16_t* k, const
     set_error("clef_gdn_prefill_noalloc: L = %lld is above %d", (long long)L, CLEF_MAX_LEN);
     return CLEF_E_TOO_LONG;
   }
-  const size_t need = gdn_scan_workspace_bytes(B, L);
+  const size_t need = gdn_scan_workspace_bytes(B, L, false);
   if (need > kStaticScratchBytes) {
     set_error("clef_gdn_prefill_noalloc: B=%lld, L=%lld needs %zu bytes of scratch, above the "
               "built-in %zu (use clef_gdn_prefill with a workspace instead)",

@@ -142,9 +142,8 @@ CLEF_API clef_status clef_gdn_prefill(const uint16_t* q, const uint16_t* k, cons
  * same inputs and outputs as clef_gdn_prefill but no workspace: its scratch is one array of
  * CLEF_GDN_NOALLOC_SCRATCH_BYTES (64 MiB) with static storage in the library, which every GPU
  * that loads the library keeps reserved until the process exits.  Sizes whose scratch
- * (clef_gdn_workspace_size(B, L), about 33 KB per position plus 1 MiB per 64-position chunk of
- * each request) exceeds it are refused with CLEF_E_SHAPE; one request of up to 1,024 positions
- * always fits.  The first call on a device looks up the array's device address (with that device
+ * (clef_gdn_workspace_size(B, L), about 37 KB per position) exceeds it are refused with
+ * CLEF_E_SHAPE; one request of up to 1,024 positions always fits.  The first call on a device looks up the array's device address (with that device
  * current), so make that first call before any stream capture.  All calls share the one array
  * and it keeps the last call's contents; nothing in it has to start at zero.  Two calls that run
  * on the GPU at the same time (other streams, other threads) race on it: serialise them.
