@@ -6,19 +6,20 @@
 //
 // GEMM design (sm_103a): Y[m, n] = sum_k X[m, k] * T[n/16][idx[n, k]], computed as the
 // transposed product D[n, m] = W X^T so that the weights are the MMA's A operand, held in tensor
-// memory, and never pass through shared memory.  Work unit: a pair of CTAs (a 2-CTA cluster) on
-// 256 output channels x 256 tokens, K walked in blocks of 64 through an 8-stage ring:
-//   * warp 0 of each CTA loads its half of the X tile (128 tokens x 64, 128-byte swizzle; the
-//     completion is counted on the leader CTA's barrier) and the 8 packed 768-byte blocks of its
-//     own 128 rows (tiled layout, see clef_lut6_tile);
-//   * warps 4..11 of each CTA dequantise its 128 rows: each warp owns one 16-row table group and
-//     writes its 16 x 64 weights straight into a tensor-memory A stage with one
-//     tcgen05.st.16x256b.x4; all lookups of a warp hit one 64-entry table (128 bytes, one entry
-//     pair per bank) and never conflict; the 32 indices a lane needs are 24 contiguous bytes;
-//   * one thread of the leader CTA issues tcgen05.mma.cta_group::2 (M = 256 channels, 128 from
-//     each CTA's tensor memory; N = 256 tokens, 128 from each CTA's shared memory; K = 16), so
-//     each SM reads only its own half of X; commits are multicast to both CTAs;
-//   * each CTA drains its 128 x 256 fp32 accumulator with tcgen05.ld into shared memory in
+// memory, and never pass through shared memory:
+//   * one CTA per 128 (output channels) x 256 (tokens) tile, K walked in blocks of 64;
+//   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and of the 8
+//     packed 768-byte blocks of the tile's rows (tiled layout, see clef_lut6_tile) into a 4-stage
+//     ring;
+//   * warps 4..11 dequantise: each warp owns one 16-row table group and writes its 16 x 64
+//     weights straight into a tensor-memory A stage with one tcgen05.st.16x256b.x4; every
+//     lookup of a warp hits the same 64-entry table (128 bytes, one entry pair per bank), so the
+//     lookups never conflict; in the tiled layout the 32 indices a lane's fragment needs are 24
+//     contiguous bytes (three 8-byte loads), and index*2 is cut into the table address with one
+//     shift and one logic op per index;
+//   * warp 1 issues tcgen05.mma (M=128 channels from tensor memory, N=256 tokens from shared
+//     memory, K=16) into a 128 x 256 fp32 accumulator in tensor memory;
+//   * the epilogue (warps 4..11) drains the accumulator with tcgen05.ld into shared memory in
 //     token-major order and writes Y coalesced (fp16 or fp32 store, fp32 residual add, or SwiGLU
 //     of an interleaved gate/up tile).
 // The dense weight never reaches global memory.
@@ -31,15 +32,14 @@
 namespace clef {
 namespace lut {
 
-constexpr int BN = 128;                       // output channels per CTA (pair: 256)
-constexpr int BT = 256;                       // tokens per pair: MMA N
-constexpr int BT_HALF = BT / 2;               // tokens held by each CTA
+constexpr int BN = 128;                       // output channels per tile: MMA M (A operand)
+constexpr int BT = 256;                       // tokens per tile: MMA N (B operand)
 constexpr int BK = 64;
-constexpr int STAGES = 8;
-constexpr int X_BYTES = BT_HALF * BK * 2;     // 16 KB per CTA per stage
+constexpr int STAGES = 4;
+constexpr int X_BYTES = BT * BK * 2;          // 32 KB
 constexpr int P_BLOCK = 768;                  // packed bytes of one 16-row group per k-block
 constexpr int P_BYTES = (BN / 16) * P_BLOCK;  // 6 KB
-constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the CTA's rows
+constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the tile's rows
 constexpr int NUM_DQ_WARPS = 8;               // one per 16-row group
 constexpr int NUM_THREADS = 32 * (4 + NUM_DQ_WARPS);
 constexpr int TMEM_COLS = 512;
@@ -49,8 +49,7 @@ constexpr int OFF_X = 0;                      // also the epilogue's staging are
 constexpr int OFF_P = OFF_X + STAGES * X_BYTES;
 constexpr int OFF_T = OFF_P + STAGES * P_BYTES;
 constexpr int OFF_BAR = OFF_T + TBL_BYTES;
-constexpr int NUM_BARS = 4 * STAGES + 1;
-constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_SLOT = OFF_BAR + 16 * 8;
 constexpr int SMEM_USED = OFF_SLOT + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -142,23 +141,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();          // 0 = leader of the pair
-  const int n0 = (blockIdx.x >> 1) * (2 * BN) + (int)rank * BN;
+  const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * BT;
   const int num_kb = K / BK;
 
-  const uint32_t bar_xfull = sb + OFF_BAR;                   // [STAGES] leader: both X halves
-  const uint32_t bar_pfull = sb + OFF_BAR + 8 * STAGES;      // [STAGES] own packed weights
-  const uint32_t bar_aready = sb + OFF_BAR + 16 * STAGES;    // [STAGES] leader: both A stages
-  const uint32_t bar_empty = sb + OFF_BAR + 24 * STAGES;     // [STAGES] MMAs of a stage done
-  const uint32_t bar_acc = sb + OFF_BAR + 32 * STAGES;
+  const uint32_t bar_full = sb + OFF_BAR;                   // [STAGES] X + packed landed
+  const uint32_t bar_aready = sb + OFF_BAR + 8 * STAGES;    // [STAGES] A stage written
+  const uint32_t bar_empty = sb + OFF_BAR + 16 * STAGES;    // [STAGES] MMAs of a stage done
+  const uint32_t bar_acc = sb + OFF_BAR + 24 * STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_xfull + 8 * s, 1);
-      mbar_init(bar_pfull + 8 * s, 1);
-      mbar_init(bar_aready + 8 * s, 2 * NUM_DQ_WARPS);
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_aready + 8 * s, NUM_DQ_WARPS);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc, 1);
@@ -167,57 +163,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmap_p);
   }
   if (warp == 1) {
-    tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish2();
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // barriers of both CTAs initialised, tensor memory of both allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- loads (both CTAs)
+    // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1;
-        if (kb >= STAGES && !mbar_wait_cl(bar_empty + 8 * s, ph ^ 1, status, DEV_TIMEOUT_TMA)) break;
-        if (rank == 0) mbar_arrive_expect_tx(bar_xfull + 8 * s, 2 * X_BYTES);
-        tma_load_2d_pair(sb + OFF_X + s * X_BYTES, &tmap_x, mapa_shared(bar_xfull + 8 * s, 0),
-                         kb * BK, m0 + (int)rank * BT_HALF);
-        mbar_arrive_expect_tx(bar_pfull + 8 * s, P_BYTES);
+        if (kb >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1, status, DEV_TIMEOUT_TMA)) break;
+        mbar_arrive_expect_tx(bar_full + 8 * s, X_BYTES + P_BYTES);
+        tma_load_2d(sb + OFF_X + s * X_BYTES, &tmap_x, bar_full + 8 * s, kb * BK, m0);
         // the 8 groups' 768-byte blocks of k-block kb: box {256 B, 3, 8 groups}
-        tma_load_3d(sb + OFF_P + s * P_BYTES, &tmap_p, bar_pfull + 8 * s, 0, 3 * kb, n0 / 16);
+        tma_load_3d(sb + OFF_P + s * P_BYTES, &tmap_p, bar_full + 8 * s, 0, 3 * kb, n0 / 16);
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (leader)
-    if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(2 * BN, BT);
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BN, BT);
       bool ok = true;
       for (int kb = 0; kb < num_kb && ok; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1;
-        ok = mbar_wait_cl(bar_xfull + 8 * s, ph, status, DEV_TIMEOUT_MMA) &&
-             mbar_wait_cl(bar_aready + 8 * s, ph, status, DEV_TIMEOUT_MMA);
+        ok = mbar_wait(bar_full + 8 * s, ph, status, DEV_TIMEOUT_MMA) &&
+             mbar_wait(bar_aready + 8 * s, ph, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t bd = sdesc_k_sw128(sb + OFF_X + s * X_BYTES + kk * 32);
-          tc_mma2_f16_ts(tmem, tmem + A_COL + s * 32 + kk * 8, bd, idesc, (kb | kk) != 0);
+          tc_mma_f16_ts(tmem, tmem + A_COL + s * 32 + kk * 8, bd, idesc, (kb | kk) != 0);
         }
-        tc_commit2_mc(bar_empty + 8 * s, 3);
+        tc_commit(bar_empty + 8 * s);
       }
-      tc_commit2_mc(bar_acc, 3);
+      tc_commit(bar_acc);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- dequant, then epilogue
     const int dq = warp - 4;              // 0..7
     const int t = threadIdx.x - 128;      // 0..255
     {
-      // the CTA's 8 tables (rows n0 .. n0+127); groups past N read as zero
+      // the tile's 8 tables (rows n0 .. n0+127); groups past N read as zero
       const int e = t * 2;
       const int g = n0 / 16 + e / 64;
       uint32_t v = 0u;
@@ -233,14 +226,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int kb = 0; kb < num_kb; ++kb) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
-      // pfull[s] completing implies the producer saw empty[s] of the previous round, so the
+      // full[s] completing implies the producer saw empty[s] of the previous round, so the
       // MMAs that read A stage s before have finished as well.
-      if (!mbar_wait(bar_pfull + 8 * s, ph, status, DEV_TIMEOUT_DEQUANT)) {
+      if (!mbar_wait(bar_full + 8 * s, ph, status, DEV_TIMEOUT_DEQUANT)) {
         ok = false;
         break;
       }
-      // this lane's 24 bytes: quadruples j = 0..3 of its row, then of the row 8 below
-      const uint32_t pa = sb + OFF_P + s * P_BYTES + grp * P_BLOCK + lane * 24;
+      // this lane's 24 bytes: quadruples j = 0..3 of row r0, then of row r0 + 8
+      const uint32_t pa = sb + OFF_P + s * P_BYTES + (grp & 7) * P_BLOCK + lane * 24;
       uint32_t w[6];
       lds_v2(pa, w[0], w[1]);
       lds_v2(pa + 8, w[2], w[3]);
@@ -261,10 +254,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_aready + 8 * s, 0));
+      if (lane == 0) mbar_arrive(bar_aready + 8 * s);
     }
     // ---- epilogue: accumulator (lane = channel, column = token) -> shared, token-major fp32
-    const bool got = ok && mbar_wait_cl(bar_acc, 0, status, DEV_TIMEOUT_EPILOGUE);
+    const bool got = ok && mbar_wait(bar_acc, 0, status, DEV_TIMEOUT_EPILOGUE);
     if (got) {
       tc_fence_after();
       float* stg = reinterpret_cast<float*>(smem + OFF_X);
@@ -288,7 +281,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tok = t >> 3; tok < BT; tok += 32) {
           const int row = m0 + tok;
           if (row >= M) break;
-          if (n0 >= N) break;
           const float4* gp = reinterpret_cast<const float4*>(stg + tok * BN + c8);
           const float4* up = reinterpret_cast<const float4*>(stg + tok * BN + BN / 2 + c8);
           const float4 g0 = gp[0], g1 = gp[1], u0 = up[0], u1 = up[1];
@@ -330,10 +322,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // both CTAs are done with tensor memory and with each other's barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc2(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -385,13 +376,13 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   if (M == 0) return CLEF_OK;
   CUtensorMap tx, tp;
   if (tma_encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)K, (uint64_t)M,
-                    (uint64_t)K * 2, BK, BT_HALF, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+                    (uint64_t)K * 2, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
     return CLEF_E_CUDA;
   {
     // tiled weights as [N/16 groups][3 * K/64][256 bytes]; groups past N read as zero
     const uint64_t dims[3] = {256, (uint64_t)(3 * (K / BK)), (uint64_t)(N / 16)};
     const uint64_t st[2] = {256, (uint64_t)(K / BK) * P_BLOCK};
-    const uint32_t box[3] = {256, 3, BN / 16};  // one CTA's 8 groups
+    const uint32_t box[3] = {256, 3, BN / 16};
     if (tma_encode(&tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, tiled, dims, st, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
       return CLEF_E_CUDA;
@@ -402,27 +393,16 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     attr_set = true;
   }
-  dim3 grid((unsigned)(2 * ((N + 2 * BN - 1) / (2 * BN))), (unsigned)((M + BT - 1) / BT));
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BT - 1) / BT));
   const double out_bytes = mode == EPI_F16 ? 2.0 * M * N
                            : mode == EPI_F32 ? 4.0 * M * N
                            : mode == EPI_ADD_F32 ? 8.0 * M * N
                                                  : 1.0 * M * N;  // SwiGLU: fp16 [M, N/2]
   TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
                 0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  CLEF_CUDA_CHECK(cudaLaunchKernelEx(&cfg, lut6_gemm_kernel, tx, tp, lut, y, ldy, (int)M, (int)N,
-                                     (int)K, mode, status_word_ptr()));
+  lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
 
