@@ -11,15 +11,17 @@
 //   * warp 0 issues TMA loads of the X tile (256 tokens x 64, 128-byte swizzle) and of the 8
 //     packed 768-byte blocks of the tile's rows (tiled layout, see clef_lut6_tile) into a 4-stage
 //     ring;
-//   * warps 4..11 dequantise: each warp owns one 16-row table group and writes its 16 x 64
-//     weights straight into a tensor-memory A stage with one tcgen05.st.16x256b.x4; every
+//   * warps 4..19 dequantise: each warp owns one 16-row table group on every other k-block and
+//     writes its 16 x 64 weights straight into a tensor-memory A stage with one
+//     tcgen05.st.16x256b.x4 (two warps per group take turns, so each has two MMA periods to
+//     cover its chain of dependent loads); every
 //     lookup of a warp hits the same 64-entry table (128 bytes, one entry pair per bank), so the
 //     lookups never conflict; in the tiled layout the 32 indices a lane's fragment needs are 24
 //     contiguous bytes (three 8-byte loads), and index*2 is cut into the table address with one
 //     shift and one logic op per index;
 //   * warp 1 issues tcgen05.mma (M=128 channels from tensor memory, N=256 tokens from shared
 //     memory, K=16) into a 128 x 256 fp32 accumulator in tensor memory;
-//   * the epilogue (warps 4..11) drains the accumulator with tcgen05.ld into shared memory in
+//   * the epilogue (warps 4..19) drains the accumulator with tcgen05.ld into shared memory in
 //     token-major order and writes Y coalesced (fp16 or fp32 store, fp32 residual add, or SwiGLU
 //     of an interleaved gate/up tile).
 // The dense weight never reaches global memory.
@@ -40,7 +42,7 @@ constexpr int X_BYTES = BT * BK * 2;          // 32 KB
 constexpr int P_BLOCK = 768;                  // packed bytes of one 16-row group per k-block
 constexpr int P_BYTES = (BN / 16) * P_BLOCK;  // 6 KB
 constexpr int TBL_BYTES = (BN / 16) * 64 * 2; // 1 KB: the 8 tables of the tile's rows
-constexpr int NUM_DQ_WARPS = 8;               // one per 16-row group
+constexpr int NUM_DQ_WARPS = 16;              // two per 16-row group (even / odd k-blocks)
 constexpr int NUM_THREADS = 32 * (4 + NUM_DQ_WARPS);
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t A_COL = BT;                // A stages: 32 columns each from column 256
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_aready + 8 * s, NUM_DQ_WARPS);
+      mbar_init(bar_aready + 8 * s, NUM_DQ_WARPS / 2);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc, 1);
@@ -207,9 +209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- dequant, then epilogue
-    const int dq = warp - 4;              // 0..7
-    const int t = threadIdx.x - 128;      // 0..255
-    {
+    const int dq = warp - 4;              // 0..15
+    const int t = threadIdx.x - 128;      // 0..511
+    if (t < 256) {
       // the tile's 8 tables (rows n0 .. n0+127); groups past N read as zero
       const int e = t * 2;
       const int g = n0 / 16 + e / 64;
@@ -219,11 +221,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     named_bar_sync(1, 32 * NUM_DQ_WARPS);
     const int quarter = warp & 3;         // TMEM lanes 32*quarter .. (this warp's access window)
-    const int grp = 2 * quarter + (dq >> 2);          // 16-row group of this warp
+    const int grp = 2 * quarter + ((dq >> 2) & 1);    // 16-row group of this warp
+    const int par = dq >> 3;                          // k-blocks kb with kb % 2 == par
     const uint32_t tb = sb + OFF_T + grp * 128;
     const uint32_t tl = tmem + ((uint32_t)(grp * 16) << 16) + A_COL;
     bool ok = true;
-    for (int kb = 0; kb < num_kb; ++kb) {
+    for (int kb = par; kb < num_kb; kb += 2) {
       const int s = kb % STAGES;
       const uint32_t ph = (kb / STAGES) & 1;
       // full[s] completing implies the producer saw empty[s] of the previous round, so the
@@ -256,15 +259,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_aready + 8 * s);
     }
-    // ---- epilogue: accumulator (lane = channel, column = token) -> shared, token-major fp32
+    // ---- epilogue: accumulator (lane = channel, column = token) -> shared, token-major fp32;
+    //      warp dq takes TMEM lanes 32 (dq & 3).. and token columns 64 (dq >> 2) .. +63
     const bool got = ok && mbar_wait(bar_acc, 0, status, DEV_TIMEOUT_EPILOGUE);
     if (got) {
       tc_fence_after();
       float* stg = reinterpret_cast<float*>(smem + OFF_X);
       const int ch = quarter * 32 + lane;
-      const int tok0 = (dq >> 2) * 128;
+      const int tok0 = (dq >> 2) * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + tok0 + c * 32, r);
         tc_wait_ld();
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (mode == EPI_SWIGLU_F16) {
         const int c8 = (t & 7) * 8;
 #pragma unroll 1
-        for (int tok = t >> 3; tok < BT; tok += 32) {
+        for (int tok = t >> 3; tok < BT; tok += 64) {
           const int row = m0 + tok;
           if (row >= M) break;
           const float4* gp = reinterpret_cast<const float4*>(stg + tok * BN + c8);
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int c8 = (t & 15) * 8;
         const bool col_ok = n0 + c8 < N;
 #pragma unroll 1
-        for (int tok = t >> 4; tok < BT; tok += 16) {
+        for (int tok = t >> 4; tok < BT; tok += 32) {
           const int row = m0 + tok;
           if (row >= M) break;
           if (!col_ok) continue;
