@@ -19,7 +19,7 @@ INTER = 12288
 GDN_HK, GDN_HV, GDN_D = 16, 32, 128
 ATT_HQ, ATT_HKV, ATT_D = 16, 4, 256
 MAX_LEN = 16384
-SWIGLU_BLOCK = 64
+SWIGLU_BLOCK = 16
 
 STATUS_NAMES = {
     0: "CLEF_OK", 1: "CLEF_E_INVALID", 2: "CLEF_E_SHAPE", 3: "CLEF_E_TOO_LONG", 4: "CLEF_E_ALIGN",

@@ -8,12 +8,12 @@ enum Epilogue : int {
   EPI_F16 = 0,        // y fp16 = acc
   EPI_F32 = 1,        // y fp32 = acc
   EPI_ADD_F32 = 2,    // y fp32 += acc (residual add, in place)
-  EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up of a gate/up tile interleaved by 64 rows
+  EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up, gate/up rows interleaved by 16
 };
 
 // y[m, n] (row stride ldy elements) = x[m, k] . W^T with W in the tiled layout
-// (clef_lut6_tile).  Requires n % 16 == 0, k % 64 == 0 (and n % 128 == 0 for EPI_SWIGLU_F16);
-// x packed [m, k].
+// (clef_lut6_tile).  Requires n % 16 == 0, k % 64 == 0 (n % 32 == 0 for EPI_SWIGLU_F16), x packed
+// [m, k], lut 16-byte aligned.
 clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
                              cudaStream_t stream);

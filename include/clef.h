@@ -68,7 +68,7 @@ typedef enum {
 /* Longest prefill the provider's code reads ("clef-flash-LiteRT" README, section "Limits"). */
 #define CLEF_MAX_LEN 16384
 /* Rows per block in the interleaved gate/up weight of the SwiGLU MLP (see clef_layer). */
-#define CLEF_SWIGLU_BLOCK 64
+#define CLEF_SWIGLU_BLOCK 16
 
 typedef void* clef_stream; /* a cudaStream_t */
 
@@ -192,9 +192,9 @@ typedef struct {
      attention: rows [query 4096 | gate 4096 | k 1024 | v 1024] = [10240, 4096]. */
   clef_lut6 in_proj;
   clef_lut6 out_proj;        /* [4096, 4096] */
-  /* MLP gate and up, interleaved in blocks of CLEF_SWIGLU_BLOCK (64) rows: rows
-     [128j, 128j+64) are gate rows [64j, 64j+64), rows [128j+64, 128j+128) are up rows
-     [64j, 64j+64).  [24576, 4096]. */
+  /* MLP gate and up, interleaved in blocks of CLEF_SWIGLU_BLOCK (16) rows, one table group
+     each: rows [32j, 32j+16) are gate rows [16j, 16j+16), rows [32j+16, 32j+32) are up rows
+     [16j, 16j+16).  [24576, 4096]. */
   clef_lut6 gate_up;
   clef_lut6 down;            /* [4096, 12288] */
   /* GDN only (NULL for attention layers), fp16: */
