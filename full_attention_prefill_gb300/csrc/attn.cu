@@ -76,31 +76,36 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
 // ------------------------------------------------------------------------------------------
 // tcgen05 flash attention.  CTA = 128 rows (32 positions x the 4 query heads of kv head g), keys
 // in tiles of 64, two K/V stages.
-//   warp 0   TMA: Q once (4 boxes of 64 dims, 128-byte swizzle), then K and V tiles
-//   warp 1   MMA: S_j = Q K_j^T (M=128, N=64, 16 steps of K=16) into one of two 64-column
-//            TMEM buffers; O += P_{j-1} V_{j-1} (M=128, N=256, K=64) with P read from TMEM and
+//   warp 0   TMA: K and V tiles (4 boxes of 64 dims, 128-byte swizzle)
+//   warp 1   MMA: S_j = Q K_j^T (M=128, N=64, 16 steps of K=16; Q from tensor memory, so only
+//            K streams through shared memory) into one of two 64-column TMEM buffers; O += P_{j-1} V_{j-1} (M=128, N=256, K=64) with P read from TMEM and
 //            V an MN-major shared operand; O is a 256-column fp32 TMEM accumulator
-//   warps 4-7 softmax, one thread per row: read S, mask, online max/sum in base 2, write P
-//            (fp16) over the first 32 columns of its S buffer.  O is rescaled (in TMEM) only
-//            when a row's max grows by more than 2^8, so P stays below 256; the final O is
-//            divided by the row sum, multiplied by sigmoid(gate) and stored.
+//   warps 4-11 first copy Q (rows of 256 dims, after rotary) from global memory into tensor
+//            memory; then softmax, two threads per row (warps w and w+4 share TMEM lanes 32 (w % 4)..;
+//            warps 4-7 take keys 0..31 of a tile, warps 8-11 keys 32..63): read S, mask, online
+//            max/sum in base 2 with the two halves' maxima combined through shared memory, write
+//            P (fp16) over the first 32 columns of its S buffer.  O is rescaled (in TMEM, each
+//            half of its columns by one of the two threads) only when a row's max grows by more
+//            than 2^8, so P stays below 256; the final O is divided by the row sum, multiplied
+//            by sigmoid(gate) and stored.
 // ------------------------------------------------------------------------------------------
 constexpr int TBN = 64;                   // keys per tile
-constexpr int Q_BYTES = BM * D * 2;       // 64 KB: 4 blocks [128 rows][64 dims]
 constexpr int KV_BYTES = TBN * D * 2;     // 32 KB: 4 blocks [64 keys][64 dims]
 constexpr int KV_BLOCK = TBN * 128;       // 8 KB
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
-constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+constexpr int KVS = 3;                    // K/V stages
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + KVS * KV_BYTES;
+constexpr int OFF_BAR = OFF_V + KVS * KV_BYTES;
 constexpr int OFF_SLOT = OFF_BAR + 16 * 8;
-constexpr int FLASH_SMEM = OFF_SLOT + 16 + 1024;
-constexpr int FLASH_THREADS = 256;
+constexpr int OFF_XCH = OFF_SLOT + 16;       // [2 halves][128 rows] fp32: row max / row sum
+constexpr int FLASH_SMEM = OFF_XCH + 2 * BM * 4 + 1024;
+constexpr int FLASH_THREADS = 384;
 constexpr uint32_t S_COL = 256;           // S/P buffers at TMEM columns 256 and 320
+constexpr uint32_t Q_COL = 384;           // Q (the MMA's A operand): 128 columns of fp16 pairs
 constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 units)
 
 __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
-    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __half* __restrict__ q, int64_t ldq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __half* __restrict__ gate, int64_t ldg,
     __half* __restrict__ out, int64_t ldo, int L, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -117,26 +122,29 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   const int nt = last_pos / TBN + 1;
 
   const uint32_t bar_q = sb + OFF_BAR;
-  const uint32_t bar_k = bar_q + 8;         // [2]
-  const uint32_t bar_v = bar_q + 24;        // [2]
-  const uint32_t bar_empty = bar_q + 40;    // [2]
-  const uint32_t bar_s = bar_q + 56;        // [2]
-  const uint32_t bar_p = bar_q + 72;        // [2]
-  const uint32_t bar_o = bar_q + 88;
+  const uint32_t bar_k = bar_q + 8;         // [KVS] K tile landed
+  const uint32_t bar_v = bar_k + 8 * KVS;   // [KVS] V tile landed
+  const uint32_t bar_empty = bar_v + 8 * KVS;  // [KVS] MMAs done with a K/V stage
+  const uint32_t bar_s = bar_empty + 8 * KVS;  // [2] S_j complete
+  const uint32_t bar_p = bar_s + 16;        // [2] P_j written
+  const uint32_t bar_o = bar_p + 16;        // each P V done
+  const uint32_t bar_fin = bar_o + 8;       // the last P V done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(bar_q, 8);  // the 8 warps that write Q into tensor memory
+    for (int i = 0; i < KVS; ++i) {
       mbar_init(bar_k + 8 * i, 1);
       mbar_init(bar_v + 8 * i, 1);
       mbar_init(bar_empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, 4);
+      mbar_init(bar_p + 8 * i, 8);
     }
     mbar_init(bar_o, 1);
+    mbar_init(bar_fin, 1);
     fence_mbar_init();
-    tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
   }
@@ -151,13 +159,10 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, Q_BYTES);
-      for (int blk = 0; blk < 4; ++blk)
-        tma_load_3d(sb + OFF_Q + blk * (BM * 128), &tq, bar_q, blk * 64, 4 * g, tb + p0);
       for (int j = 0; j < nt; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar_empty + 8 * s, ((j >> 1) & 1) ^ 1, status, DEV_TIMEOUT_TMA))
-          break;
+        const int s = j % KVS;
+        const uint32_t ph = (uint32_t)(j / KVS) & 1;
+        if (j >= KVS && !mbar_wait(bar_empty + 8 * s, ph ^ 1, status, DEV_TIMEOUT_TMA)) break;
         mbar_arrive_expect_tx(bar_k + 8 * s, KV_BYTES);
         for (int blk = 0; blk < 4; ++blk)
           tma_load_3d(sb + OFF_K + s * KV_BYTES + blk * KV_BLOCK, &tk, bar_k + 8 * s, blk * 64, g,
@@ -174,85 +179,118 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
       bool ok = mbar_wait(bar_q, 0, status, DEV_TIMEOUT_MMA);
       auto issue_pv = [&](int jj) -> bool {
-        const int sp = jj & 1;
+        const int sp = jj & 1;             // S/P buffer
+        const int sv = jj % KVS;           // K/V stage
         if (!mbar_wait(bar_p + 8 * sp, (jj >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
-            !mbar_wait(bar_v + 8 * sp, (jj >> 1) & 1, status, DEV_TIMEOUT_MMA))
+            !mbar_wait(bar_v + 8 * sv, (uint32_t)(jj / KVS) & 1, status, DEV_TIMEOUT_MMA))
           return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t bd = sdesc_mn_sw128(sb + OFF_V + sp * KV_BYTES + kk * 16 * 128, KV_BLOCK, 1024);
+          const uint64_t bd = sdesc_mn_sw128(sb + OFF_V + sv * KV_BYTES + kk * 16 * 128, KV_BLOCK, 1024);
           tc_mma_f16_ts(tmem, tmem + S_COL + sp * TBN + kk * 8, bd, idesc_o, (jj | kk) != 0);
         }
         tc_commit(bar_o);
-        tc_commit(bar_empty + 8 * sp);
+        tc_commit(bar_empty + 8 * sv);
         return true;
       };
       for (int j = 0; j < nt && ok; ++j) {
-        const int s = j & 1;
-        ok = mbar_wait(bar_k + 8 * s, (j >> 1) & 1, status, DEV_TIMEOUT_MMA);
+        const int s = j & 1;               // S/P buffer
+        const int sk = j % KVS;            // K/V stage
+        ok = mbar_wait(bar_k + 8 * sk, (uint32_t)(j / KVS) & 1, status, DEV_TIMEOUT_MMA);
+        // S buffer s still holds P_{j-2} until P_{j-2} V_{j-2} (issued last iteration) is done;
+        // P_{j-3} V_{j-3} was waited for the same way, so bar_o is at most one phase behind
+        if (ok && j >= 2) ok = mbar_wait(bar_o, (uint32_t)(j - 2) & 1, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_k_sw128(sb + OFF_Q + (kk >> 2) * (BM * 128) + (kk & 3) * 32);
           const uint64_t bd =
-              sdesc_k_sw128(sb + OFF_K + s * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32);
-          tc_mma_f16_ss(tmem + S_COL + s * TBN, ad, bd, idesc_s, kk != 0);
+              sdesc_k_sw128(sb + OFF_K + sk * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32);
+          tc_mma_f16_ts(tmem + S_COL + s * TBN, tmem + Q_COL + kk * 8, bd, idesc_s, kk != 0);
         }
         tc_commit(bar_s + 8 * s);
         if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) issue_pv(nt - 1);
+      if (ok && issue_pv(nt - 1)) tc_commit(bar_fin);
     }
   } else if (warp >= 4) {
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;                  // 0: keys 0..31 of a tile, 1: keys 32..63
     const int r = quarter * 32 + lane;                 // row of this thread
     const int pos = p0 + (r >> 2);
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [half][row]
     const float sl2 = 0.0625f * 1.4426950408889634f;  // 1/sqrt(256) in base 2
+    // the two warps of a lane quarter meet on named barrier 1 + quarter (64 threads)
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
+    {
+      // Q into tensor memory: row r, column Q_COL + c holds dims 2c, 2c+1 (the A-operand layout
+      // of kind::f16); this thread writes its row's dims 128 half .. 128 half + 127
+      const bool valid = pos < L;
+      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + half * 128;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 d = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 2 * c0) + i)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * i] = d.x;
+          qv[4 * i + 1] = d.y;
+          qv[4 * i + 2] = d.z;
+          qv[4 * i + 3] = d.w;
+        }
+        tmem_st_32x32b_x32(tl + Q_COL + half * 64 + c0, qv);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_q);
+    }
     float m_ref = -INFINITY, lsum = 0.f;
+    // Both threads of a row pass the same named barriers every iteration, whatever happens: a
+    // failed (timed-out) wait only turns the rest of the work off (ok is warp-uniform).
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
-      if (!mbar_wait(bar_s + 8 * s, (j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[64];
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld_32x32b_x32(tl + S_COL + s * TBN, lo);
-        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + 32, hi);
-      }
-      tc_wait_ld();
-      const int key0 = j * TBN;
+      ok = ok && mbar_wait(bar_s + 8 * s, (j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
+      ok = __all_sync(0xffffffffu, ok);
+      uint32_t sv[32];
       float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < TBN; ++c) {
-        float v = __uint_as_float(sv[c]) * sl2;
-        v = (key0 + c <= pos) ? v : -INFINITY;
-        sv[c] = __float_as_uint(v);
-        mt = fmaxf(mt, v);
-      }
-      const float m_new = fmaxf(m_ref, mt);
-      const bool need = m_new > m_ref + kRescale;
-      // P_j may only be published once P_{j-1} V_{j-1} has landed in O (tested: publishing it
-      // while that MMA is in flight corrupts O)
-      if (j > 0) {
-        if (!mbar_wait(bar_o, (j - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
-          ok = false;
-          break;
-        }
+      if (ok) {
         tc_fence_after();
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + half * 32, sv);
+        tc_wait_ld();
+        const int key0 = j * TBN + half * 32;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float v = __uint_as_float(sv[c]) * sl2;
+          v = (key0 + c <= pos) ? v : -INFINITY;
+          sv[c] = __float_as_uint(v);
+          mt = fmaxf(mt, v);
+        }
       }
+      // row max over both halves (the previous exchange's reads are fenced off by that
+      // exchange's second barrier)
+      xch[half * BM + r] = mt;
+      pair_sync();
+      mt = fmaxf(mt, xch[(half ^ 1) * BM + r]);
+      pair_sync();
+      if (!ok) continue;
+      const float m_new = fmaxf(m_ref, mt);
+      const bool need = m_new > m_ref + kRescale;      // the same in both threads of a row
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale this warp's O rows
+        // O may only be rescaled once P_{j-1} V_{j-1} has landed in it.  S_j being complete
+        // means every MMA issued before Q K_j^T, P_{j-2} V_{j-2} included, has completed, so
+        // bar_o is at most one phase behind and its parity test is unambiguous.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (j - 1) & 1, status, DEV_TIMEOUT_EPILOGUE));
+        if (!ok) continue;
+        tc_fence_after();
+        // rescale this warp's half (128 columns) of its O rows
         const float f = need ? exp2f(m_ref - m_new) : 1.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
           uint32_t ov[32];
           tmem_ld_32x32b_x32(tl + c0, ov);
           tc_wait_ld();
@@ -264,30 +302,34 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
         lsum *= f;
       }
       if (need) m_ref = m_new;
-      uint32_t pk[32];
+      uint32_t pk[16];
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < TBN / 2; ++c) {
+      for (int c = 0; c < 16; ++c) {
         const float e0 = exp2f(__uint_as_float(sv[2 * c]) - m_ref);
         const float e1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_ref);
         rs += e0 + e1;
         pk[c] = pack_half2(e0, e1);
       }
-      lsum += rs;
-      tmem_st_32x32b_x32(tl + S_COL + s * TBN, pk);
+      lsum += rs;  // this half's share of the row sum
+      tmem_st_32x32b_x16(tl + S_COL + s * TBN + half * 16, pk);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p + 8 * s);
     }
-    // epilogue: wait for the last P V, then O / l * sigmoid(gate)
-    if (ok && mbar_wait(bar_o, (nt - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+    // epilogue: wait for the last P V (its own barrier: bar_o may trail by two phases here), then
+    // O / l * sigmoid(gate), each thread of a row taking half of its columns
+    xch[half * BM + r] = lsum;
+    pair_sync();
+    lsum += xch[(half ^ 1) * BM + r];
+    if (ok && mbar_wait(bar_fin, 0, status, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const int hq = 4 * g + (r & 3);
       const int64_t row = (int64_t)tb + pos;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(tl + c0, ov);
         tc_wait_ld();
@@ -344,16 +386,10 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
                                          attn::FLASH_SMEM));
     attr = true;
   }
+  // Q rows are read with 16-byte loads
+  if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (ldq & 7) != 0) return CLEF_E_ALIGN;
   const uint64_t M = (uint64_t)(B * L);
-  CUtensorMap mq, mk, mv;
-  {
-    const uint64_t dims[3] = {256, 16, M};
-    const uint64_t st[2] = {512, (uint64_t)ldq * 2};
-    const uint32_t box[3] = {64, 4, attn::POS};
-    if (tma_encode(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, q, dims, st, box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
-      return CLEF_E_CUDA;
-  }
+  CUtensorMap mk, mv;
   {
     const uint64_t dims[3] = {256, 4, M};
     const uint32_t box[3] = {64, 1, attn::TBN};
@@ -369,7 +405,7 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
   TraceScope ts(stream, "flash_attn", 4.0 * attn::D * attn::HQ * (double)B * L * (L + 1) / 2.0,
                 (double)B * L * (16 + 4 + 4 + 16 + 16) * attn::D * 2.0);
   attn::flash_tc_kernel<<<grid, attn::FLASH_THREADS, attn::FLASH_SMEM, stream>>>(
-      mq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
+      q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
