@@ -24,10 +24,11 @@ def test_dequant_bit_exact(n, k):
     assert np.array_equal(w.view(np.uint16), ref.view(np.uint16))
 
 
-# (m, n, k): config-0 smoke size, ragged m, ragged n (not a multiple of the 256-row tile),
-# one k-block, several k-blocks with a ring wrap, and a tall m spanning many tiles
+# (m, n, k): config-0 smoke size, ragged m, ragged n (not a multiple of the 128-row tile),
+# one k-block, several k-blocks with a ring wrap, a tall m spanning many tiles, and two tall
+# cases spanning more CTAs than the GPU has SMs (persistent walk: several tiles per CTA)
 CASES = [(128, 4096, 4096), (77, 256, 128), (300, 784, 320), (1, 16, 64), (129, 512, 64 * 7),
-         (1000, 1024, 1024)]
+         (1000, 1024, 1024), (4100, 1296, 128), (2600, 2048, 64 * 3)]
 
 
 @pytest.mark.parametrize("m,n,k", CASES)
