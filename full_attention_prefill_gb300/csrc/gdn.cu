@@ -15,12 +15,11 @@
 //   gdn_chunk_wy    (parallel over chunks x heads): cumulative g, T by forward substitution,
 //                   W, U', the decayed keys exp(g_C - g) k and the intra-chunk matrix
 //                   Aqk = tril(Q K^T) o exp(g_r - g_s) / sqrt(128)
-//   gdn_state_pass  (sequential over chunks; one warp per 16 value rows of a head): the state
-//                   slice stays in mma accumulators and is reused in registers as the fp16
-//                   operand S0^T; per chunk U = U' - W S0^T, O = exp(g) Q S0^T / sqrt(128) + Aqk U,
-//                   S <- exp(g_C) S + U^T Kd, with U transposed in registers (movmatrix)
+//   gdn_state_tc    (gdn_state.cu; sequential over chunks, one CTA per value head): the state
+//                   stays in tensor memory; per chunk U = U' - W S0^T, S <- exp(g_C) S + U^T Kd,
+//                   O = exp(g) Q S0^T / sqrt(128) + Aqk U, all on tcgen05
 //   gdn_gated_norm  (decoder layer only): y = RMSNorm_128(O) * w_o * SiLU(z)
-// All products run on tensor cores (mma.sync m16n8k16, fp16 inputs, fp32 accumulation); the
+// The chunk phase's products run on mma.sync (m16n8k16, fp16 inputs, fp32 accumulation); the
 // state and the scalars stay fp32.
 #include <algorithm>
 
@@ -31,10 +30,6 @@
 namespace clef {
 namespace gdn {
 
-constexpr int C = 64;          // chunk width
-constexpr int D = 128;         // head size (key and value)
-constexpr int HV = 32;         // value heads
-constexpr int HK = 16;         // key heads
 constexpr int LDH = D + 8;     // padded fp16 row (272 bytes) for conflict-free ldmatrix
 constexpr float kLogAlphaMin = -30.0f;
 
@@ -144,7 +139,7 @@ struct WySmem {
 
 __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const __half* __restrict__ qq, const __half* __restrict__ kk, const __half* __restrict__ vv,
-    const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ gcum,
+    const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ ef,
     __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Ktout,
     __half* __restrict__ Aqk, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
@@ -187,7 +182,8 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (tid < C && tid < nvalid) gcum[(t0 + tid) * HV + h] = s.gc[tid];
+  // exp of the cumulative log alpha for the state pass (rows past the end repeat the last one)
+  if (tid < C) ef[((int64_t)cg * HV + h) * C + tid] = __expf(s.gc[tid]);
   const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
   if (tid < C) {
     s.eb[tid] = s.bt[tid] * __expf(s.gc[tid]);
@@ -314,217 +310,6 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
-// Phase 2: the fused state pass.  CTA = (request, value head, 32 value rows); warp w owns value
-// rows 16w.. of that slice.  Per chunk (all data prefetched by cp.async one chunk ahead):
-//   SB   = fp16 B fragments of S0^T, taken straight from the fp32 state accumulators
-//   U    = U' - W S0^T                               (rows past the end set to zero)
-//   UT   = U transposed in registers (movmatrix): A fragments of U^T, B fragments of U
-//   O    = exp(g) / sqrt(128) * (Q S0^T) + Aqk U     -> out
-//   S   <- exp(g_C) S + U^T Kd
-// One barrier per chunk (the two warps share the prefetched tiles).
-// ------------------------------------------------------------------------------------------
-constexpr int SW = 2;              // warps (16-row value slices) per CTA
-struct PassBuf {
-  __half W[C][LDH];
-  __half Q[C][LDH];
-  __half K[C][LDH];       // decayed keys
-  __half Aq[C][C + 8];
-  float U[SW][C][16 + 4];
-  float gc[C];
-};
-struct PassSmem {
-  PassBuf buf[2];
-};
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ void pass_prefetch(PassBuf& pb, const __half* __restrict__ Wg,
-                                              const __half* __restrict__ qq,
-                                              const __half* __restrict__ Kt,
-                                              const __half* __restrict__ Aqk,
-                                              const float* __restrict__ Ug,
-                                              const float* __restrict__ gcum, int64_t t0,
-                                              int64_t cgi, int nvalid, int h, int dv0, int tid) {
-  for (int i = tid; i < C * (D / 8); i += 32 * SW) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    const bool ok = r < nvalid;
-    const int64_t rr = ok ? (t0 + r) : t0;
-    cp_async16(smem_u32(&pb.W[r][c8]), Wg + (rr * HV + h) * D + c8, ok);
-    cp_async16(smem_u32(&pb.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
-    cp_async16(smem_u32(&pb.K[r][c8]), Kt + (rr * HV + h) * D + c8, ok);
-  }
-  for (int i = tid; i < C * (C / 8); i += 32 * SW) {
-    const int r = i / (C / 8), c8 = (i % (C / 8)) * 8;
-    cp_async16(smem_u32(&pb.Aq[r][c8]), Aqk + ((cgi * HV + h) * C + r) * C + c8, true);
-  }
-  for (int i = tid; i < SW * C * 4; i += 32 * SW) {
-    const int w = i / (C * 4), r = (i / 4) % C, c4 = (i % 4) * 4;
-    const bool ok = r < nvalid;
-    const int64_t rr = ok ? (t0 + r) : t0;
-    cp_async16(smem_u32(&pb.U[w][r][c4]), Ug + (rr * HV + h) * D + dv0 + 16 * w + c4, ok);
-  }
-  if (tid < C) {
-    // rows past the end repeat the last valid g
-    const int64_t rr = t0 + min(tid, nvalid - 1);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&pb.gc[tid])),
-                 "l"(gcum + rr * HV + h)
-                 : "memory");
-  }
-  cp_async_commit();
-}
-
-__global__ void __launch_bounds__(32 * SW) gdn_state_pass_kernel(
-    const __half* __restrict__ qq, const __half* __restrict__ Kt, const __half* __restrict__ Wg,
-    const float* __restrict__ Ug, const __half* __restrict__ Aqk, const float* __restrict__ gcum,
-    const float* __restrict__ s0, __half* __restrict__ out, int64_t ldo,
-    float* __restrict__ s_out, int L, int nch) {
-  extern __shared__ __align__(16) uint8_t smraw[];
-  PassSmem& s = *reinterpret_cast<PassSmem*>(smraw);
-  constexpr int NSL = D / (16 * SW);     // CTAs per head
-  const int sl = blockIdx.x % NSL;
-  const int h = (blockIdx.x / NSL) % HV;
-  const int b = blockIdx.x / (NSL * HV);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int dv0 = sl * 16 * SW;          // first value row of the CTA
-  const int dvw = dv0 + 16 * warp;       // first value row of this warp
-
-  // state slice [16 value rows x 128 key cols]: n-tile nt covers key columns 8nt..8nt+7
-  float S[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float v0 = 0.f;
-      if (s0) {
-        const int r = dvw + gq + (e >= 2 ? 8 : 0);
-        const int col = nt * 8 + 2 * tq + (e & 1);
-        v0 = s0[(((int64_t)b * HV + h) * D + r) * D + col];
-      }
-      S[nt][e] = v0;
-    }
-  }
-  const int64_t tb = (int64_t)b * L;
-  pass_prefetch(s.buf[0], Wg, qq, Kt, Aqk, Ug, gcum, tb, (int64_t)b * nch, min(C, L), h, dv0, tid);
-  const float inv_sqrt_d = 0.08838834764831845f;
-
-  for (int c = 0; c < nch; ++c) {
-    const int64_t t0 = tb + (int64_t)c * C;
-    const int nvalid = min(C, L - c * C);
-    PassBuf& pb = s.buf[c & 1];
-    cp_async_wait<0>();
-    __syncthreads();  // chunk c landed for both warps; both are done with chunk c-1's buffer
-    if (c + 1 < nch)
-      pass_prefetch(s.buf[(c + 1) & 1], Wg, qq, Kt, Aqk, Ug, gcum, t0 + C, (int64_t)b * nch + c + 1,
-                    min(C, L - (c + 1) * C), h, dv0, tid);
-    // SB[ks][nv]: B fragments of S0^T for key step ks (16 columns) and value n-tile nv
-    uint32_t SB[8][2][2];
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      SB[ks][0][0] = h2u(S[2 * ks][0], S[2 * ks][1]);
-      SB[ks][0][1] = h2u(S[2 * ks + 1][0], S[2 * ks + 1][1]);
-      SB[ks][1][0] = h2u(S[2 * ks][2], S[2 * ks][3]);
-      SB[ks][1][1] = h2u(S[2 * ks + 1][2], S[2 * ks + 1][3]);
-    }
-    const uint32_t sW = smem_u32(&pb.W[0][0]), sQ = smem_u32(&pb.Q[0][0]);
-    const uint32_t sK = smem_u32(&pb.K[0][0]), sA = smem_u32(&pb.Aq[0][0]);
-    // U = U' - W S0^T, transposed into UT[mt][nv][2] (fp16): rows tok 16mt.., value rows 8nv..
-    uint32_t UT[4][2][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      float acc[2][4];
-#pragma unroll
-      for (int nv = 0; nv < 2; ++nv) acc[nv][0] = acc[nv][1] = acc[nv][2] = acc[nv][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, a_addr(sW, LDH, mt * 16, ks * 16, lane));
-        mma16816(acc[0], a, SB[ks][0][0], SB[ks][0][1]);
-        mma16816(acc[1], a, SB[ks][1][0], SB[ks][1][1]);
-      }
-#pragma unroll
-      for (int nv = 0; nv < 2; ++nv) {
-        const int r0 = mt * 16 + gq, r1 = r0 + 8;
-        const int col = nv * 8 + 2 * tq;
-        const float u00 = r0 < nvalid ? pb.U[warp][r0][col] - acc[nv][0] : 0.f;
-        const float u01 = r0 < nvalid ? pb.U[warp][r0][col + 1] - acc[nv][1] : 0.f;
-        const float u10 = r1 < nvalid ? pb.U[warp][r1][col] - acc[nv][2] : 0.f;
-        const float u11 = r1 < nvalid ? pb.U[warp][r1][col + 1] - acc[nv][3] : 0.f;
-        UT[mt][nv][0] = movmatrix_t(h2u(u00, u01));
-        UT[mt][nv][1] = movmatrix_t(h2u(u10, u11));
-      }
-    }
-    // O = e^g / sqrt(128) * (Q S0^T) + Aqk U
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      float acc[2][4];
-#pragma unroll
-      for (int nv = 0; nv < 2; ++nv) acc[nv][0] = acc[nv][1] = acc[nv][2] = acc[nv][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, a_addr(sQ, LDH, mt * 16, ks * 16, lane));
-        mma16816(acc[0], a, SB[ks][0][0], SB[ks][0][1]);
-        mma16816(acc[1], a, SB[ks][1][0], SB[ks][1][1]);
-      }
-      const int r0 = mt * 16 + gq, r1 = r0 + 8;
-      const float f0 = __expf(pb.gc[r0]) * inv_sqrt_d, f1 = __expf(pb.gc[r1]) * inv_sqrt_d;
-#pragma unroll
-      for (int nv = 0; nv < 2; ++nv) {
-        acc[nv][0] *= f0; acc[nv][1] *= f0; acc[nv][2] *= f1; acc[nv][3] *= f1;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, a_addr(sA, C + 8, mt * 16, ks * 16, lane));
-        mma16816(acc[0], a, UT[ks][0][0], UT[ks][0][1]);
-        mma16816(acc[1], a, UT[ks][1][0], UT[ks][1][1]);
-      }
-#pragma unroll
-      for (int nv = 0; nv < 2; ++nv) {
-        const int col = dvw + nv * 8 + 2 * tq;
-        if (r0 < nvalid)
-          *reinterpret_cast<uint32_t*>(out + (t0 + r0) * ldo + h * D + col) = h2u(acc[nv][0], acc[nv][1]);
-        if (r1 < nvalid)
-          *reinterpret_cast<uint32_t*>(out + (t0 + r1) * ldo + h * D + col) = h2u(acc[nv][2], acc[nv][3]);
-      }
-    }
-    // S <- e^{g_C} S + U^T Kd
-    const float eC = __expf(pb.gc[C - 1]);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      S[nt][0] *= eC; S[nt][1] *= eC; S[nt][2] *= eC; S[nt][3] *= eC;
-    }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint32_t a[4] = {UT[ks][0][0], UT[ks][1][0], UT[ks][0][1], UT[ks][1][1]};
-#pragma unroll
-      for (int nt = 0; nt < 16; nt += 2) {
-        uint32_t bq[4];
-        ldsm_x4_t(bq, bk_addr(sK, LDH, nt * 8, ks * 16, lane));
-        mma16816(S[nt], a, bq[0], bq[1]);
-        mma16816(S[nt + 1], a, bq[2], bq[3]);
-      }
-    }
-  }
-  if (s_out) {
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = dvw + gq + (e >= 2 ? 8 : 0);
-        const int col = nt * 8 + 2 * tq + (e & 1);
-        s_out[(((int64_t)b * HV + h) * D + r) * D + col] = S[nt][e];
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------------------------------
 // Output gate of the decoder layer: y[t, h*128 + i] = RMSNorm_128(o[t, h, :])_i * w_i * SiLU(z).
 // One CTA (256 threads) per token; 8 threads x 16 values per head.
 // ------------------------------------------------------------------------------------------
@@ -581,7 +366,7 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   const int64_t nch = (L + gdn::C - 1) / gdn::C;
   size_t n = 0;
   n += al256g(M * gdn::HV * 4);                          // g (from alpha)
-  n += al256g(M * gdn::HV * 4);                          // gcum
+  n += al256g(B * nch * gdn::HV * gdn::C * 4);           // exp(g) per chunk row
   n += al256g(M * gdn::HV * gdn::D * 2);                 // W
   n += al256g(M * gdn::HV * gdn::D * 4);                 // U'
   n += al256g(M * gdn::HV * gdn::D * 2);                 // decayed keys
@@ -592,7 +377,7 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
 
 struct GdnWs {
   float* g;
-  float* gcum;
+  float* ef;
   __half* W;
   float* U1;
   __half* Kt;
@@ -605,7 +390,7 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   uint8_t* p = static_cast<uint8_t*>(ws);
   GdnWs w;
   w.g = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * 4);
-  w.gcum = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * 4);
+  w.ef = reinterpret_cast<float*>(p); p += al256g(B * nch * gdn::HV * gdn::C * 4);
   w.W = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
   w.U1 = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * gdn::D * 4);
   w.Kt = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
@@ -619,8 +404,6 @@ static clef_status gdn_set_attrs() {
   if (g_gdn_attr) return CLEF_OK;
   CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_chunk_wy_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::WySmem)));
-  CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_state_pass_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::PassSmem)));
   g_gdn_attr = true;
   return CLEF_OK;
 }
@@ -658,23 +441,13 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 8.0 * C * C * D,
                   (double)M * HVd * D * (2 + 2 + 2 + 2 + 4) + nchunks * HVd * C * C * 2);
     gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(
-        q, k, v, g, beta, w.gcum, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch);
+        q, k, v, g, beta, w.ef, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch);
     CLEF_LAUNCH_CHECK();
   }
   __half* o = z ? w.o : out;
   const int64_t ldo_pass = z ? (int64_t)gdn::HV * gdn::D : ldo;
-  {
-    TraceScope ts(stream, "gdn_state_pass",
-                  nchunks * HVd * (6.0 * C * D * D + 2.0 * C * C * D),
-                  (double)M * HVd * D * (2 + 2 + 4 + 2) + (double)M * 16 * D * 2 +
-                      nchunks * HVd * C * C * 2);
-    constexpr int nsl = gdn::D / (16 * gdn::SW);
-    gdn::gdn_state_pass_kernel<<<(unsigned)(B * gdn::HV * nsl), 32 * gdn::SW,
-                                 sizeof(gdn::PassSmem), stream>>>(q, w.Kt, w.W, w.U1, w.Aqk, w.gcum,
-                                                                  s0, o, ldo_pass, s_out, (int)L,
-                                                                  nch);
-    CLEF_LAUNCH_CHECK();
-  }
+  st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, s0, s_out, o, ldo_pass, B, L, stream);
+  if (st != CLEF_OK) return st;
   if (z) {
     TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);
     gdn::gdn_gated_norm_kernel<<<(unsigned)M, 256, 0, stream>>>(o, z, ldz, o_norm, out, ldo);

@@ -4,6 +4,13 @@
 
 namespace clef {
 
+namespace gdn {
+constexpr int C = 64;          // chunk width
+constexpr int D = 128;         // head size (key and value)
+constexpr int HV = 32;         // value heads
+constexpr int HK = 16;         // key heads
+}  // namespace gdn
+
 // conv(4) + SiLU + q/k L2 norm, for M tokens of requests of L positions.
 clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
                             __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream);
@@ -17,5 +24,13 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
                             const float* alpha, const float* beta, const float* s0, float* s_out,
                             const __half* z, int64_t ldz, const __half* o_norm, __half* out,
                             int64_t ldo, int64_t B, int64_t L, void* ws, cudaStream_t stream);
+
+// The sequential state pass on tcgen05 (gdn_state.cu).  Inputs are the chunk phase's outputs:
+// W, decayed keys Kd [B, L, 32, 128] fp16, U' [B, L, 32, 128] fp32, Aqk [B * nch, 32, 64, 64]
+// fp16, ef [B * nch, 32, 64] fp32 (exp of the in-chunk cumulative log alpha), and q
+// [B, L, 16, 128] fp16.  out [B * L, ldo] fp16 (head h at columns 128 h ..).
+clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W, const float* U1,
+                             const __half* Aqk, const float* ef, const float* s0, float* s_out,
+                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream);
 
 }  // namespace clef

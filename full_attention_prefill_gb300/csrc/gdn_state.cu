@@ -1,0 +1,461 @@
+// Gated DeltaNet: the sequential state pass on tcgen05, one CTA per (request, value head).
+//
+// The chunked form of the gated delta rule ("Clef-Flash-ANE-LUT6" model card, "Model
+// architecture"; "clef-flash-LiteRT" README, "Provenance": chunks of 64 positions), for the chunk
+// of rows t0 .. t0+63 entering with state S (value rows x key columns, fp32):
+//     U   = U' - W S^T                          (per token: the new value minus the predicted one)
+//     O   = diag(exp(g)) Q S^T / sqrt(128) + Aqk U
+//     S  <- exp(g_C) S + U^T Kd                 (Kd = exp(g_C - g) K, the decayed keys)
+// W, U', Kd, Aqk and exp(g) come from the parallel chunk phase.  Only U and S depend on the
+// previous chunk, so the pass is a chain of two products per chunk; the O products hang off it.
+//
+// Everything transposed so that the 128 value rows are the MMA's M dimension (TMEM lanes):
+//     U^T [v, tok]  = S0h . W^T        M=128, N=64,  K=128   A = S0h (TMEM), B = W  (smem, K-major)
+//     S   [v, k]   += U^T . Kd         M=128, N=128, K=64    A = U^T (TMEM), B = Kd (smem, MN-major)
+//     O1^T[v, tok]  = S0h . Q^T        M=128, N=64,  K=128   A = S0h (TMEM), B = Q  (smem, K-major)
+//     O2^T[v, tok]  = U^T . Aqk^T      M=128, N=64,  K=64    A = U^T (TMEM), B = Aqk (smem, K-major)
+// with S0h the fp16 copy of S.  The fp32 state never leaves tensor memory.
+//
+// Warp roles (512 threads):
+//   warp 0      TMA: per chunk part A = W (two 64-column boxes, 128-byte swizzle) and U' (fp32
+//               [64 tok][128 v]); part B = Q, Kd (two boxes each) and Aqk; two stages of each.
+//               Part A is freed once U is formed, part B once the chunk's MMAs are done, so the
+//               next loads start early enough to hide their latency
+//   warp 1      MMA issue (one thread) and tensor-memory allocation
+//   warps 4-11  row threads, two per value row v = TMEM lane (warps 4-7 key columns / tokens
+//               0..63 / 0..31, warps 8-11 the rest): per chunk copy S to S0h (fp16) and scale S
+//               by exp(g_C) in place; then U = U' - acc, fp16, into TMEM
+//   warps 12-15 output: O = exp(g)/sqrt(128) O1 + O2 -> fp16, staged in shared memory and
+//               written by a TMA store (rows past the request's end are clipped)
+// MMA order per chunk: U(c), O1(c) (runs while U is converted), S update(c), O2(c) (runs while
+// the next chunk's S is converted).
+// Tensor memory (512 columns): S fp32 [0,128), S0h fp16 [128,192), U acc fp32 [192,256),
+// U fp16 [256,288), O1 [288,352), O2 [352,416).
+#include "common.cuh"
+#include "gdn.cuh"
+
+namespace clef {
+namespace gdn {
+
+constexpr int ST_THREADS = 512;
+constexpr int BLK = C * 128;                   // one [64 rows][64 fp16] swizzled block: 8 KB
+// part A (per stage): W, U'
+constexpr int A_W = 0;                         // 2 blocks: key columns 0..63, 64..127
+constexpr int A_U = 2 * BLK;                   // fp32 [64 tok][128 v]
+constexpr int A_BYTES = A_U + C * D * 4;       // 48 KB
+// part B (per stage): Q, Kd, Aqk
+constexpr int B_Q = 0;                         // 2 blocks
+constexpr int B_KD = 2 * BLK;                  // 2 blocks
+constexpr int B_AQ = 4 * BLK;                  // 1 block [64 r][64 s]
+constexpr int B_BYTES = 5 * BLK;               // 40 KB
+constexpr int NSTAGE = 2;
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + NSTAGE * A_BYTES;
+constexpr int OFF_EPI = OFF_B + NSTAGE * B_BYTES;   // 4 x [64 tok][32 v] fp16
+constexpr int EPI_BYTES = C * 32 * 2;
+constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BYTES;
+constexpr int NUM_BARS = 4 * NSTAGE + 7;
+constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int ST_SMEM = OFF_SLOT + 16 + 1024;  // slack to align the base to 1024
+static_assert(ST_SMEM <= 232448, "shared memory per CTA");
+static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled blocks stay 1024-aligned");
+
+constexpr uint32_t COL_S = 0;
+constexpr uint32_t COL_S0H = 128;
+constexpr uint32_t COL_UACC = 192;
+constexpr uint32_t COL_UH = 256;
+constexpr uint32_t COL_O1 = 288;
+constexpr uint32_t COL_O2 = 352;
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
+    const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tQ,
+    const __grid_constant__ CUtensorMap tKd, const __grid_constant__ CUtensorMap tU,
+    const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tO,
+    const float* __restrict__ ef, const float* __restrict__ s0, float* __restrict__ s_out, int L,
+    int nch, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x % HV;
+  const int b = blockIdx.x / HV;
+  const float* efh = ef + ((int64_t)b * nch * HV + h) * C;   // chunk c at efh + c * HV * C
+
+  const uint32_t bar_fa = sb + OFF_BAR;            // [2] part A landed
+  const uint32_t bar_ea = bar_fa + 16;             // [2] part A consumed
+  const uint32_t bar_fb = bar_ea + 16;             // [2] part B landed
+  const uint32_t bar_eb = bar_fb + 16;             // [2] part B consumed
+  const uint32_t bar_s0 = bar_eb + 16;             // S0h written and S scaled (row threads)
+  const uint32_t bar_uh = bar_s0 + 8;              // U (fp16) written (row threads)
+  const uint32_t bar_u = bar_uh + 8;               // U acc complete
+  const uint32_t bar_s = bar_u + 8;                // S update complete
+  const uint32_t bar_o = bar_s + 8;                // O1, O2 complete
+  const uint32_t bar_oe = bar_o + 8;               // O1, O2 drained
+  const uint32_t bar_fin = bar_oe + 8;             // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(bar_fa + 8 * i, 1);
+      mbar_init(bar_ea + 8 * i, 1 + 8);            // U(c) commit + the 8 row warps
+      mbar_init(bar_fb + 8 * i, 1);
+      mbar_init(bar_eb + 8 * i, 1);                // O2(c) commit
+    }
+    mbar_init(bar_s0, 8);
+    mbar_init(bar_uh, 8);
+    mbar_init(bar_u, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_oe, 4);
+    mbar_init(bar_fin, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tW);
+    tma_prefetch_desc(&tQ);
+    tma_prefetch_desc(&tKd);
+    tma_prefetch_desc(&tU);
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued_a = 0, issued_b = 0;
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        const int t0 = c * C;
+        if (c >= NSTAGE &&
+            !mbar_wait(bar_ea + 8 * st, ((c - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
+          break;
+        {
+          const uint32_t base = sb + OFF_A + st * A_BYTES;
+          const uint32_t fb = bar_fa + 8 * st;
+          mbar_arrive_expect_tx(fb, A_BYTES);
+          tma_load_4d(base + A_W, &tW, fb, 0, h, t0, b);
+          tma_load_4d(base + A_W + BLK, &tW, fb, 64, h, t0, b);
+          tma_load_4d(base + A_U, &tU, fb, 0, h, t0, b);
+          issued_a = c + 1;
+        }
+        if (c >= NSTAGE &&
+            !mbar_wait(bar_eb + 8 * st, ((c - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
+          break;
+        {
+          const uint32_t base = sb + OFF_B + st * B_BYTES;
+          const uint32_t fb = bar_fb + 8 * st;
+          const int64_t cgi = (int64_t)b * nch + c;
+          mbar_arrive_expect_tx(fb, B_BYTES);
+          tma_load_4d(base + B_Q, &tQ, fb, 0, h >> 1, t0, b);
+          tma_load_4d(base + B_Q + BLK, &tQ, fb, 64, h >> 1, t0, b);
+          tma_load_4d(base + B_KD, &tKd, fb, 0, h, t0, b);
+          tma_load_4d(base + B_KD + BLK, &tKd, fb, 64, h, t0, b);
+          tma_load_2d(base + B_AQ, &tA, fb, 0, (int)((cgi * HV + h) * C));
+          issued_b = c + 1;
+        }
+      }
+      // copies still in flight land before the CTA may exit (no later phase of these barriers
+      // can complete, so the parity tests are unambiguous)
+      for (int c = issued_a > NSTAGE ? issued_a - NSTAGE : 0; c < issued_a; ++c)
+        mbar_wait(bar_fa + 8 * (c & 1), (c >> 1) & 1, status, DEV_TIMEOUT_TMA);
+      for (int c = issued_b > NSTAGE ? issued_b - NSTAGE : 0; c < issued_b; ++c)
+        mbar_wait(bar_fb + 8 * (c & 1), (c >> 1) & 1, status, DEV_TIMEOUT_TMA);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t id_n64 = idesc_f16_f32(128, 64);
+      constexpr uint32_t id_s = idesc_f16_f32(128, 128, 0, 1);   // B (Kd) MN-major
+      bool any = false;
+      for (int c = 0; c < nch; ++c) {
+        const int st = c & 1;
+        const uint32_t ph = (uint32_t)c & 1;
+        const uint32_t pa = sb + OFF_A + st * A_BYTES;
+        const uint32_t pb = sb + OFF_B + st * B_BYTES;
+        if (!mbar_wait(bar_fa + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
+            !mbar_wait(bar_s0, ph, status, DEV_TIMEOUT_MMA))
+          break;
+        tc_fence_after();
+        // U^T = S0h . W^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_f16_ts(tmem + COL_UACC, tmem + COL_S0H + kk * 8,
+                        sdesc_k_sw128(pa + A_W + (kk >> 2) * BLK + (kk & 3) * 32), id_n64, kk != 0);
+        tc_commit(bar_u);
+        tc_commit(bar_ea + 8 * st);   // W no longer read (the row threads add theirs for U')
+        any = true;
+        // O1^T = S0h . Q^T, once the previous chunk's O is drained and part B has landed
+        if ((c >= 1 && !mbar_wait(bar_oe, (c - 1) & 1, status, DEV_TIMEOUT_MMA)) ||
+            !mbar_wait(bar_fb + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_f16_ts(tmem + COL_O1, tmem + COL_S0H + kk * 8,
+                        sdesc_k_sw128(pb + B_Q + (kk >> 2) * BLK + (kk & 3) * 32), id_n64, kk != 0);
+        // S += U^T . Kd  (S was scaled by exp(g_C) in place by the row threads)
+        if (!mbar_wait(bar_uh, ph, status, DEV_TIMEOUT_MMA)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          tc_mma_f16_ts(tmem + COL_S, tmem + COL_UH + kk * 8,
+                        sdesc_mn_sw128(pb + B_KD + kk * 16 * 128, BLK, 1024), id_s, 1);
+        tc_commit(bar_s);
+        // O2^T = U^T . Aqk^T
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          tc_mma_f16_ts(tmem + COL_O2, tmem + COL_UH + kk * 8,
+                        sdesc_k_sw128(pb + B_AQ + kk * 32), id_n64, kk != 0);
+        tc_commit(bar_o);
+        tc_commit(bar_eb + 8 * st);
+      }
+      // tensor memory is freed only after every MMA issued here has completed
+      if (any) {
+        tc_commit(bar_fin);
+        mbar_wait(bar_fin, 0, status, DEV_TIMEOUT_MMA);
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------------ row threads
+    const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;                        // which half of the columns
+    const int v = quarter * 32 + lane;                       // value row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    // entering state: s0 row v (this thread's 64 key columns), or zero
+#pragma unroll 1
+    for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+      uint32_t r[32];
+      if (s0) {
+        const float4* src =
+            reinterpret_cast<const float4*>(s0 + (((int64_t)b * HV + h) * D + v) * D + cb * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = __ldg(src + i);
+          r[4 * i] = __float_as_uint(x.x);
+          r[4 * i + 1] = __float_as_uint(x.y);
+          r[4 * i + 2] = __float_as_uint(x.z);
+          r[4 * i + 3] = __float_as_uint(x.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      tmem_st_32x32b_x32(tl + COL_S + cb * 32, r);
+    }
+    tc_wait_st();
+    float eC_next = __ldg(efh + (C - 1));
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const int st = c & 1;
+      // exp(g_C) of this chunk; the next chunk's is fetched now, its latency hidden by the chunk
+      const float eC = eC_next;
+      if (c + 1 < nch) eC_next = __ldg(efh + (int64_t)(c + 1) * HV * C + (C - 1));
+      ok = ok && mbar_wait(bar_fa + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
+      ok = ok && (c == 0 || mbar_wait(bar_s, (c - 1) & 1, status, DEV_TIMEOUT_EPILOGUE));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // S0h = fp16(S); S <- exp(g_C) S   (this thread: key columns 64 half .. 64 half + 63)
+      {
+        uint32_t r0[32], r1[32], hh[32];
+        tmem_ld_32x32b_x32(tl + COL_S + half * 64, r0);
+        tmem_ld_32x32b_x32(tl + COL_S + half * 64 + 32, r1);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          hh[i] = pack_half2(u2f(r0[2 * i]), u2f(r0[2 * i + 1]));
+          hh[16 + i] = pack_half2(u2f(r1[2 * i]), u2f(r1[2 * i + 1]));
+        }
+        tmem_st_32x32b_x32(tl + COL_S0H + half * 32, hh);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          r0[i] = __float_as_uint(u2f(r0[i]) * eC);
+          r1[i] = __float_as_uint(u2f(r1[i]) * eC);
+        }
+        tmem_st_32x32b_x32(tl + COL_S + half * 64, r0);
+        tmem_st_32x32b_x32(tl + COL_S + half * 64 + 32, r1);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s0);
+      // U' of this row for tokens 32 half .. 32 half + 31, read while the U MMAs run
+      const float* us = reinterpret_cast<const float*>(smem + OFF_A + st * A_BYTES + A_U) +
+                        (half * 32) * D + v;
+      float up[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) up[j] = us[j * D];
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      if (!ok) break;
+      tc_fence_after();
+      // U = U' - W S0^T (rows past the request's end have W = U' = 0 from the zero-filled
+      // loads, hence U = 0)
+      {
+        uint32_t a[32], uh[16];
+        tmem_ld_32x32b_x32(tl + COL_UACC + half * 32, a);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          uh[i] = pack_half2(up[2 * i] - u2f(a[2 * i]), up[2 * i + 1] - u2f(a[2 * i + 1]));
+        tmem_st_32x32b_x16(tl + COL_UH + half * 16, uh);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_uh);
+        mbar_arrive(bar_ea + 8 * st);   // done with this stage's U'
+      }
+    }
+    if (ok && s_out) {
+      // the state after the last chunk
+      if (mbar_wait(bar_s, (nch - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+        tc_fence_after();
+        float* dst = s_out + (((int64_t)b * HV + h) * D + v) * D;
+#pragma unroll 1
+        for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tl + COL_S + cb * 32, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dst + cb * 32)[i] =
+                make_float4(u2f(r[4 * i]), u2f(r[4 * i + 1]), u2f(r[4 * i + 2]), u2f(r[4 * i + 3]));
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------------ output
+    const int quarter = warp & 3;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const float inv_sqrt_d = 0.08838834764831845f;
+    // staging [64 tok][32 v] fp16 for this warp's 32 value rows
+    const uint32_t stg = sb + OFF_EPI + quarter * EPI_BYTES;
+    // exp(g) of the chunk's rows: lane j holds rows j and 32 + j (fetched one chunk ahead)
+    float fa_next = __ldg(efh + lane), fb_next = __ldg(efh + 32 + lane);
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const float fa = fa_next * inv_sqrt_d, fb = fb_next * inv_sqrt_d;
+      if (c + 1 < nch) {
+        fa_next = __ldg(efh + (int64_t)(c + 1) * HV * C + lane);
+        fb_next = __ldg(efh + (int64_t)(c + 1) * HV * C + 32 + lane);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      if (!ok) break;
+      tc_fence_after();
+      // O = exp(g)/sqrt(128) O1 + O2 in two halves of 32 tokens, kept as fp16 pairs
+      uint32_t y[32];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o1[32], o2[32];
+        tmem_ld_32x32b_x32(tl + COL_O1 + hf * 32, o1);
+        tmem_ld_32x32b_x32(tl + COL_O2 + hf * 32, o2);
+        tc_wait_ld();
+        const float fh = hf ? fb : fa;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float f0 = __shfl_sync(0xffffffffu, fh, 2 * j);
+          const float f1 = __shfl_sync(0xffffffffu, fh, 2 * j + 1);
+          y[hf * 16 + j] = pack_half2(f0 * u2f(o1[2 * j]) + u2f(o2[2 * j]),
+                                      f1 * u2f(o1[2 * j + 1]) + u2f(o2[2 * j + 1]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_oe);
+        bulk_wait_read0();   // the previous chunk's store has finished reading the staging
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + ((2 * j) * 32 + lane) * 2),
+                     "h"((unsigned short)(y[j] & 0xffffu)) : "memory");
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + ((2 * j + 1) * 32 + lane) * 2),
+                     "h"((unsigned short)(y[j] >> 16)) : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_4d(&tO, stg, quarter * 32, h, c * C, b);
+        bulk_commit_group();
+      }
+    }
+    if (lane == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace gdn
+
+clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W, const float* U1,
+                             const __half* Aqk, const float* ef, const float* s0, float* s_out,
+                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream) {
+  using namespace gdn;
+  if (B == 0 || L == 0) return CLEF_OK;
+  if ((ldo % 8) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) {
+    set_error("GDN scan output: row stride must be a multiple of 8 and the base 16-byte aligned");
+    return CLEF_E_ALIGN;
+  }
+  const int64_t nch = (L + C - 1) / C;
+  static bool attr = false;
+  if (!attr) {
+    CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn_state_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM));
+    attr = true;
+  }
+  CUtensorMap tW, tQ, tKd, tU, tA, tO;
+  {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)HV, (uint64_t)L, (uint64_t)B};
+    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)HV * D * 2, (uint64_t)L * HV * D * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)C, 1};
+    if (tma_encode(&tW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, W, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+        tma_encode(&tKd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Kd, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+      return CLEF_E_CUDA;
+    const uint64_t dq[4] = {(uint64_t)D, (uint64_t)HK, (uint64_t)L, (uint64_t)B};
+    const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)HK * D * 2, (uint64_t)L * HK * D * 2};
+    if (tma_encode(&tQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, q, dq, sq, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+      return CLEF_E_CUDA;
+    const uint64_t su[3] = {(uint64_t)D * 4, (uint64_t)HV * D * 4, (uint64_t)L * HV * D * 4};
+    const uint32_t bu[4] = {(uint32_t)D, 1, (uint32_t)C, 1};
+    if (tma_encode(&tU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, U1, dims, su, bu,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+      return CLEF_E_CUDA;
+    if (tma_encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aqk, (uint64_t)C,
+                      (uint64_t)(B * nch * HV * C), (uint64_t)C * 2, (uint32_t)C, (uint32_t)C,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+      return CLEF_E_CUDA;
+    const uint64_t so[3] = {(uint64_t)D * 2, (uint64_t)ldo * 2, (uint64_t)L * ldo * 2};
+    const uint32_t bo[4] = {32, 1, (uint32_t)C, 1};
+    if (tma_encode(&tO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, out, dims, so, bo,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
+      return CLEF_E_CUDA;
+  }
+  const double Cd = C, Dd = D, chunks = (double)B * nch * HV;
+  TraceScope ts(stream, "gdn_state_pass", chunks * (6.0 * Cd * Dd * Dd + 2.0 * Cd * Cd * Dd),
+                (double)B * L * HV * D * (2 + 2 + 4 + 2) + (double)B * L * HK * D * 2 +
+                    chunks * Cd * Cd * 2);
+  gdn_state_tc_kernel<<<(unsigned)(B * HV), ST_THREADS, ST_SMEM, stream>>>(
+      tW, tQ, tKd, tU, tA, tO, ef, s0, s_out, (int)L, (int)nch, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+}  // namespace clef
