@@ -14,7 +14,7 @@
 // Kernels:
 //   gdn_chunk_wy    (parallel over chunks x heads): cumulative g, T by forward substitution,
 //                   W, U', the decayed keys exp(g_C - g) k and the intra-chunk matrix
-//                   Aqk = tril(Q K^T) o exp(g_r - g_s) / sqrt(128)
+//                   Aqk = tril(Q K^T) o exp(g_r - g_s) / sqrt(128) (stored transposed)
 //   gdn_state_tc    (gdn_state.cu; sequential over chunks, one CTA per value head): the state
 //                   stays in tensor memory; per chunk U = U' - W S0^T, S <- exp(g_C) S + U^T Kd,
 //                   O = exp(g) Q S0^T / sqrt(128) + Aqk U, all on tcgen05
@@ -225,7 +225,10 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
           const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
           const float v0 = (col <= r) ? d0 * acc[n][2 * hf] * scale : 0.f;
           const float v1 = (col + 1 <= r) ? d1 * acc[n][2 * hf + 1] * scale : 0.f;
-          *reinterpret_cast<uint32_t*>(Aqk + (((int64_t)cg * HV + h) * C + r) * C + col) = h2u(v0, v1);
+          // stored transposed, [s][r], the layout the state pass reads it in
+          __half* at = Aqk + ((int64_t)cg * HV + h) * C * C;
+          at[col * C + r] = __float2half_rn(v0);
+          at[(col + 1) * C + r] = __float2half_rn(v1);
         }
       }
     }

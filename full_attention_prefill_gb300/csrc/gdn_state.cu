@@ -9,28 +9,27 @@
 // W, U', Kd, Aqk and exp(g) come from the parallel chunk phase.  Only U and S depend on the
 // previous chunk, so the pass is a chain of two products per chunk; the O products hang off it.
 //
-// Everything transposed so that the 128 value rows are the MMA's M dimension (TMEM lanes):
-//     U^T [v, tok]  = S0h . W^T        M=128, N=64,  K=128   A = S0h (TMEM), B = W  (smem, K-major)
-//     S   [v, k]   += U^T . Kd         M=128, N=128, K=64    A = U^T (TMEM), B = Kd (smem, MN-major)
-//     O1^T[v, tok]  = S0h . Q^T        M=128, N=64,  K=128   A = S0h (TMEM), B = Q  (smem, K-major)
-//     O2^T[v, tok]  = U^T . Aqk^T      M=128, N=64,  K=64    A = U^T (TMEM), B = Aqk (smem, K-major)
-// with S0h the fp16 copy of S.  The fp32 state never leaves tensor memory.
+// Everything transposed so that the 128 value rows are the MMA's M dimension (TMEM lanes), and
+// the products that share an A operand merged into one MMA chain:
+//     [U^T | O1^T] [v, 128]  = S0h . [W ; Q]^T      M=128, N=128, K=128   A = S0h (TMEM)
+//     [S | O2^T]   [v, 192] += U^T . [Kd | Aqk^T]   M=128, N=192, K=64    A = U^T (TMEM)
+// with S0h the fp16 copy of S, U^T the fp16 U, O = exp(g)/sqrt(128) O1 + O2.  [W ; Q] is a
+// K-major shared operand (W's 64 token rows, then Q's), [Kd | Aqk^T] an MN-major one (per token
+// s: 128 key columns of Kd, then the 64 entries Aqk[., s]).  The second chain accumulates into S
+// (scaled by exp(g_C) in place beforehand) and into O2 (zeroed after each drain).  The fp32
+// state never leaves tensor memory.
 //
 // Warp roles (512 threads):
-//   warp 0      TMA: per chunk part A = W (two 64-column boxes, 128-byte swizzle) and U' (fp32
-//               [64 tok][128 v]); part B = Q, Kd (two boxes each) and Aqk; two stages of each.
-//               Part A is freed once U is formed, part B once the chunk's MMAs are done, so the
-//               next loads start early enough to hide their latency
+//   warp 0      TMA: per chunk part A = W, Q (two 64-column boxes each, 128-byte swizzle) and U'
+//               (fp32 [64 tok][128 v]); part B = Kd (two boxes) and Aqk^T; two stages of each.
 //   warp 1      MMA issue (one thread) and tensor-memory allocation
 //   warps 4-11  row threads, two per value row v = TMEM lane (warps 4-7 key columns / tokens
 //               0..63 / 0..31, warps 8-11 the rest): per chunk copy S to S0h (fp16) and scale S
 //               by exp(g_C) in place; then U = U' - acc, fp16, into TMEM
-//   warps 12-15 output: O = exp(g)/sqrt(128) O1 + O2 -> fp16, staged in shared memory and
-//               written by a TMA store (rows past the request's end are clipped)
-// MMA order per chunk: U(c), O1(c) (runs while U is converted), S update(c), O2(c) (runs while
-// the next chunk's S is converted).
-// Tensor memory (512 columns): S fp32 [0,128), S0h fp16 [128,192), U acc fp32 [192,256),
-// U fp16 [256,288), O1 [288,352), O2 [352,416).
+//   warps 12-15 output: O -> fp16, staged in shared memory and written by a TMA store (rows past
+//               the request's end are clipped)
+// Tensor memory (512 columns): S [0,128) | O2 [128,192), U acc [192,256) | O1 [256,320),
+// S0h fp16 [320,384), U fp16 [384,416).
 #include "common.cuh"
 #include "gdn.cuh"
 
@@ -39,33 +38,30 @@ namespace gdn {
 
 constexpr int ST_THREADS = 512;
 constexpr int BLK = C * 128;                   // one [64 rows][64 fp16] swizzled block: 8 KB
-// part A (per stage): W, U'
-constexpr int A_W = 0;                         // 2 blocks: key columns 0..63, 64..127
-constexpr int A_U = 2 * BLK;                   // fp32 [64 tok][128 v]
-constexpr int A_BYTES = A_U + C * D * 4;       // 48 KB
-// part B (per stage): Q, Kd, Aqk
-constexpr int B_Q = 0;                         // 2 blocks
-constexpr int B_KD = 2 * BLK;                  // 2 blocks
-constexpr int B_AQ = 4 * BLK;                  // 1 block [64 r][64 s]
-constexpr int B_BYTES = 5 * BLK;               // 40 KB
+// part A (per stage): [W kb0 | Q kb0 | W kb1 | Q kb1], U'
+constexpr int A_WQ = 0;                        // key block kb at kb * 2 BLK (W rows, then Q rows)
+constexpr int A_U = 4 * BLK;                   // fp32 [64 tok][128 v]
+constexpr int A_BYTES = A_U + C * D * 4;       // 64 KB
+// part B (per stage): [Kd kb0 | Kd kb1 | Aqk^T]
+constexpr int B_BYTES = 3 * BLK;               // 24 KB
 constexpr int NSTAGE = 2;
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + NSTAGE * A_BYTES;
 constexpr int OFF_EPI = OFF_B + NSTAGE * B_BYTES;   // 4 x [64 tok][32 v] fp16
 constexpr int EPI_BYTES = C * 32 * 2;
 constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BYTES;
-constexpr int NUM_BARS = 4 * NSTAGE + 7;
+constexpr int NUM_BARS = 4 * NSTAGE + 6;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int ST_SMEM = OFF_SLOT + 16 + 1024;  // slack to align the base to 1024
 static_assert(ST_SMEM <= 232448, "shared memory per CTA");
 static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled blocks stay 1024-aligned");
 
 constexpr uint32_t COL_S = 0;
-constexpr uint32_t COL_S0H = 128;
+constexpr uint32_t COL_O2 = 128;
 constexpr uint32_t COL_UACC = 192;
-constexpr uint32_t COL_UH = 256;
-constexpr uint32_t COL_O1 = 288;
-constexpr uint32_t COL_O2 = 352;
+constexpr uint32_t COL_O1 = 256;
+constexpr uint32_t COL_S0H = 320;
+constexpr uint32_t COL_UH = 384;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
@@ -90,25 +86,23 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
   const uint32_t bar_eb = bar_fb + 16;             // [2] part B consumed
   const uint32_t bar_s0 = bar_eb + 16;             // S0h written and S scaled (row threads)
   const uint32_t bar_uh = bar_s0 + 8;              // U (fp16) written (row threads)
-  const uint32_t bar_u = bar_uh + 8;               // U acc complete
-  const uint32_t bar_s = bar_u + 8;                // S update complete
-  const uint32_t bar_o = bar_s + 8;                // O1, O2 complete
-  const uint32_t bar_oe = bar_o + 8;               // O1, O2 drained
+  const uint32_t bar_u = bar_uh + 8;               // [U acc | O1] complete
+  const uint32_t bar_s = bar_u + 8;                // [S | O2] complete
+  const uint32_t bar_oe = bar_s + 8;               // O1, O2 drained and O2 zeroed
   const uint32_t bar_fin = bar_oe + 8;             // every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(bar_fa + 8 * i, 1);
-      mbar_init(bar_ea + 8 * i, 1 + 8);            // U(c) commit + the 8 row warps
+      mbar_init(bar_ea + 8 * i, 1 + 8);            // first chain's commit + the 8 row warps
       mbar_init(bar_fb + 8 * i, 1);
-      mbar_init(bar_eb + 8 * i, 1);                // O2(c) commit
+      mbar_init(bar_eb + 8 * i, 1);                // second chain's commit
     }
     mbar_init(bar_s0, 8);
     mbar_init(bar_uh, 8);
     mbar_init(bar_u, 1);
     mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
     mbar_init(bar_oe, 4);
     mbar_init(bar_fin, 1);
     fence_mbar_init();
@@ -142,8 +136,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
           const uint32_t base = sb + OFF_A + st * A_BYTES;
           const uint32_t fb = bar_fa + 8 * st;
           mbar_arrive_expect_tx(fb, A_BYTES);
-          tma_load_4d(base + A_W, &tW, fb, 0, h, t0, b);
-          tma_load_4d(base + A_W + BLK, &tW, fb, 64, h, t0, b);
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(base + A_WQ + kb * 2 * BLK, &tW, fb, kb * 64, h, t0, b);
+            tma_load_4d(base + A_WQ + kb * 2 * BLK + BLK, &tQ, fb, kb * 64, h >> 1, t0, b);
+          }
           tma_load_4d(base + A_U, &tU, fb, 0, h, t0, b);
           issued_a = c + 1;
         }
@@ -155,11 +152,9 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
           const uint32_t fb = bar_fb + 8 * st;
           const int64_t cgi = (int64_t)b * nch + c;
           mbar_arrive_expect_tx(fb, B_BYTES);
-          tma_load_4d(base + B_Q, &tQ, fb, 0, h >> 1, t0, b);
-          tma_load_4d(base + B_Q + BLK, &tQ, fb, 64, h >> 1, t0, b);
-          tma_load_4d(base + B_KD, &tKd, fb, 0, h, t0, b);
-          tma_load_4d(base + B_KD + BLK, &tKd, fb, 64, h, t0, b);
-          tma_load_2d(base + B_AQ, &tA, fb, 0, (int)((cgi * HV + h) * C));
+          tma_load_4d(base, &tKd, fb, 0, h, t0, b);
+          tma_load_4d(base + BLK, &tKd, fb, 64, h, t0, b);
+          tma_load_2d(base + 2 * BLK, &tA, fb, 0, (int)((cgi * HV + h) * C));
           issued_b = c + 1;
         }
       }
@@ -173,49 +168,38 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t id_n64 = idesc_f16_f32(128, 64);
-      constexpr uint32_t id_s = idesc_f16_f32(128, 128, 0, 1);   // B (Kd) MN-major
+      constexpr uint32_t id_1 = idesc_f16_f32(128, 128);          // [W ; Q] K-major
+      constexpr uint32_t id_2 = idesc_f16_f32(128, 192, 0, 1);    // [Kd | Aqk^T] MN-major
       bool any = false;
       for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
         const uint32_t ph = (uint32_t)c & 1;
         const uint32_t pa = sb + OFF_A + st * A_BYTES;
         const uint32_t pb = sb + OFF_B + st * B_BYTES;
+        // [U^T | O1^T] = S0h . [W ; Q]^T, once the previous chunk's O has been drained
         if (!mbar_wait(bar_fa + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
-            !mbar_wait(bar_s0, ph, status, DEV_TIMEOUT_MMA))
+            !mbar_wait(bar_s0, ph, status, DEV_TIMEOUT_MMA) ||
+            (c >= 1 && !mbar_wait(bar_oe, (c - 1) & 1, status, DEV_TIMEOUT_MMA)))
           break;
         tc_fence_after();
-        // U^T = S0h . W^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           tc_mma_f16_ts(tmem + COL_UACC, tmem + COL_S0H + kk * 8,
-                        sdesc_k_sw128(pa + A_W + (kk >> 2) * BLK + (kk & 3) * 32), id_n64, kk != 0);
+                        sdesc_k_sw128(pa + A_WQ + (kk >> 2) * 2 * BLK + (kk & 3) * 32), id_1,
+                        kk != 0);
         tc_commit(bar_u);
-        tc_commit(bar_ea + 8 * st);   // W no longer read (the row threads add theirs for U')
+        tc_commit(bar_ea + 8 * st);   // W, Q no longer read (the row threads add theirs for U')
         any = true;
-        // O1^T = S0h . Q^T, once the previous chunk's O is drained and part B has landed
-        if ((c >= 1 && !mbar_wait(bar_oe, (c - 1) & 1, status, DEV_TIMEOUT_MMA)) ||
-            !mbar_wait(bar_fb + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA))
+        // [S | O2^T] += U^T . [Kd | Aqk^T]
+        if (!mbar_wait(bar_fb + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
+            !mbar_wait(bar_uh, ph, status, DEV_TIMEOUT_MMA))
           break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_f16_ts(tmem + COL_O1, tmem + COL_S0H + kk * 8,
-                        sdesc_k_sw128(pb + B_Q + (kk >> 2) * BLK + (kk & 3) * 32), id_n64, kk != 0);
-        // S += U^T . Kd  (S was scaled by exp(g_C) in place by the row threads)
-        if (!mbar_wait(bar_uh, ph, status, DEV_TIMEOUT_MMA)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
           tc_mma_f16_ts(tmem + COL_S, tmem + COL_UH + kk * 8,
-                        sdesc_mn_sw128(pb + B_KD + kk * 16 * 128, BLK, 1024), id_s, 1);
+                        sdesc_mn_sw128(pb + kk * 16 * 128, BLK, 1024), id_2, 1);
         tc_commit(bar_s);
-        // O2^T = U^T . Aqk^T
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          tc_mma_f16_ts(tmem + COL_O2, tmem + COL_UH + kk * 8,
-                        sdesc_k_sw128(pb + B_AQ + kk * 32), id_n64, kk != 0);
-        tc_commit(bar_o);
         tc_commit(bar_eb + 8 * st);
       }
       // tensor memory is freed only after every MMA issued here has completed
@@ -230,7 +214,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     const int half = (warp - 4) >> 2;                        // which half of the columns
     const int v = quarter * 32 + lane;                       // value row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    // entering state: s0 row v (this thread's 64 key columns), or zero
+    // entering state: s0 row v (this thread's 64 key columns), or zero; O2 starts at zero
 #pragma unroll 1
     for (int cb = 2 * half; cb < 2 * half + 2; ++cb) {
       uint32_t r[32];
@@ -250,6 +234,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         for (int i = 0; i < 32; ++i) r[i] = 0u;
       }
       tmem_st_32x32b_x32(tl + COL_S + cb * 32, r);
+    }
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      tmem_st_32x32b_x32(tl + COL_O2 + half * 32, z);
     }
     tc_wait_st();
     float eC_next = __ldg(efh + (C - 1));
@@ -288,7 +278,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_s0);
-      // U' of this row for tokens 32 half .. 32 half + 31, read while the U MMAs run
+      // U' of this row for tokens 32 half .. 32 half + 31, read while the MMAs run
       const float* us = reinterpret_cast<const float*>(smem + OFF_A + st * A_BYTES + A_U) +
                         (half * 32) * D + v;
       float up[32];
@@ -349,7 +339,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         fa_next = __ldg(efh + (int64_t)(c + 1) * HV * C + lane);
         fb_next = __ldg(efh + (int64_t)(c + 1) * HV * C + 32 + lane);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      // O1 is complete with [U | O1], O2 with [S | O2]
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
       if (!ok) break;
       tc_fence_after();
       // O = exp(g)/sqrt(128) O1 + O2 in two halves of 32 tokens, kept as fp16 pairs
@@ -369,6 +360,15 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
                                       f1 * u2f(o1[2 * j + 1]) + u2f(o2[2 * j + 1]));
         }
       }
+      {
+        // O2 accumulates from zero in the next chunk
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+        tmem_st_32x32b_x32(tl + COL_O2, z);
+        tmem_st_32x32b_x32(tl + COL_O2 + 32, z);
+      }
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
