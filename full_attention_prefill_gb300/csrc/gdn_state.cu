@@ -339,26 +339,36 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         fa_next = __ldg(efh + (int64_t)(c + 1) * HV * C + lane);
         fb_next = __ldg(efh + (int64_t)(c + 1) * HV * C + 32 + lane);
       }
-      // O1 is complete with [U | O1], O2 with [S | O2]
+      // O1 is complete with [U | O1]: read and scale it while U is converted and S updated
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      if (!ok) break;
+      tc_fence_after();
+      float fo[64];
+      {
+        uint32_t o1[32];
+        tmem_ld_32x32b_x32(tl + COL_O1, o1);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) fo[j] = __shfl_sync(0xffffffffu, fa, j) * u2f(o1[j]);
+        tmem_ld_32x32b_x32(tl + COL_O1 + 32, o1);
+        tc_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) fo[32 + j] = __shfl_sync(0xffffffffu, fb, j) * u2f(o1[j]);
+      }
+      // O2 with [S | O2]; O = exp(g)/sqrt(128) O1 + O2, kept as fp16 pairs
       ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
       if (!ok) break;
       tc_fence_after();
-      // O = exp(g)/sqrt(128) O1 + O2 in two halves of 32 tokens, kept as fp16 pairs
       uint32_t y[32];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t o1[32], o2[32];
-        tmem_ld_32x32b_x32(tl + COL_O1 + hf * 32, o1);
+        uint32_t o2[32];
         tmem_ld_32x32b_x32(tl + COL_O2 + hf * 32, o2);
         tc_wait_ld();
-        const float fh = hf ? fb : fa;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float f0 = __shfl_sync(0xffffffffu, fh, 2 * j);
-          const float f1 = __shfl_sync(0xffffffffu, fh, 2 * j + 1);
-          y[hf * 16 + j] = pack_half2(f0 * u2f(o1[2 * j]) + u2f(o2[2 * j]),
-                                      f1 * u2f(o1[2 * j + 1]) + u2f(o2[2 * j + 1]));
-        }
+        for (int j = 0; j < 16; ++j)
+          y[hf * 16 + j] = pack_half2(fo[hf * 32 + 2 * j] + u2f(o2[2 * j]),
+                                      fo[hf * 32 + 2 * j + 1] + u2f(o2[2 * j + 1]));
       }
       {
         // O2 accumulates from zero in the next chunk
