@@ -122,32 +122,46 @@ __global__ void log_alpha_kernel(const float* __restrict__ alpha, float* __restr
 }
 
 // ------------------------------------------------------------------------------------------
-// Phase 1: per (chunk, value head): cumulative g, T = (I + A)^-1, W = T diag(beta e^g) K,
-// U' = T diag(beta) V.  128 threads; warp w owns rows 16w .. 16w+15 of every 64-row product.
+// Phase 1: per (chunk, value head): cumulative g, A, T = (I + A)^-1, W = T diag(beta e^g) K,
+// U' = T diag(beta) V, the decayed keys and Aqk.  128 threads; warp w owns rows 16w .. 16w+15
+// of every 64-row product.  Outputs go to one contiguous block per (chunk, head): W [64][128]
+// fp16, U' [64][128] fp32, Kd [64][128] fp16, Aqk^T [64][64] fp16, exp(g) [64] fp32.  Rows past
+// the request's end come out zero (their beta, K and V are zero).
+// T is formed blockwise: the four 16x16 diagonal blocks by forward substitution (one warp each),
+// then the off-diagonal blocks by distance d = 1, 2, 3 from the diagonal:
+//     T_ij = -T_ii (sum_{j <= k < i} A_ik T_kj),
+// all in fp32.
 // ------------------------------------------------------------------------------------------
 struct WySmem {
-  __half Q[C][LDH];
-  __half K[C][LDH];    // K, then beta * exp(g) * K in place
-  __half V[C][LDH];    // V, then beta * V in place
-  __half T[C][C + 8];  // (I + A)^-1 in fp16 for the products
-  float A[C][C + 4];   // 16-byte aligned rows for broadcast float4 reads
+  union {
+    __half Q[C][LDH];                            // until Aqk is formed
+    float A[C][C + 4];                           // then A (strictly lower triangular)
+    struct {
+      __half Tw[C][C + 8];                       // then T diag(beta e^g)
+      __half Tu[C][C + 8];                       //  and T diag(beta), the products' A operands
+    } t;
+  } u;
+  __half K[C][LDH];
+  __half V[C][LDH];
+  float Tf[C][C + 4];                            // T in fp32
   float gc[C];
   float bt[C];
-  float eb[C];         // beta_r exp(g_r)
-  float ed[C];         // exp(g_C - g_r)
+  float eb[C];                                   // beta_r exp(g_r)
+  float ed[C];                                   // exp(g_C - g_r)
 };
 
 __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const __half* __restrict__ qq, const __half* __restrict__ kk, const __half* __restrict__ vv,
     const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ ef,
-    __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Ktout,
-    __half* __restrict__ Aqk, int L, int nch) {
+    __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Kdout,
+    __half* __restrict__ AqkT, int L, int nch) {
   extern __shared__ __align__(16) uint8_t smraw[];
   WySmem& s = *reinterpret_cast<WySmem*>(smraw);
   const int cg = blockIdx.x;           // global chunk index = b * nch + c
   const int h = blockIdx.y;            // value head
   const int b = cg / nch, c = cg % nch;
   const int64_t t0 = (int64_t)b * L + (int64_t)c * C;
+  const int64_t blk = (int64_t)cg * HV + h;   // output block
   const int nvalid = min(C, L - c * C);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -157,7 +171,7 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < nvalid;
     const int64_t rr = ok ? t0 + r : t0;
-    cp_async16(smem_u32(&s.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
+    cp_async16(smem_u32(&s.u.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
     cp_async16(smem_u32(&s.K[r][c8]), kk + rr * (HK * D) + (h >> 1) * D + c8, ok);
     cp_async16(smem_u32(&s.V[r][c8]), vv + rr * (HV * D) + h * D + c8, ok);
   }
@@ -182,27 +196,75 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   }
   cp_async_wait<0>();
   __syncthreads();
-  // exp of the cumulative log alpha for the state pass (rows past the end repeat the last one)
-  if (tid < C) ef[((int64_t)cg * HV + h) * C + tid] = __expf(s.gc[tid]);
   const float gC = s.gc[C - 1];  // rows past the end add g = 0, so this is the chunk's last g
   if (tid < C) {
-    s.eb[tid] = s.bt[tid] * __expf(s.gc[tid]);
+    const float e = __expf(s.gc[tid]);
+    ef[blk * C + tid] = e;       // for the state pass
+    s.eb[tid] = s.bt[tid] * e;
     s.ed[tid] = __expf(gC - s.gc[tid]);
   }
+  __syncthreads();
 
   const uint32_t sK = smem_u32(&s.K[0][0]);
-  const uint32_t sQ = smem_u32(&s.Q[0][0]);
-  // A = strict_tril(beta_r e^{g_r - g_s} k_r . k_s) and Aqk = tril(q_r . k_s e^{g_r - g_s}) / sqrt(128)
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    const uint32_t sA = which == 0 ? sK : sQ;
+  // Aqk = tril(q_r . k_s e^{g_r - g_s}) / sqrt(128), stored transposed ([s][r])
+  {
+    const uint32_t sQ = smem_u32(&s.u.Q[0][0]);
     float acc[8][4];
 #pragma unroll
     for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t a[4];
-      ldsm_x4(a, a_addr(sA, LDH, warp * 16, ks * 16, lane));
+      ldsm_x4(a, a_addr(sQ, LDH, warp * 16, ks * 16, lane));
+#pragma unroll
+      for (int n = 0; n < 8; n += 2) {
+        uint32_t bq[4];
+        ldsm_x4(bq, bn_addr(sK, LDH, n * 8, ks * 16, lane));
+        mma16816(acc[n], a, bq[0], bq[1]);
+        mma16816(acc[n + 1], a, bq[2], bq[3]);
+      }
+    }
+    __half* at = AqkT + blk * C * C;
+    const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = warp * 16 + gq + hf * 8;
+        const int col = n * 8 + 2 * tq;
+        const float v0 = (col <= r) ? __expf(s.gc[r] - s.gc[col]) * acc[n][2 * hf] * scale : 0.f;
+        const float v1 =
+            (col + 1 <= r) ? __expf(s.gc[r] - s.gc[col + 1]) * acc[n][2 * hf + 1] * scale : 0.f;
+        at[col * C + r] = __float2half_rn(v0);
+        at[(col + 1) * C + r] = __float2half_rn(v1);
+      }
+    }
+  }
+  // decayed keys exp(g_C - g_r) k_r, 16 bytes per store
+  for (int i = tid; i < C * (D / 8); i += 128) {
+    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
+    const uint4 kv = *reinterpret_cast<const uint4*>(&s.K[r][c8]);
+    const __half2* kh = reinterpret_cast<const __half2*>(&kv);
+    const float e = s.ed[r];
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(kh[j]);
+      op[j] = h2u(e * f.x, e * f.y);
+    }
+    *reinterpret_cast<uint4*>(Kdout + (blk * C + r) * D + c8) = o;
+  }
+  __syncthreads();  // Q is dead: A takes its place
+  // A = strict_tril(beta_r e^{g_r - g_s} k_r . k_s)
+  {
+    float acc[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(a, a_addr(sK, LDH, warp * 16, ks * 16, lane));
 #pragma unroll
       for (int n = 0; n < 8; n += 2) {
         uint32_t bq[4];
@@ -217,67 +279,81 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
       for (int hf = 0; hf < 2; ++hf) {
         const int r = warp * 16 + gq + hf * 8;
         const int col = n * 8 + 2 * tq;
-        const float d0 = __expf(s.gc[r] - s.gc[col]), d1 = __expf(s.gc[r] - s.gc[col + 1]);
-        if (which == 0) {
-          s.A[r][col] = (col < r) ? s.bt[r] * d0 * acc[n][2 * hf] : 0.f;
-          s.A[r][col + 1] = (col + 1 < r) ? s.bt[r] * d1 * acc[n][2 * hf + 1] : 0.f;
-        } else {
-          const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
-          const float v0 = (col <= r) ? d0 * acc[n][2 * hf] * scale : 0.f;
-          const float v1 = (col + 1 <= r) ? d1 * acc[n][2 * hf + 1] * scale : 0.f;
-          // stored transposed, [s][r], the layout the state pass reads it in
-          __half* at = Aqk + ((int64_t)cg * HV + h) * C * C;
-          at[col * C + r] = __float2half_rn(v0);
-          at[(col + 1) * C + r] = __float2half_rn(v1);
+        const float br = s.bt[r];
+        s.u.A[r][col] = (col < r) ? br * __expf(s.gc[r] - s.gc[col]) * acc[n][2 * hf] : 0.f;
+        s.u.A[r][col + 1] =
+            (col + 1 < r) ? br * __expf(s.gc[r] - s.gc[col + 1]) * acc[n][2 * hf + 1] : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  // T, diagonal blocks: warp w inverts I + A_ww, lane j < 16 owning column j of the block
+  if (lane < 16) {
+    const int base = 16 * warp;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) t[r] = (r == lane) ? 1.f : 0.f;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) {
+        if (j & 1) a1 += s.u.A[base + r][base + j] * t[j];
+        else a0 += s.u.A[base + r][base + j] * t[j];
+      }
+      if (r > lane) t[r] = -(a0 + a1);
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) s.Tf[base + r][base + lane] = t[r];
+  }
+  __syncthreads();
+  // T, off-diagonal blocks at distance d: block (i, j = i - d); thread (block, column cc, row
+  // half rh) forms column cc of X = sum_k A_ik T_kj, then rows 8 rh .. 8 rh + 7 of -T_ii X
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {
+    if (tid < (4 - d) * 32) {
+      const int j = tid >> 5, i = j + d;
+      const int cc = lane & 15, rh = lane >> 4;
+      const int i0 = 16 * i, colg = 16 * j + cc;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) x[r] = 0.f;
+      for (int kq = 4 * j; kq < 4 * i; ++kq) {   // 4 columns of A_i. (rows of T_.j) per step
+        float tv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tv[e] = s.Tf[4 * kq + e][colg];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float4 av = *reinterpret_cast<const float4*>(&s.u.A[i0 + r][4 * kq]);
+          x[r] += av.x * tv[0] + av.y * tv[1] + av.z * tv[2] + av.w * tv[3];
         }
       }
-    }
-  }
-  __syncthreads();
-  // decayed keys to global; K -> beta e^g K and V -> beta V in place
-  for (int i = tid; i < C * (D / 2); i += 128) {
-    const int r = i / (D / 2), c2 = (i % (D / 2)) * 2;
-    const float eb = s.eb[r], ed = s.ed[r];
-    const float2 kf = __half22float2(*reinterpret_cast<const __half2*>(&s.K[r][c2]));
-    const float2 vf = __half22float2(*reinterpret_cast<const __half2*>(&s.V[r][c2]));
-    *reinterpret_cast<__half2*>(&s.K[r][c2]) = __floats2half2_rn(eb * kf.x, eb * kf.y);
-    *reinterpret_cast<__half2*>(&s.V[r][c2]) = __floats2half2_rn(s.bt[r] * vf.x, s.bt[r] * vf.y);
-    if (r < nvalid)
-      *reinterpret_cast<__half2*>(Ktout + ((t0 + r) * HV + h) * D + c2) =
-          __floats2half2_rn(ed * kf.x, ed * kf.y);
-  }
-  __syncthreads();
-  // T = (I + A)^-1 by forward substitution: T[r][sc] = -sum_{j<r} A[r][j] T[j][sc] (r > sc).
-  // Column sc depends only on earlier rows of the same column: thread sc keeps its column in
-  // registers and all 64 threads read each A row as the same (broadcast) float4s.  A is zero on
-  // and above the diagonal, so whole float4s can be read past j = r.
-  if (tid < C) {
-    const int sc = tid;
-    float tcol[C];
 #pragma unroll
-    for (int r = 0; r < C; ++r) tcol[r] = (r == sc) ? 1.f : 0.f;
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = 8 * rh + rr;
+        float acc = 0.f;
 #pragma unroll
-    for (int r = 1; r < C; ++r) {
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-      for (int j = 0; j < r; j += 4) {
-        const float4 av = *reinterpret_cast<const float4*>(&s.A[r][j]);
-        a0 += av.x * tcol[j];
-        a1 += av.y * tcol[j + 1];
-        a2 += av.z * tcol[j + 2];
-        a3 += av.w * tcol[j + 3];
+        for (int m = 0; m < 16; m += 4) {
+          const float4 tvv = *reinterpret_cast<const float4*>(&s.Tf[i0 + r][i0 + m]);
+          acc += tvv.x * x[m] + tvv.y * x[m + 1] + tvv.z * x[m + 2] + tvv.w * x[m + 3];
+        }
+        s.Tf[i0 + r][colg] = -acc;
       }
-      const float val = -((a0 + a1) + (a2 + a3));
-      tcol[r] = (r > sc) ? val : tcol[r];
     }
-#pragma unroll
-    for (int r = 0; r < C; ++r) s.T[r][sc] = __float2half_rn(tcol[r]);
+    __syncthreads();
+  }
+  // A is dead: T diag(beta e^g) and T diag(beta) in fp16 (blocks above the diagonal are zero)
+  for (int i = tid; i < C * C; i += 128) {
+    const int r = i / C, sc = i % C;
+    const float tv = (sc >> 4) > (r >> 4) ? 0.f : s.Tf[r][sc];
+    s.u.t.Tw[r][sc] = __float2half_rn(tv * s.eb[sc]);
+    s.u.t.Tu[r][sc] = __float2half_rn(tv * s.bt[sc]);
   }
   __syncthreads();
-  // W = T KB and U' = T VB  (rows 16w.., all 128 columns)
-  const uint32_t sT = smem_u32(&s.T[0][0]);
+  // W = T diag(beta e^g) K and U' = T diag(beta) V  (rows 16w.., all 128 columns)
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
+    const uint32_t sT = smem_u32(which == 0 ? &s.u.t.Tw[0][0] : &s.u.t.Tu[0][0]);
     const uint32_t sB = smem_u32(which == 0 ? &s.K[0][0] : &s.V[0][0]);
     float acc[16][4];
 #pragma unroll
@@ -297,8 +373,7 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int r = warp * 16 + gq + half * 8;
-      if (r >= nvalid) continue;
-      const int64_t row = (t0 + r) * HV + h;
+      const int64_t row = blk * C + r;
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         const int col = n * 8 + 2 * tq;
@@ -370,9 +445,10 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   size_t n = 0;
   n += al256g(M * gdn::HV * 4);                          // g (from alpha)
   n += al256g(B * nch * gdn::HV * gdn::C * 4);           // exp(g) per chunk row
-  n += al256g(M * gdn::HV * gdn::D * 2);                 // W
-  n += al256g(M * gdn::HV * gdn::D * 4);                 // U'
-  n += al256g(M * gdn::HV * gdn::D * 2);                 // decayed keys
+  const int64_t rows = B * nch * gdn::C;                 // whole chunks
+  n += al256g(rows * gdn::HV * gdn::D * 2);              // W
+  n += al256g(rows * gdn::HV * gdn::D * 4);              // U'
+  n += al256g(rows * gdn::HV * gdn::D * 2);              // decayed keys
   n += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);  // Aqk
   if (with_norm) n += al256g(M * gdn::HV * gdn::D * 2);  // o before the output gate
   return n;
@@ -394,9 +470,10 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   GdnWs w;
   w.g = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * 4);
   w.ef = reinterpret_cast<float*>(p); p += al256g(B * nch * gdn::HV * gdn::C * 4);
-  w.W = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
-  w.U1 = reinterpret_cast<float*>(p); p += al256g(M * gdn::HV * gdn::D * 4);
-  w.Kt = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
+  const int64_t rows = B * nch * gdn::C;
+  w.W = reinterpret_cast<__half*>(p); p += al256g(rows * gdn::HV * gdn::D * 2);
+  w.U1 = reinterpret_cast<float*>(p); p += al256g(rows * gdn::HV * gdn::D * 4);
+  w.Kt = reinterpret_cast<__half*>(p); p += al256g(rows * gdn::HV * gdn::D * 2);
   w.Aqk = reinterpret_cast<__half*>(p); p += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);
   w.o = reinterpret_cast<__half*>(p);
   return w;

@@ -25,10 +25,10 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
                             const __half* z, int64_t ldz, const __half* o_norm, __half* out,
                             int64_t ldo, int64_t B, int64_t L, void* ws, cudaStream_t stream);
 
-// The sequential state pass on tcgen05 (gdn_state.cu).  Inputs are the chunk phase's outputs:
-// W, decayed keys Kd [B, L, 32, 128] fp16, U' [B, L, 32, 128] fp32, Aqk^T [B * nch, 32, 64, 64]
-// fp16 ([s][r]), ef [B * nch, 32, 64] fp32 (exp of the in-chunk cumulative log alpha), and q
-// [B, L, 16, 128] fp16.  out [B * L, ldo] fp16 (head h at columns 128 h ..).
+// The sequential state pass on tcgen05 (gdn_state.cu).  Inputs are the chunk phase's outputs,
+// one block per (chunk, head) in [B * nch, 32] order: W and decayed keys Kd [64][128] fp16, U'
+// [64][128] fp32, Aqk^T [64][64] fp16 ([s][r]), ef [64] fp32 (exp of the in-chunk cumulative
+// log alpha); and q [B, L, 16, 128] fp16.  out [B * L, ldo] fp16 (head h at columns 128 h ..).
 clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W, const float* U1,
                              const __half* Aqk, const float* ef, const float* s0, float* s_out,
                              __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream);

@@ -21,7 +21,8 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA: per chunk part A = W, Q (two 64-column boxes each, 128-byte swizzle) and U'
-//               (fp32 [64 tok][128 v]); part B = Kd (two boxes) and Aqk^T; two stages of each.
+//               (fp32 [64 tok][128 v], one bulk copy); part B = Kd (two boxes) and Aqk^T; two
+//               stages of each.  W, U', Kd, Aqk^T are the chunk phase's per-(chunk, head) blocks.
 //   warp 1      MMA issue (one thread) and tensor-memory allocation
 //   warps 4-11  row threads, two per value row v = TMEM lane (warps 4-7 key columns / tokens
 //               0..63 / 0..31, warps 8-11 the rest): per chunk copy S to S0h (fp16) and scale S
@@ -67,9 +68,8 @@ __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tQ,
-    const __grid_constant__ CUtensorMap tKd, const __grid_constant__ CUtensorMap tU,
-    const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tO,
-    const float* __restrict__ ef, const float* __restrict__ s0, float* __restrict__ s_out, int L,
+    const __grid_constant__ CUtensorMap tKd, const __grid_constant__ CUtensorMap tA,
+    const __grid_constant__ CUtensorMap tO, const float* __restrict__ U1, const float* __restrict__ ef, const float* __restrict__ s0, float* __restrict__ s_out, int L,
     int nch, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     tma_prefetch_desc(&tW);
     tma_prefetch_desc(&tQ);
     tma_prefetch_desc(&tKd);
-    tma_prefetch_desc(&tU);
     tma_prefetch_desc(&tA);
     tma_prefetch_desc(&tO);
   }
@@ -135,13 +134,14 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         {
           const uint32_t base = sb + OFF_A + st * A_BYTES;
           const uint32_t fb = bar_fa + 8 * st;
+          const int64_t blk = ((int64_t)b * nch + c) * HV + h;   // the chunk phase's block
           mbar_arrive_expect_tx(fb, A_BYTES);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            tma_load_4d(base + A_WQ + kb * 2 * BLK, &tW, fb, kb * 64, h, t0, b);
+            tma_load_2d(base + A_WQ + kb * 2 * BLK, &tW, fb, kb * 64, (int)(blk * C));
             tma_load_4d(base + A_WQ + kb * 2 * BLK + BLK, &tQ, fb, kb * 64, h >> 1, t0, b);
           }
-          tma_load_4d(base + A_U, &tU, fb, 0, h, t0, b);
+          bulk_copy_g2s(base + A_U, U1 + blk * C * D, C * D * 4, fb);
           issued_a = c + 1;
         }
         if (c >= NSTAGE &&
@@ -150,11 +150,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         {
           const uint32_t base = sb + OFF_B + st * B_BYTES;
           const uint32_t fb = bar_fb + 8 * st;
-          const int64_t cgi = (int64_t)b * nch + c;
+          const int64_t blk = ((int64_t)b * nch + c) * HV + h;
           mbar_arrive_expect_tx(fb, B_BYTES);
-          tma_load_4d(base, &tKd, fb, 0, h, t0, b);
-          tma_load_4d(base + BLK, &tKd, fb, 64, h, t0, b);
-          tma_load_2d(base + 2 * BLK, &tA, fb, 0, (int)((cgi * HV + h) * C));
+          tma_load_2d(base, &tKd, fb, 0, (int)(blk * C));
+          tma_load_2d(base + BLK, &tKd, fb, 64, (int)(blk * C));
+          tma_load_2d(base + 2 * BLK, &tA, fb, 0, (int)(blk * C));
           issued_b = c + 1;
         }
       }
@@ -428,29 +428,24 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM));
     attr = true;
   }
-  CUtensorMap tW, tQ, tKd, tU, tA, tO;
+  CUtensorMap tW, tQ, tKd, tA, tO;
   {
-    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)HV, (uint64_t)L, (uint64_t)B};
-    const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)HV * D * 2, (uint64_t)L * HV * D * 2};
-    const uint32_t box[4] = {64, 1, (uint32_t)C, 1};
-    if (tma_encode(&tW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, W, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        tma_encode(&tKd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Kd, dims, strides, box,
-                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+    // the chunk phase's outputs: one block of 64 rows per (chunk, head)
+    const uint64_t rows = (uint64_t)(B * nch * HV * C);
+    if (tma_encode_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W, (uint64_t)D, rows, (uint64_t)D * 2,
+                      64, (uint32_t)C, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+        tma_encode_2d(&tKd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Kd, (uint64_t)D, rows,
+                      (uint64_t)D * 2, 64, (uint32_t)C, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+        tma_encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aqk, (uint64_t)C, rows,
+                      (uint64_t)C * 2, (uint32_t)C, (uint32_t)C,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
       return CLEF_E_CUDA;
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)HV, (uint64_t)L, (uint64_t)B};
+    const uint32_t box[4] = {64, 1, (uint32_t)C, 1};
     const uint64_t dq[4] = {(uint64_t)D, (uint64_t)HK, (uint64_t)L, (uint64_t)B};
     const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)HK * D * 2, (uint64_t)L * HK * D * 2};
     if (tma_encode(&tQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, q, dq, sq, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
-      return CLEF_E_CUDA;
-    const uint64_t su[3] = {(uint64_t)D * 4, (uint64_t)HV * D * 4, (uint64_t)L * HV * D * 4};
-    const uint32_t bu[4] = {(uint32_t)D, 1, (uint32_t)C, 1};
-    if (tma_encode(&tU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, U1, dims, su, bu,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
-      return CLEF_E_CUDA;
-    if (tma_encode_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Aqk, (uint64_t)C,
-                      (uint64_t)(B * nch * HV * C), (uint64_t)C * 2, (uint32_t)C, (uint32_t)C,
-                      CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
       return CLEF_E_CUDA;
     const uint64_t so[3] = {(uint64_t)D * 2, (uint64_t)ldo * 2, (uint64_t)L * ldo * 2};
     const uint32_t bo[4] = {32, 1, (uint32_t)C, 1};
@@ -463,7 +458,7 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
                 (double)B * L * HV * D * (2 + 2 + 4 + 2) + (double)B * L * HK * D * 2 +
                     chunks * Cd * Cd * 2);
   gdn_state_tc_kernel<<<(unsigned)(B * HV), ST_THREADS, ST_SMEM, stream>>>(
-      tW, tQ, tKd, tU, tA, tO, ef, s0, s_out, (int)L, (int)nch, status_word_ptr());
+      tW, tQ, tKd, tA, tO, U1, ef, s0, s_out, (int)L, (int)nch, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
