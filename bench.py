@@ -303,7 +303,9 @@ def run_micro(args):
     """One kernel entry point in a loop (CUDA events), for profiling and tuning.
 
     gemm: clef_lut6_gemm at M x N x K (fp16 out); attn: clef_gqa_attn_prefill at L (gated);
-    gdn: clef_gdn_prefill at L.  Prints one JSON line; not the headline metric.
+    gdn: clef_gdn_prefill at L; layer: clef_decoder_layer of layer --layer at L (the residual
+    copy-in is part of each iteration).  Prints one JSON line with the per-kernel times of the
+    library's trace; not the headline metric.
     """
     import numpy as np
     import torch
@@ -330,6 +332,19 @@ def run_micro(args):
         g = torch.from_numpy(synth.normal_f16(0, "g", 0, (1, L, 16, 256))).to(dev)
         fn = lambda: clef.gqa_attn_prefill(q, k, v, g)  # noqa: E731
         flops, desc = 4.0 * 256 * 16 * L * (L + 1) / 2, f"gqa_attn L={L}"
+    elif args.micro == "layer":
+        # one decoder layer (GDN for --layer 0, attention for --layer 3) on an fp32 residual
+        from full_attention_prefill_gb300.model import DeviceLayer, DeviceModel
+        L = args.L
+        layer = DeviceLayer(synth.layer_weights(0, args.layer), DeviceModel.kind_of(args.layer), dev)
+        x0 = torch.from_numpy(synth.normal_f32(0, "micro.x", 0, (1, L, 4096))).to(dev)
+        x = x0.clone()
+        ws = torch.empty(clef.prefill_workspace_size(1, L), dtype=torch.uint8, device=dev)
+
+        def fn():
+            x.copy_(x0)
+            clef.decoder_layer(layer, x, workspace=ws)
+        flops, desc = 0.0, f"decoder_layer {args.layer} L={L}"
     else:
         L = args.L
         q = torch.from_numpy(synth.normal_f16(0, "q", 0, (1, L, 16, 128))).to(dev)
@@ -345,20 +360,36 @@ def run_micro(args):
         fn()
     clef.sync_status()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lib = clef.lib()
+    lib.clef_trace_begin()
     e0.record()
     for _ in range(args.steps):
         fn()
     e1.record()
     torch.cuda.synchronize()
+    entries = (TraceEntry * 32)()
+    n = ctypes.c_int32(0)
+    lib.clef_trace_end.argtypes = [ctypes.POINTER(TraceEntry), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    rc = lib.clef_trace_end(entries, 32, ctypes.byref(n))
     clef.sync_status()
     ms = e0.elapsed_time(e1) / args.steps
+    kernels = {}
+    if rc == 0:
+        for i in range(n.value):
+            e = entries[i]
+            kernels[e.name.decode()] = {"ms": round(e.ms / args.steps, 4),
+                                        "GB/s": round(e.bytes / (e.ms * 1e6), 1) if e.ms > 0 else None}
+        if flops == 0.0:
+            flops = sum(entries[i].flops for i in range(n.value)) / args.steps
     print(json.dumps({"micro": desc, "ms": ms, "tflops": flops / ms / 1e9,
-                      "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"]}), flush=True)
+                      "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"], "kernels": kernels}),
+          flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--micro", choices=["gemm", "attn", "gdn"], default=None)
+    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer"], default=None)
+    ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--n", type=int, default=24576)
     ap.add_argument("--k", type=int, default=4096)

@@ -35,80 +35,101 @@ constexpr float kLogAlphaMin = -30.0f;
 
 // ------------------------------------------------------------------------------------------
 // Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels and
-// the per-head L2 norm of q and k.  A CTA covers 16 consecutive tokens for 1024 channels (128
-// threads x 8 channels); each thread issues the loads of all 19 rows it needs at once and keeps
-// them in registers.  The gates come from the a/b projection's epilogue.
+// the per-head L2 norm of q and k.  A CTA (256 threads) takes a tile of PREP_T tokens x 512
+// channels: all PREP_T + 3 rows (the conv's history included) are copied into shared memory at
+// once with cp.async, so three CTAs per SM keep ~200 KB of loads in flight; then thread (token
+// half, 4 channels) walks its PREP_T / 2 tokens with the 3-row history in registers.  A warp
+// covers 128 channels, exactly one q or k head, so the norm is a warp reduction.  The gates
+// come from the a/b projection's epilogue.
 // proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..).
 // ------------------------------------------------------------------------------------------
-constexpr int PREP_T = 16;
-__global__ void __launch_bounds__(128) gdn_prep_kernel(
+constexpr int PREP_T = 64;
+constexpr int PREP_CH = 512;
+constexpr int PREP_SMEM = (PREP_T + 3) * PREP_CH * 2;
+__global__ void __launch_bounds__(256) gdn_prep_kernel(
     const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
     __half* __restrict__ q, __half* __restrict__ k, __half* __restrict__ v, int64_t M, int L) {
+  extern __shared__ __align__(16) uint8_t prep_smem[];
+  __half* tile = reinterpret_cast<__half*>(prep_smem);   // [PREP_T + 3][PREP_CH], row i = token tok0 - 3 + i
   const int tid = threadIdx.x;
-  const int ch0 = blockIdx.x * 1024 + tid * 8;
+  const int cbase = blockIdx.x * PREP_CH;
   const int64_t tok0 = (int64_t)blockIdx.y * PREP_T;
-  float w[8][4];
+  // rows outside [0, M) are zero-filled
+  for (int i = tid; i < (PREP_T + 3) * (PREP_CH / 8); i += 256) {
+    const int r = i / (PREP_CH / 8), c8 = (i % (PREP_CH / 8)) * 8;
+    const int64_t t = tok0 - 3 + r;
+    const bool ok = t >= 0 && t < M;
+    cp_async16(smem_u32(tile + r * PREP_CH + c8), proj + (ok ? t : 0) * ldp + cbase + c8, ok);
+  }
+  cp_async_commit();
+  const int cl = (tid & 127) * 4;           // this thread's 4 channels within the tile
+  const int ch0 = cbase + cl;
+  const int th = tid >> 7;                  // token half
+  float w[4][4];                            // [channel][tap]
   {
     const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (int64_t)ch0 * 4);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 u = wp[i];
+    for (int i = 0; i < 2; ++i) {
+      const uint4 u = __ldg(wp + i);
       const __half* hh = reinterpret_cast<const __half*>(&u);
 #pragma unroll
       for (int j = 0; j < 8; ++j) w[(i * 8 + j) / 4][(i * 8 + j) % 4] = __half2float(hh[j]);
     }
   }
-  // rows tok0 - 3 .. tok0 + PREP_T - 1, all loads in flight at once; rows before the start of
-  // their request or past M are zero
-  uint4 xr[PREP_T + 3];
-  const int pos0 = (int)(tok0 % L);
+  const bool is_qk = ch0 < 4096;
+  __half* dst0 = ch0 < 2048 ? q + ch0 : (ch0 < 4096 ? k + (ch0 - 2048) : v + (ch0 - 4096));
+  const int64_t ldd = ch0 < 4096 ? 2048 : 4096;
+  const int j0 = th * (PREP_T / 2);         // first token of this thread, within the tile
+  int pos = (int)((tok0 + j0) % L);         // its position in its request
+  cp_async_wait<0>();
+  __syncthreads();
+  // the 4 channels of tile row r as floats
+  auto rd = [&](int r, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(tile + r * PREP_CH + cl);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  };
+  float h0[4], h1[4], h2[4];                // tokens t-3, t-2, t-1
+  rd(j0, h0);
+  rd(j0 + 1, h1);
+  rd(j0 + 2, h2);
+#pragma unroll 4
+  for (int j = j0; j < j0 + PREP_T / 2; ++j) {
+    const int64_t tok = tok0 + j;
+    float x3[4];
+    rd(j + 3, x3);
+    if (tok < M) {
+      float y[4];
+      if (pos >= 3) {                         // the same for the whole warp (one token)
 #pragma unroll
-  for (int i = 0; i < PREP_T + 3; ++i) {
-    const int64_t tok = tok0 - 3 + i;
-    const bool ok = (i >= 3 || pos0 >= 3 - i) && tok < M;
-    xr[i] = ok ? *reinterpret_cast<const uint4*>(proj + tok * ldp + ch0) : make_uint4(0, 0, 0, 0);
-  }
+        for (int c = 0; c < 4; ++c)
+          y[c] = silu_f(w[c][0] * h0[c] + w[c][1] * h1[c] + w[c][2] * h2[c] + w[c][3] * x3[c]);
+      } else {
+        // taps reaching before the request's start read zero
+        const float m0 = pos >= 3 ? 1.f : 0.f, m1 = pos >= 2 ? 1.f : 0.f, m2 = pos >= 1 ? 1.f : 0.f;
 #pragma unroll
-  for (int i = 0; i < PREP_T; ++i) {
-    const int64_t tok = tok0 + i;
-    if (tok >= M) break;
-    const int pos = (int)(tok % L);
-    float y[8];
-#pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2) {
-      float2 xs[4];
-#pragma unroll
-      for (int tap = 0; tap < 4; ++tap) {
-        // tap j multiplies x[t - 3 + j]; positions before the request's start are zero
-        const uint4 u = xr[i + tap];
-        const __half2 hv = reinterpret_cast<const __half2*>(&u)[c2];
-        xs[tap] = (pos - 3 + tap >= 0) ? __half22float2(hv) : make_float2(0.f, 0.f);
+        for (int c = 0; c < 4; ++c)
+          y[c] = silu_f(m0 * w[c][0] * h0[c] + m1 * w[c][1] * h1[c] + m2 * w[c][2] * h2[c] +
+                        w[c][3] * x3[c]);
       }
+      if (is_qk) {
+        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = 2 * c2 + e;
-        const float pre = w[c][0] * (e ? xs[0].y : xs[0].x) + w[c][1] * (e ? xs[1].y : xs[1].x) +
-                          w[c][2] * (e ? xs[2].y : xs[2].x) + w[c][3] * (e ? xs[3].y : xs[3].x);
-        y[c] = silu_f(pre);
+        for (int off = 1; off < 32; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) y[c] *= r;
       }
+      *reinterpret_cast<uint2*>(dst0 + tok * ldd) = make_uint2(h2u(y[0], y[1]), h2u(y[2], y[3]));
     }
-    __half* dst;
-    if (ch0 < 4096) {
-      // q or k: a head is 128 channels = 16 consecutive threads
-      float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ss += y[c] * y[c];
-#pragma unroll
-      for (int off = 1; off < 16; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      const float r = rsqrtf(ss + 1e-6f);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] *= r;
-      dst = ch0 < 2048 ? q + tok * 2048 + ch0 : k + tok * 2048 + (ch0 - 2048);
-    } else {
-      dst = v + tok * 4096 + (ch0 - 4096);
+    for (int c = 0; c < 4; ++c) {
+      h0[c] = h1[c];
+      h1[c] = h2[c];
+      h2[c] = x3[c];
     }
-    *reinterpret_cast<uint4*>(dst) =
-        make_uint4(h2u(y[0], y[1]), h2u(y[2], y[3]), h2u(y[4], y[5]), h2u(y[6], y[7]));
+    pos = pos + 1 == L ? 0 : pos + 1;
   }
 }
 
@@ -492,8 +513,14 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
                             __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
-  dim3 grid(8, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
-  gdn::gdn_prep_kernel<<<grid, 128, 0, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
+  static bool attr = false;
+  if (!attr) {
+    CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::PREP_SMEM));
+    attr = true;
+  }
+  dim3 grid(8192 / gdn::PREP_CH, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
+  gdn::gdn_prep_kernel<<<grid, 256, gdn::PREP_SMEM, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
