@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
                      void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
-                     unsigned* status) {
+                     int ksplit, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -175,9 +175,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int n_tiles = (N + BN - 1) / BN;
   const int m_tiles = (M + BT - 1) / BT;
   const int num_tiles = n_tiles * m_tiles;
+  // work units: (tile, k part); with ksplit > 1 (residual-add mode only) each unit covers
+  // num_kb / ksplit steps and adds its partial sum into Y
+  const int nkb = num_kb / ksplit;
+  const int num_units = num_tiles * ksplit;
   // the accumulator of tile i is drained after the first `lead` steps of tile i+1 have been
   // dequantised, so the MMAs of tile i+1 start as soon as it is free
-  const int lead = min(AS - 1, num_kb - 1);
+  const int lead = min(AS - 1, nkb - 1);
 
   // One "ready" and one "empty" barrier per step (ring of AS): step g may run its MMAs once its
   // X tile has landed and its A stage is written (ready[g % AS]: the X bytes plus one arrival
@@ -231,10 +235,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int64_t g = 0;
       bool ok = true;
-      for (int t = first; t < num_tiles && ok; t += stride) {
+      for (int u = first; u < num_units && ok; u += stride) {
         int n0, m0;
-        tile_coord(t, n_tiles, m_tiles, n0, m0);
-        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        const int kb0 = (u / num_tiles) * nkb;
+        for (int kb = kb0; kb < kb0 + nkb; ++kb, ++g) {
           // X slot g % XS was last read by step g - XS
           const int64_t f = g - XS;
           if (f >= 0 && !mbar_wait(bar_empty + 8 * (int)(f % AS), (uint32_t)(f / AS) & 1, status,
@@ -258,9 +263,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int64_t g = 0;
       int it = 0;
       bool ok = true;
-      for (int t = first; t < num_tiles && ok; t += stride, ++it) {
+      for (int u = first; u < num_units && ok; u += stride, ++it) {
         int n0, m0;
-        tile_coord(t, n_tiles, m_tiles, n0, m0);
+        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        const int kb0 = (u / num_tiles) * nkb;
         const int ts = it & 1;
         if (it >= 2 && !mbar_wait(bar_tempty + 8 * ts, ((uint32_t)(it >> 1) & 1) ^ 1, status,
                                   DEV_TIMEOUT_TMA)) {
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(bar_tfull + 8 * ts, groups * 128);
         bulk_load(sb + OFF_T + ts * TBL_BYTES, lut + (size_t)(n0 / 16) * 64, groups * 128,
                   bar_tfull + 8 * ts);
-        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+        for (int kb = kb0; kb < kb0 + nkb; ++kb, ++g) {
           // slot s (indices and A stage) was last used by step g - AS
           const int s = (int)(g % AS);
           const uint32_t ph = (uint32_t)(g / AS) & 1;
@@ -297,12 +303,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;         // phase parity of ready[sa]
       int it = 0;
       bool ok = true;
-      for (int t = first; t < num_tiles && ok; t += stride, ++it) {
+      for (int u = first; u < num_units && ok; u += stride, ++it) {
         if (it >= 1 && !mbar_wait(bar_acce, (uint32_t)(it - 1) & 1, status, DEV_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(bar_ready + 8 * sa, ph, status, DEV_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -402,16 +408,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int it = 0;
     bool ok = true;
     int pn0 = -1, pm0 = 0;  // tile whose epilogue is pending
-    for (int t = first; t < num_tiles && ok; t += stride, ++it) {
+    for (int u = first; u < num_units && ok; u += stride, ++it) {
       int n0, m0;
-      tile_coord(t, n_tiles, m_tiles, n0, m0);
+      tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
       const int ts = it & 1;
       if (!mbar_wait(bar_tfull + 8 * ts, (uint32_t)(it >> 1) & 1, status, DEV_TIMEOUT_DEQUANT)) {
         ok = false;
         break;
       }
       const uint32_t tb = sb + OFF_T + ts * TBL_BYTES + grp * 128;
-      for (int kb = 0; kb < num_kb; ++kb, ++g) {
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
         if (kb == lead && pn0 >= 0) {
           ok = epilogue(pn0, pm0, it - 1);
           pn0 = -1;
@@ -533,7 +539,25 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   if ((reinterpret_cast<uintptr_t>(lut) & 15) != 0) return CLEF_E_ALIGN;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);
   const int sms = num_sms();
-  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  // Residual-add mode may split K across CTAs (each part adds its partial sum): when there are
+  // too few tiles to fill the GPU, pick the split that minimises the longest CTA's work, counted
+  // in k-steps plus about four steps per unit for its epilogue.
+  int ksplit = 1;
+  if (mode == EPI_ADD_F32) {
+    const int64_t nkb = K / BK;
+    int64_t best = -1;
+    for (int s = 1; s <= 8; ++s) {
+      if (nkb % s != 0 || nkb / s < 4) continue;
+      const int64_t rounds = (tiles * s + sms - 1) / sms;
+      const int64_t cost = rounds * (nkb / s + 4);
+      if (best < 0 || cost < best) {
+        best = cost;
+        ksplit = s;
+      }
+    }
+  }
+  const int64_t units = tiles * ksplit;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
   const double out_bytes = mode == EPI_F16 ? 2.0 * M * N
                            : mode == EPI_F32 ? 4.0 * M * N
                            : mode == EPI_ADD_F32 ? 8.0 * M * N
@@ -541,7 +565,7 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
                 0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
   lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, status_word_ptr());
+      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, ksplit, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
