@@ -76,45 +76,42 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
 // ------------------------------------------------------------------------------------------
 // tcgen05 flash attention.  CTA = 128 rows (32 positions x the 4 query heads of kv head g, row
 // r = 4 * position + head), keys in tiles of 64.
-//   warp 0   TMA: the Q tile once ([32 pos][4 heads][64 dims] boxes, 128-byte swizzle: a
-//            K-major [128 rows][256 dims] operand), then K tiles (3 stages)
+//   warp 0   TMA: K tiles (4 stages, 4 boxes of 64 dims, 128-byte swizzle)
 //   warp 2   TMA: V tiles (2 stages), a ring of its own so K runs ahead of V
-//   warp 1   MMA: S_j = Q K_j^T (M=128, N=64, 16 steps of K=16, both operands in shared memory)
-//            into one of three 64-column S buffers, as far ahead as the buffers allow
-//   warp 3   MMA: O += P_j V_j (M=128, N=256, K=64; P_j from one of two 32-column tensor-memory
-//            buffers, V an MN-major shared operand)
-//   warps 4-11 softmax, two threads per row (warps w and w+4 share TMEM lanes 32 (w % 4)..;
-//            warps 4-7 take keys 0..31 of a tile, warps 8-11 keys 32..63): read S_j and free its
-//            buffer, mask, online max/sum in base 2 with the two halves' maxima combined through
-//            shared memory, write P_j (fp16) into a P buffer once P_{j-2} V_{j-2} is done.  O is
-//            rescaled (in TMEM, each half of its columns by one of the two threads) only when a
-//            row's max grows by more than 2^8, so P stays below 256; the final O is divided by
-//            the row sum, multiplied by sigmoid(gate) and stored.
-// Tensor memory (512 columns): O [0,256), S_i [256 + 64 i) for i < 3, P_i [448 + 32 i), i < 2.
+//   warp 1   MMA: S_j = Q K_j^T (M=128, N=64, 16 steps of K=16; Q from tensor memory) into one
+//            of two 64-column S buffers, once P_{j-2} V_{j-2} has released that buffer
+//   warp 3   MMA: O += P_j V_j (M=128, N=256, K=64; P_j read from the first 32 columns of its S
+//            buffer, V an MN-major shared operand).  The two MMA chains have a thread each: a
+//            thread's mbarrier waits complete only after the MMAs it has committed.
+//   warps 4-11 first copy Q (rows of 256 dims, after rotary) from global memory into tensor
+//            memory; then softmax, two threads per row (warps w and w+4 share TMEM lanes
+//            32 (w % 4)..; warps 4-7 take keys 0..31 of a tile, warps 8-11 keys 32..63): read S,
+//            mask (diagonal tiles only), online max/sum in base 2 with the two halves' maxima
+//            combined through shared memory, write P (fp16) over the first 32 columns of its S
+//            buffer.  O is rescaled (in TMEM, each half of its columns by one of the two
+//            threads) only when a row's max grows by more than 2^8, so P stays below 256; the
+//            final O is divided by the row sum, multiplied by sigmoid(gate) and stored.
+// Tensor memory (512 columns): O [0,256), S/P buffers [256,320) and [320,384), Q [384,512).
 // ------------------------------------------------------------------------------------------
 constexpr int TBN = 64;                   // keys per tile
 constexpr int KV_BLOCK = TBN * 128;       // 8 KB: [64 keys][64 dims]
 constexpr int KV_BYTES = TBN * D * 2;     // 32 KB: 4 blocks
-constexpr int Q_BLOCK = BM * 128;         // 16 KB: [128 rows][64 dims]
-constexpr int Q_BYTES = BM * D * 2;       // 64 KB: 4 blocks
-constexpr int KST = 3, VST = 2;           // K and V ring stages
-constexpr int NSB = 3, NPB = 2;           // S buffers, P buffers
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int KST = 4, VST = 2;           // K and V ring stages
+constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KST * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
-constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 * NSB + 2 * NPB + 2;
+constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_XCH = OFF_SLOT + 16;       // [2 halves][128 rows] fp32: row max / row sum
 constexpr int FLASH_SMEM = OFF_XCH + 2 * BM * 4 + 1024;
 static_assert(FLASH_SMEM <= 232448, "shared memory per CTA");
 constexpr int FLASH_THREADS = 384;
-constexpr uint32_t S_COL = 256;           // S buffers
-constexpr uint32_t P_COL = 448;           // P buffers (fp16 pairs, the P V MMA's A operand)
+constexpr uint32_t S_COL = 256;           // S/P buffers at TMEM columns 256 and 320
+constexpr uint32_t Q_COL = 384;           // Q (the S MMAs' A operand): 128 columns of fp16 pairs
 constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 units)
 
 __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
-    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __half* __restrict__ q, int64_t ldq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __half* __restrict__ gate, int64_t ldg,
     __half* __restrict__ out, int64_t ldo, int L, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -130,21 +127,20 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   const int last_pos = min(p0 + POS, L) - 1;
   const int nt = last_pos / TBN + 1;
 
-  const uint32_t bar_q = sb + OFF_BAR;              // Q landed
+  const uint32_t bar_q = sb + OFF_BAR;              // Q written into tensor memory
   const uint32_t bar_kf = bar_q + 8;                // [KST] K tile landed
   const uint32_t bar_ke = bar_kf + 8 * KST;         // [KST] S MMAs done with a K stage
   const uint32_t bar_vf = bar_ke + 8 * KST;         // [VST] V tile landed
   const uint32_t bar_ve = bar_vf + 8 * VST;         // [VST] P V MMAs done with a V stage
-  const uint32_t bar_s = bar_ve + 8 * VST;          // [NSB] S_j complete
-  const uint32_t bar_sf = bar_s + 8 * NSB;          // [NSB] S_j read by the softmax warps
-  const uint32_t bar_p = bar_sf + 8 * NSB;          // [NPB] P_j written
-  const uint32_t bar_pf = bar_p + 8 * NPB;          // [NPB] P_j V_j done (P buffer free)
-  const uint32_t bar_fin = bar_pf + 8 * NPB;        // the last P V done
+  const uint32_t bar_s = bar_ve + 8 * VST;          // [2] S_j complete
+  const uint32_t bar_p = bar_s + 16;                // [2] P_j written
+  const uint32_t bar_pf = bar_p + 16;               // [2] P_j V_j done (S/P buffer free)
+  const uint32_t bar_fin = bar_pf + 16;             // the last P V done
   const uint32_t bar_sfin = bar_fin + 8;            // the last S done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    mbar_init(bar_q, 8);  // the 8 warps that write Q into tensor memory
     for (int i = 0; i < KST; ++i) {
       mbar_init(bar_kf + 8 * i, 1);
       mbar_init(bar_ke + 8 * i, 1);
@@ -153,18 +149,14 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       mbar_init(bar_vf + 8 * i, 1);
       mbar_init(bar_ve + 8 * i, 1);
     }
-    for (int i = 0; i < NSB; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_sf + 8 * i, 8);
-    }
-    for (int i = 0; i < NPB; ++i) {
       mbar_init(bar_p + 8 * i, 8);
       mbar_init(bar_pf + 8 * i, 1);
     }
     mbar_init(bar_fin, 1);
     mbar_init(bar_sfin, 1);
     fence_mbar_init();
-    tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
   }
@@ -179,15 +171,8 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
-    // warp 0: Q, then the K ring; warp 2: the V ring (one thread each, so neither ring waits
-    // for the other's stages to free)
     if (lane == 0) {
       const bool kside = warp == 0;
-      if (kside) {
-        mbar_arrive_expect_tx(bar_q, Q_BYTES);
-        for (int blk = 0; blk < 4; ++blk)
-          tma_load_4d(sb + OFF_Q + blk * Q_BLOCK, &tq, bar_q, blk * 64, 4 * g, p0, b);
-      }
       const int nst = kside ? KST : VST;
       const uint32_t bf = kside ? bar_kf : bar_vf, be = kside ? bar_ke : bar_ve;
       const uint32_t base = sb + (kside ? OFF_K : OFF_V);
@@ -206,33 +191,30 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       }
       // copies still in flight land before the CTA may exit (no later phase of these barriers
       // can complete, so the parity tests are unambiguous)
-      if (kside) mbar_wait(bar_q, 0, status, DEV_TIMEOUT_TMA);
       for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
         mbar_wait(bf + 8 * (j % nst), (uint32_t)(j / nst) & 1, status, DEV_TIMEOUT_TMA);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ S MMAs
-    // A thread's mbarrier waits complete only after the MMAs it has committed, so the S chain
-    // and the P V chain have a thread each: S_j is issued as soon as K_j has landed and its S
-    // buffer has been read, whatever the P V chain is waiting for.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16_f32(128, TBN);
       bool ok = mbar_wait(bar_q, 0, status, DEV_TIMEOUT_MMA);
       for (int j = 0; j < nt && ok; ++j) {
-        const int sk = j % KST, sbuf = j % NSB;
+        const int sk = j % KST, s = j & 1;
         ok = mbar_wait(bar_kf + 8 * sk, (uint32_t)(j / KST) & 1, status, DEV_TIMEOUT_MMA);
-        // S buffer sbuf held S_{j-3}, which the softmax warps have read once bar_sf completes
-        if (ok && j >= NSB)
-          ok = mbar_wait(bar_sf + 8 * sbuf, (uint32_t)((j - NSB) / NSB) & 1, status, DEV_TIMEOUT_MMA);
+        // buffer s holds P_{j-2} until P_{j-2} V_{j-2} is done (P_j V_j cannot be done yet, so
+        // the parity test is unambiguous)
+        if (ok && j >= 2)
+          ok = mbar_wait(bar_pf + 8 * s, (uint32_t)((j - 2) >> 1) & 1, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_f16_ss(tmem + S_COL + sbuf * TBN,
-                        sdesc_k_sw128(sb + OFF_Q + (kk >> 2) * Q_BLOCK + (kk & 3) * 32),
-                        sdesc_k_sw128(sb + OFF_K + sk * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32),
-                        idesc_s, kk != 0);
-        tc_commit(bar_s + 8 * sbuf);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_k_sw128(sb + OFF_K + sk * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32);
+          tc_mma_f16_ts(tmem + S_COL + s * TBN, tmem + Q_COL + kk * 8, bd, idesc_s, kk != 0);
+        }
+        tc_commit(bar_s + 8 * s);
         tc_commit(bar_ke + 8 * sk);
       }
       // tensor memory is freed only after every MMA issued here has completed
@@ -245,17 +227,17 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       constexpr uint32_t idesc_o = idesc_f16_f32(128, D, 0, 1);
       bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
-        const int sv = j % VST, pb = j % NPB;
-        ok = mbar_wait(bar_p + 8 * pb, (uint32_t)(j / NPB) & 1, status, DEV_TIMEOUT_MMA) &&
+        const int sv = j % VST, s = j & 1;
+        ok = mbar_wait(bar_p + 8 * s, (uint32_t)(j >> 1) & 1, status, DEV_TIMEOUT_MMA) &&
              mbar_wait(bar_vf + 8 * sv, (uint32_t)(j / VST) & 1, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk) {
           const uint64_t bd = sdesc_mn_sw128(sb + OFF_V + sv * KV_BYTES + kk * 16 * 128, KV_BLOCK, 1024);
-          tc_mma_f16_ts(tmem, tmem + P_COL + pb * 32 + kk * 8, bd, idesc_o, (j | kk) != 0);
+          tc_mma_f16_ts(tmem, tmem + S_COL + s * TBN + kk * 8, bd, idesc_o, (j | kk) != 0);
         }
-        tc_commit(bar_pf + 8 * pb);
+        tc_commit(bar_pf + 8 * s);
         tc_commit(bar_ve + 8 * sv);
       }
       // the epilogue waits for the last P V; tensor memory is freed only after every MMA
@@ -273,30 +255,58 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const float sl2 = 0.0625f * 1.4426950408889634f;  // 1/sqrt(256) in base 2
     // the two warps of a lane quarter meet on named barrier 1 + quarter (64 threads)
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
-    float m_ref = -INFINITY, lsum = 0.f;
+    {
+      // Q into tensor memory: row r, column Q_COL + c holds dims 2c, 2c+1 (the A-operand layout
+      // of kind::f16); this thread writes its row's dims 128 half .. 128 half + 127
+      const bool valid = pos < L;
+      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + half * 128;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 d = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 2 * c0) + i)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * i] = d.x;
+          qv[4 * i + 1] = d.y;
+          qv[4 * i + 2] = d.z;
+          qv[4 * i + 3] = d.w;
+        }
+        tmem_st_32x32b_x32(tl + Q_COL + half * 64 + c0, qv);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_q);
+    }
+    // keys of tiles before this one are all at or before the CTA's first position: no mask
+    const int p_first = p0;
+    float m_ref = -INFINITY;   // reference max of the raw scores (P = 2^((s - m_ref) sl2))
+    float lsum = 0.f;
     // Both threads of a row pass the same named barriers every iteration, whatever happens: a
     // failed (timed-out) wait only turns the rest of the work off (ok is warp-uniform).
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int sbuf = j % NSB, pb = j % NPB;
-      ok = ok && mbar_wait(bar_s + 8 * sbuf, (uint32_t)(j / NSB) & 1, status, DEV_TIMEOUT_EPILOGUE);
+      const int s = j & 1;
+      ok = ok && mbar_wait(bar_s + 8 * s, (uint32_t)(j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
       ok = __all_sync(0xffffffffu, ok);
       uint32_t sv[32];
       float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
-        tmem_ld_32x32b_x32(tl + S_COL + sbuf * TBN + half * 32, sv);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + half * 32, sv);
         tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sf + 8 * sbuf);   // S buffer free for S_{j+3}
         const int key0 = j * TBN + half * 32;
+        if (j * TBN + TBN - 1 <= p_first) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float v = __uint_as_float(sv[c]) * sl2;
-          v = (key0 + c <= pos) ? v : -INFINITY;
-          sv[c] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
+          for (int c = 0; c < 32; ++c) mt = fmaxf(mt, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float v = (key0 + c <= pos) ? __uint_as_float(sv[c]) : -INFINITY;
+            sv[c] = __float_as_uint(v);
+            mt = fmaxf(mt, v);
+          }
         }
       }
       // row max over both halves (the previous exchange's reads are fenced off by that
@@ -307,17 +317,17 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       pair_sync();
       if (!ok) continue;
       const float m_new = fmaxf(m_ref, mt);
-      const bool need = m_new > m_ref + kRescale;      // the same in both threads of a row
+      const bool need = (m_new - m_ref) * sl2 > kRescale;   // the same in both threads of a row
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O may only be rescaled once P_{j-1} V_{j-1} (and so every earlier P V) has landed in
-        // it; P_{j+1} is not written yet, so that phase of its barrier is unambiguous
+        // O may only be rescaled once P_{j-1} V_{j-1} has landed in it (P_{j+1} V_{j+1} cannot
+        // be done yet, so the parity test is unambiguous)
         const int jp = j - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_pf + 8 * (jp % NPB), (uint32_t)(jp / NPB) & 1,
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pf + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1,
                                                status, DEV_TIMEOUT_EPILOGUE));
         if (!ok) continue;
         tc_fence_after();
         // rescale this warp's half (128 columns) of its O rows
-        const float f = need ? exp2f(m_ref - m_new) : 1.f;
+        const float f = need ? exp2f((m_ref - m_new) * sl2) : 1.f;
 #pragma unroll 1
         for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
           uint32_t ov[32];
@@ -331,29 +341,23 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
         lsum *= f;
       }
       if (need) m_ref = m_new;
+      // P = 2^(s sl2 - m_ref sl2): one FFMA and one exp2 per score
+      const float moff = -m_ref * sl2;
       uint32_t pk[16];
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float e0 = exp2f(__uint_as_float(sv[2 * c]) - m_ref);
-        const float e1 = exp2f(__uint_as_float(sv[2 * c + 1]) - m_ref);
+        const float e0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sl2, moff));
+        const float e1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, moff));
         rs += e0 + e1;
         pk[c] = pack_half2(e0, e1);
       }
       lsum += rs;  // this half's share of the row sum
-      // P buffer pb held P_{j-2}; P_j is not written yet, so that phase is unambiguous
-      if (j >= NPB) {
-        const int jp = j - NPB;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_pf + 8 * pb, (uint32_t)(jp / NPB) & 1, status,
-                                               DEV_TIMEOUT_EPILOGUE));
-        if (!ok) continue;
-        tc_fence_after();
-      }
-      tmem_st_32x32b_x16(tl + P_COL + pb * 32 + half * 16, pk);
+      tmem_st_32x32b_x16(tl + S_COL + s * TBN + half * 16, pk);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p + 8 * pb);
+      if (lane == 0) mbar_arrive(bar_p + 8 * s);
     }
     // epilogue: wait for the last P V, then O / l * sigmoid(gate), each thread of a row taking
     // half of its columns
@@ -423,26 +427,19 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
                                          attn::FLASH_SMEM));
     attr = true;
   }
-  // TMA: row strides a multiple of 16 bytes, bases 16-byte aligned
+  // Q rows are read with 16-byte loads; K and V by TMA (row strides a multiple of 16 bytes)
   if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (ldq & 7) != 0 ||
       (reinterpret_cast<uintptr_t>(k) & 15) != 0 || (ldk & 7) != 0 ||
       (reinterpret_cast<uintptr_t>(v) & 15) != 0 || (ldv & 7) != 0)
     return CLEF_E_ALIGN;
   const uint64_t M = (uint64_t)(B * L);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mk, mv;
   {
-    // Q: [B][L][16 heads][256], a box of 4 heads x 32 positions; rows past the request's end
-    // read zero
-    const uint64_t dq[4] = {256, 16, (uint64_t)L, (uint64_t)B};
-    const uint64_t sq[3] = {512, (uint64_t)ldq * 2, (uint64_t)L * ldq * 2};
-    const uint32_t bq[4] = {64, 4, attn::POS, 1};
     const uint64_t dims[3] = {256, 4, M};
     const uint32_t box[3] = {64, 1, attn::TBN};
     const uint64_t stk[2] = {512, (uint64_t)ldk * 2};
     const uint64_t stv[2] = {512, (uint64_t)ldv * 2};
-    if (tma_encode(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, q, dq, sq, bq,
-                   CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        tma_encode(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, stk, box,
+    if (tma_encode(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, stk, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
         tma_encode(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v, dims, stv, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
@@ -452,7 +449,7 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
   TraceScope ts(stream, "flash_attn", 4.0 * attn::D * attn::HQ * (double)B * L * (L + 1) / 2.0,
                 (double)B * L * (16 + 4 + 4 + 16 + 16) * attn::D * 2.0);
   attn::flash_tc_kernel<<<grid, attn::FLASH_THREADS, attn::FLASH_SMEM, stream>>>(
-      mq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
+      q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
