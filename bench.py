@@ -30,6 +30,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s, 32-layer hybrid (L=512, L=16384); % of HBM/tensor roofline"
+# DRAM bytes (read + written) per LUT-6 GEMM launch, averaged over the 128 launches of one
+# 16,384-position prefill: ncu dram__bytes_read.sum + dram__bytes_write.sum of each of the eight
+# launch shapes, captured in their decoder layers at 16,384 positions; no capture for the other
+# workloads.
+GEMM_DRAM_BYTES_PER_LAUNCH = {"l16384": 1077.6e6}
+
 WORKLOADS = {
     "l16384": dict(B=1, L=16384, desc="32-layer hybrid prefill, 1 request x 16384 positions"),
     "l512": dict(B=1, L=512, desc="32-layer hybrid prefill, 1 request x 512 positions"),
@@ -260,7 +266,8 @@ def run_clef(args, wl):
         achieved = per_launch_flops / (avg_ms / 1000.0) / 1e12
         peak = pk["tc_sust"]
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": None, "kernel": "lut6_gemm",
+                    "frac": achieved / peak,
+                    "traffic": GEMM_DRAM_BYTES_PER_LAUNCH.get(args.workload), "kernel": "lut6_gemm",
                     "peak_kind": f"bf16 dense sustained ({pk['source']}), fp16 same nominal rate",
                     "algorithmic_flops_per_launch": per_launch_flops, "avg_launch_ms": avg_ms}
     cpu_v, _ = cpu_oracle_sample(0, ids_np[0], 64)
