@@ -103,6 +103,27 @@ def dist_env():
     return rank, world, local
 
 
+def request_seed(rank):
+    """Seed of the synthetic token ids of a rank's requests: every replica prefills its own."""
+    return 1000 + rank
+
+
+def slowest_rank_ms(ms, world, device=None):
+    """The timed region's length on the slowest rank (max over ranks; the local value at N = 1)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(B, L, steps, world, slowest_ms):
+    """Whole-job throughput: the tokens all ranks prefilled over the slowest rank's time."""
+    return B * L * steps * world / (slowest_ms / 1000.0)
+
+
 def cpu_oracle_sample(seed, ids_row, n_tokens):
     """Oracle seconds for one GDN layer and one attention layer on the first n_tokens of a request,
     extrapolated to the 32-layer model (24 GDN + 8 attention layers): tokens/s."""
@@ -174,7 +195,7 @@ def run_clef(args, wl):
 
     B, L = wl["B"], wl["L"]
     model = synth_model(0, 32, device=dev)
-    ids_np = synth.token_ids(1000 + rank, B, L)      # each rank: its own requests
+    ids_np = synth.token_ids(request_seed(rank), B, L)   # each rank: its own requests
     ids = torch.from_numpy(ids_np).to(dev)
     out = torch.empty((B, L, 4096), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -211,14 +232,9 @@ def run_clef(args, wl):
     clk = clocks.stop()
     clef.sync_status()
     step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(ev[0].elapsed_time(ev[-1]), world, dev)
     tokens = B * L * args.steps * world
-    value = tokens / (total_ms / 1000.0)
+    value = job_tokens_per_s(B, L, args.steps, world, total_ms)
     trace = {}
     if rc == 0:
         for i in range(n.value):
@@ -243,13 +259,8 @@ def run_clef(args, wl):
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens / (e2e_ms / 1000.0)
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_tokens_per_s(B, L, args.steps, world, e2e_ms)
 
     if rank != 0:
         if world > 1:
