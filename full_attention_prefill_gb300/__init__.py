@@ -65,6 +65,18 @@ class Model(ctypes.Structure):
     ]
 
 
+class State(ctypes.Structure):
+    """clef_state: the carried state of a chunked prefill (device buffers, see clef.h)."""
+    _fields_ = [
+        ("conv", ctypes.c_void_p),
+        ("rec", ctypes.c_void_p),
+        ("kcache", ctypes.c_void_p),
+        ("vcache", ctypes.c_void_p),
+        ("ctx", ctypes.c_int64),
+        ("pos", ctypes.c_int64),
+    ]
+
+
 _lib = None
 
 _SIGS = {
@@ -94,6 +106,10 @@ _SIGS = {
     "clef_prefill_forward": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_size_t, ctypes.c_void_p]),
+    "clef_prefill_chunk_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "clef_prefill_forward_chunk": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.POINTER(State), ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "clef_decoder_layer": (ctypes.c_int, [ctypes.POINTER(Layer), ctypes.c_void_p, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t,
                                           ctypes.c_void_p]),

@@ -11,6 +11,8 @@
 //   flash_tc_kernel  one CTA = 32 positions x the 4 query heads of one kv head (128 rows), so
 //                 each K/V tile is read once for the group; tcgen05 MMAs with S and O in tensor
 //                 memory; online softmax over 64-key tiles; epilogue o * sigmoid(gate).
+#include <algorithm>
+
 #include "attn.cuh"
 #include "common.cuh"
 
@@ -25,10 +27,14 @@ constexpr int POS = BM / 4;        // positions per CTA
 __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qin, int64_t ldqi,
                                                    __half* __restrict__ qout, int64_t ldqo,
                                                    const __half* __restrict__ kin, int64_t ldki,
-                                                   __half* __restrict__ kout, int64_t ldko, int L) {
+                                                   __half* __restrict__ kout, int64_t ldko, int L,
+                                                   int pos0, int64_t kctx) {
   __shared__ float cs[32], sn[32];
   const int64_t tok = blockIdx.x;
-  const int pos = (int)(tok % L);
+  const int64_t t = tok % L;
+  const int pos = pos0 + (int)t;
+  // k goes to row (request * kctx + pos) of kout (kctx = L, pos0 = 0: the token's own row)
+  const int64_t krow = (tok / L) * kctx + pos;
   const int tid = threadIdx.x;
   if (tid < 32) {
     // angle = pos * theta^(-j/32), reduced and evaluated in fp64 (ln 1e7 = 16.118...)
@@ -50,7 +56,7 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
       dst = qout + tok * ldqo + head * D;
     } else {
       src = kin + tok * ldki + (head - HQ) * D;
-      dst = kout + tok * ldko + (head - HQ) * D;
+      dst = kout + krow * ldko + (head - HQ) * D;
     }
     const float x1 = __half2float(src[j]), x2 = __half2float(src[j + 32]);
     dst[j] = __float2half_rn(x1 * cs[j] - x2 * sn[j]);
@@ -67,7 +73,7 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
   if (copy_k) {
     for (int i = tid; i < HKV * (D - 64) / 8; i += blockDim.x) {
       const int head = i / ((D - 64) / 8), c8 = 64 + (i % ((D - 64) / 8)) * 8;
-      *reinterpret_cast<uint4*>(kout + tok * ldko + head * D + c8) =
+      *reinterpret_cast<uint4*>(kout + krow * ldko + head * D + c8) =
           *reinterpret_cast<const uint4*>(kin + tok * ldki + head * D + c8);
     }
   }
@@ -113,7 +119,7 @@ constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 unit
 __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const __half* __restrict__ q, int64_t ldq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __half* __restrict__ gate, int64_t ldg,
-    __half* __restrict__ out, int64_t ldo, int L, unsigned* status) {
+    __half* __restrict__ out, int64_t ldo, int L, int pos0, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -123,9 +129,9 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   const int p0 = pblk * POS;
   const int g = blockIdx.y % HKV;
   const int b = blockIdx.y / HKV;
-  const int tb = b * L;
-  const int last_pos = min(p0 + POS, L) - 1;
-  const int nt = last_pos / TBN + 1;
+  const int tb = b * L;                          // first query row of the request
+  const int last_pos = min(p0 + POS, L) - 1;     // query positions are pos0 + local position
+  const int nt = (pos0 + last_pos) / TBN + 1;
 
   const uint32_t bar_q = sb + OFF_BAR;              // Q written into tensor memory
   const uint32_t bar_kf = bar_q + 8;                // [KST] K tile landed
@@ -185,8 +191,8 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
           break;
         mbar_arrive_expect_tx(bf + 8 * st, KV_BYTES);
         for (int blk = 0; blk < 4; ++blk)
-          tma_load_3d(base + st * KV_BYTES + blk * KV_BLOCK, map, bf + 8 * st, blk * 64, g,
-                      tb + j * TBN);
+          tma_load_4d(base + st * KV_BYTES + blk * KV_BLOCK, map, bf + 8 * st, blk * 64, g,
+                      j * TBN, b);
         issued = j + 1;
       }
       // copies still in flight land before the CTA may exit (no later phase of these barriers
@@ -280,7 +286,8 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       if (lane == 0) mbar_arrive(bar_q);
     }
     // keys of tiles before this one are all at or before the CTA's first position: no mask
-    const int p_first = p0;
+    const int p_first = pos0 + p0;
+    const int qpos = pos0 + pos;                        // this row's position in the request
     float m_ref = -INFINITY;   // reference max of the raw scores (P = 2^((s - m_ref) sl2))
     float lsum = 0.f;
     // Both threads of a row pass the same named barriers every iteration, whatever happens: a
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float v = (key0 + c <= pos) ? __uint_as_float(sv[c]) : -INFINITY;
+            const float v = (key0 + c <= qpos) ? __uint_as_float(sv[c]) : -INFINITY;
             sv[c] = __float_as_uint(v);
             mt = fmaxf(mt, v);
           }
@@ -403,22 +410,39 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   }
 }
 
+// Rows of one request chunk into a cache: dst row (request * dctx + pos0 + t) <- src row
+// (request * L + t), `cols` fp16 per row (a multiple of 8), 16 bytes per thread.
+__global__ void kv_store_kernel(const __half* __restrict__ src, int64_t lds, __half* __restrict__ dst,
+                                int64_t ldd, int64_t M, int L, int pos0, int64_t dctx, int cols) {
+  const int per_row = cols / 8;
+  const int64_t n = M * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = i / per_row;
+    const int c8 = (int)(i % per_row) * 8;
+    const int64_t drow = (tok / L) * dctx + pos0 + tok % L;
+    *reinterpret_cast<uint4*>(dst + drow * ldd + c8) =
+        *reinterpret_cast<const uint4*>(src + tok * lds + c8);
+  }
+}
+
 }  // namespace attn
 
 clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t ldqo,
                         const __half* kin, int64_t ldki, __half* kout, int64_t ldko, int64_t M,
-                        int64_t L, cudaStream_t stream) {
+                        int64_t L, int64_t pos0, int64_t kctx, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
   attn::rope_kernel<<<(unsigned)M, 128, 0, stream>>>(qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
-                                                     (int)L);
+                                                     (int)L, (int)pos0, kctx);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }
 
 clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t ldk,
                          const __half* v, int64_t ldv, const __half* gate, int64_t ldg, __half* out,
-                         int64_t ldo, int64_t B, int64_t L, cudaStream_t stream) {
+                         int64_t ldo, int64_t B, int64_t L, int64_t pos0, int64_t kv_req,
+                         cudaStream_t stream) {
   if (B == 0 || L == 0) return CLEF_OK;
   static bool attr = false;
   if (!attr) {
@@ -432,24 +456,37 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
       (reinterpret_cast<uintptr_t>(k) & 15) != 0 || (ldk & 7) != 0 ||
       (reinterpret_cast<uintptr_t>(v) & 15) != 0 || (ldv & 7) != 0)
     return CLEF_E_ALIGN;
-  const uint64_t M = (uint64_t)(B * L);
   CUtensorMap mk, mv;
   {
-    const uint64_t dims[3] = {256, 4, M};
-    const uint32_t box[3] = {64, 1, attn::TBN};
-    const uint64_t stk[2] = {512, (uint64_t)ldk * 2};
-    const uint64_t stv[2] = {512, (uint64_t)ldv * 2};
-    if (tma_encode(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k, dims, stk, box,
+    // keys and values [B][kv_req rows][4 heads][256]; only positions below pos0 + L are in the
+    // map, so a key tile's rows past them read zero
+    const uint64_t dims[4] = {256, 4, (uint64_t)(pos0 + L), (uint64_t)B};
+    const uint32_t box[4] = {64, 1, attn::TBN, 1};
+    const uint64_t stk[3] = {512, (uint64_t)ldk * 2, (uint64_t)kv_req * ldk * 2};
+    const uint64_t stv[3] = {512, (uint64_t)ldv * 2, (uint64_t)kv_req * ldv * 2};
+    if (tma_encode(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, k, dims, stk, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
-        tma_encode(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, v, dims, stv, box,
+        tma_encode(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, v, dims, stv, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
       return CLEF_E_CUDA;
   }
   dim3 grid((unsigned)((L + attn::POS - 1) / attn::POS), (unsigned)(B * attn::HKV));
-  TraceScope ts(stream, "flash_attn", 4.0 * attn::D * attn::HQ * (double)B * L * (L + 1) / 2.0,
-                (double)B * L * (16 + 4 + 4 + 16 + 16) * attn::D * 2.0);
+  TraceScope ts(stream, "flash_attn",
+                4.0 * attn::D * attn::HQ * (double)B * ((double)L * pos0 + (double)L * (L + 1) / 2.0),
+                (double)B * L * (16 + 16 + 16) * attn::D * 2.0 + (double)B * (pos0 + L) * 8 * attn::D * 2.0);
   attn::flash_tc_kernel<<<grid, attn::FLASH_THREADS, attn::FLASH_SMEM, stream>>>(
-      q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, status_word_ptr());
+      q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, (int)pos0, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status kv_store_launch(const __half* src, int64_t lds, __half* dst, int64_t ldd, int64_t M,
+                            int64_t L, int64_t pos0, int64_t dctx, int cols, cudaStream_t stream) {
+  if (M == 0) return CLEF_OK;
+  TraceScope ts(stream, "kv_store", 0.0, (double)M * cols * 4.0);
+  const int64_t n = M * (cols / 8);
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 4096);
+  attn::kv_store_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, M, (int)L, (int)pos0, dctx, cols);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

@@ -75,8 +75,19 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
     if (_s != CLEF_OK) return _s;      \
   } while (0)
 
+// Carried state of one layer for a chunk of positions pos0 .. pos0 + L - 1 (NULL pointers and
+// pos0 = 0: a whole prefill from an empty state).
+struct LayerState {
+  __half* conv = nullptr;   // GDN: [B][3][8192]
+  float* rec = nullptr;     // GDN: [B][32][128][128]
+  __half* kc = nullptr;     // attention: [B][ctx][4][256]
+  __half* vc = nullptr;
+  int64_t ctx = 0;
+  int64_t pos0 = 0;
+};
+
 static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, int64_t L,
-                             cudaStream_t s) {
+                             cudaStream_t s, const LayerState& st = LayerState()) {
   const int64_t M = B * L;
   const __half* attn_norm = reinterpret_cast<const __half*>(ly.attn_norm);
   CLEF_TRY(rmsnorm_launch(w.x, attn_norm, w.xn, M, s));
@@ -88,9 +99,11 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
                             reinterpret_cast<const __half*>(ly.A_log),
                             reinterpret_cast<const __half*>(ly.dt_bias), w.g, w.beta, w.abpart, M,
                             s));
-    CLEF_TRY(gdn_prep_launch(w.proj, GDN_PROJ, reinterpret_cast<const __half*>(ly.conv_w), w.q,
-                             w.k, w.v, M, L, s));
-    CLEF_TRY(gdn_scan_launch(w.q, w.k, w.v, w.g, nullptr, w.beta, nullptr, nullptr,
+    CLEF_TRY(gdn_prep_launch(w.proj, GDN_PROJ, reinterpret_cast<const __half*>(ly.conv_w),
+                             st.conv, w.q, w.k, w.v, M, L, s));
+    if (st.conv) CLEF_TRY(conv_state_launch(w.proj, GDN_PROJ, st.conv, B, L, s));
+    // the recurrent state enters from and returns to st.rec (each CTA reads its slice first)
+    CLEF_TRY(gdn_scan_launch(w.q, w.k, w.v, w.g, nullptr, w.beta, st.rec, st.rec,
                              w.proj + 8192, GDN_PROJ, reinterpret_cast<const __half*>(ly.o_norm),
                              w.mix, H, B, L, w.scan, s));
   } else {
@@ -100,8 +113,20 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
     __half* gp = w.proj + 4096;
     __half* kp = w.proj + 8192;
     __half* vp = w.proj + 9216;
-    CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, kp, ATT_PROJ, M, L, s));
-    CLEF_TRY(flash_launch(qp, ATT_PROJ, kp, ATT_PROJ, vp, ATT_PROJ, gp, ATT_PROJ, w.mix, H, B, L, s));
+    if (st.kc) {
+      // rotated keys and the values go into the caches at positions pos0 ..; attention reads
+      // positions 0 .. pos0 + L - 1 from there
+      constexpr int64_t KV = 4 * 256;
+      CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, st.kc, KV, M, L, st.pos0,
+                           st.ctx, s));
+      CLEF_TRY(kv_store_launch(vp, ATT_PROJ, st.vc, KV, M, L, st.pos0, st.ctx, (int)KV, s));
+      CLEF_TRY(flash_launch(qp, ATT_PROJ, st.kc, KV, st.vc, KV, gp, ATT_PROJ, w.mix, H, B, L,
+                            st.pos0, st.ctx, s));
+    } else {
+      CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, kp, ATT_PROJ, M, L, 0, L, s));
+      CLEF_TRY(flash_launch(qp, ATT_PROJ, kp, ATT_PROJ, vp, ATT_PROJ, gp, ATT_PROJ, w.mix, H, B, L,
+                            0, L, s));
+    }
   }
   CLEF_TRY(lut6_gemm_launch(w.mix, ly.out_proj.packed,
                             reinterpret_cast<const __half*>(ly.out_proj.lut), w.x, H, M, H, H,
@@ -241,10 +266,10 @@ clef_status clef_gqa_attn_prefill(const uint16_t* q, const uint16_t* k, const ui
   __half* kr = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + al256((size_t)M * 16 * 256 * 2));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CLEF_TRY(rope_launch(reinterpret_cast<const __half*>(q), ldq, qr, 16 * 256,
-                       reinterpret_cast<const __half*>(k), ldkv, kr, 4 * 256, M, L, s));
+                       reinterpret_cast<const __half*>(k), ldkv, kr, 4 * 256, M, L, 0, L, s));
   return flash_launch(qr, 16 * 256, kr, 4 * 256, reinterpret_cast<const __half*>(v), ldkv,
                       reinterpret_cast<const __half*>(gate), ldg, reinterpret_cast<__half*>(o),
-                      16 * 256, B, L, s);
+                      16 * 256, B, L, 0, L, s);
 }
 
 size_t clef_prefill_workspace_size(int64_t B, int64_t L) {
@@ -301,6 +326,79 @@ clef_status clef_prefill_forward(const clef_model* model, const int32_t* ids, in
   for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(run_layer(model->layers[i], w, B, L, s));
   return rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
                         reinterpret_cast<__half*>(hidden), M, s);
+}
+
+size_t clef_prefill_chunk_workspace_size(int64_t B, int64_t L) {
+  return clef_prefill_workspace_size(B, L);
+}
+
+clef_status clef_prefill_forward_chunk(const clef_model* model, const int32_t* ids, int64_t B,
+                                       int64_t L, clef_state* state, uint16_t* hidden,
+                                       void* workspace, size_t workspace_bytes,
+                                       clef_stream stream) {
+  CLEF_TRY(check_bl(B, L));
+  if (!model || !model->layers || model->n_layers < 1 || model->n_layers > 64 ||
+      model->vocab < 1 || !state) {
+    set_error("clef_prefill_forward_chunk: bad model (layers, n_layers in 1..64, vocab >= 1) or "
+              "NULL state");
+    return CLEF_E_INVALID;
+  }
+  if (bad_ptr(ids) || bad_ptr(hidden) || bad_ptr(workspace) || bad_ptr(model->embed) ||
+      bad_ptr(model->final_norm)) {
+    set_error("clef_prefill_forward_chunk: a pointer is NULL or not 16-byte aligned");
+    return CLEF_E_INVALID;
+  }
+  int n_gdn = 0, n_attn = 0;
+  for (int i = 0; i < model->n_layers; ++i) {
+    CLEF_TRY(check_layer(&model->layers[i], i));
+    (model->layers[i].kind == CLEF_LAYER_GDN ? n_gdn : n_attn) += 1;
+  }
+  if (state->ctx < 1 || state->ctx > CLEF_MAX_LEN || state->pos < 0) {
+    set_error("clef_prefill_forward_chunk: state ctx must be in 1..%d and pos >= 0", CLEF_MAX_LEN);
+    return CLEF_E_INVALID;
+  }
+  if (state->pos + L > state->ctx) {
+    set_error("clef_prefill_forward_chunk: pos %lld + L %lld is above the state's %lld positions "
+              "(refused, never cut)", (long long)state->pos, (long long)L, (long long)state->ctx);
+    return CLEF_E_TOO_LONG;
+  }
+  if ((n_gdn && (bad_ptr(state->conv) || bad_ptr(state->rec))) ||
+      (n_attn && (bad_ptr(state->kcache) || bad_ptr(state->vcache)))) {
+    set_error("clef_prefill_forward_chunk: a state buffer is NULL or not 16-byte aligned");
+    return CLEF_E_INVALID;
+  }
+  if (workspace_bytes < fwd_layout(B, L, nullptr, nullptr)) {
+    set_error("clef_prefill_forward_chunk: workspace of %zu bytes, need %zu", workspace_bytes,
+              fwd_layout(B, L, nullptr, nullptr));
+    return CLEF_E_WORKSPACE;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FwdWs w;
+  fwd_layout(B, L, workspace, &w);
+  const int64_t M = B * L;
+  CLEF_TRY(embed_launch(ids, reinterpret_cast<const __half*>(model->embed), model->vocab, w.x, M, s));
+  int gi = 0, ai = 0;
+  for (int i = 0; i < model->n_layers; ++i) {
+    LayerState ls;
+    ls.ctx = state->ctx;
+    ls.pos0 = state->pos;
+    if (model->layers[i].kind == CLEF_LAYER_GDN) {
+      ls.conv = reinterpret_cast<__half*>(state->conv) + (size_t)gi * B * 3 * 8192;
+      ls.rec = state->rec + (size_t)gi * B * 32 * 128 * 128;
+      ++gi;
+    } else {
+      const size_t per_layer = (size_t)B * state->ctx * 4 * 256;
+      ls.kc = reinterpret_cast<__half*>(state->kcache) + (size_t)ai * per_layer;
+      ls.vc = reinterpret_cast<__half*>(state->vcache) + (size_t)ai * per_layer;
+      ++ai;
+    }
+    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+  }
+  CLEF_TRY(rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
+                          reinterpret_cast<__half*>(hidden), M, s));
+  state->pos += L;
+  return CLEF_OK;
 }
 
 }  // extern "C"

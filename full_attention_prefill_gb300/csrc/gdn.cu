@@ -48,7 +48,8 @@ constexpr int PREP_CH = 512;
 constexpr int PREP_SMEM = (PREP_T + 3) * PREP_CH * 2;
 __global__ void __launch_bounds__(256) gdn_prep_kernel(
     const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
-    __half* __restrict__ q, __half* __restrict__ k, __half* __restrict__ v, int64_t M, int L) {
+    const __half* __restrict__ conv_in, __half* __restrict__ q, __half* __restrict__ k,
+    __half* __restrict__ v, int64_t M, int L) {
   extern __shared__ __align__(16) uint8_t prep_smem[];
   __half* tile = reinterpret_cast<__half*>(prep_smem);   // [PREP_T + 3][PREP_CH], row i = token tok0 - 3 + i
   const int tid = threadIdx.x;
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
   const int64_t ldd = ch0 < 4096 ? 2048 : 4096;
   const int j0 = th * (PREP_T / 2);         // first token of this thread, within the tile
   int pos = (int)((tok0 + j0) % L);         // its position in its request
+  int64_t req = (tok0 + j0) / L;            // and the request
   cp_async_wait<0>();
   __syncthreads();
   // the 4 channels of tile row r as floats
@@ -106,12 +108,26 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
         for (int c = 0; c < 4; ++c)
           y[c] = silu_f(w[c][0] * h0[c] + w[c][1] * h1[c] + w[c][2] * h2[c] + w[c][3] * x3[c]);
       } else {
-        // taps reaching before the request's start read zero
-        const float m0 = pos >= 3 ? 1.f : 0.f, m1 = pos >= 2 ? 1.f : 0.f, m2 = pos >= 1 ? 1.f : 0.f;
+        // taps reaching before the request's start read the carried conv input (its last three
+        // rows, oldest first), or zero without one
+        float x0[4], x1[4], x2[4];
+        auto hist = [&](int r, float (&x)[4]) {   // carried row r = 0..2
+          if (conv_in) {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(conv_in + (req * 3 + r) * 8192 + ch0));
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            x[0] = a.x; x[1] = a.y; x[2] = bb.x; x[3] = bb.y;
+          } else {
+            x[0] = x[1] = x[2] = x[3] = 0.f;
+          }
+        };
+        // tap j reads position pos - 3 + j, i.e. carried row pos + j when that is negative
+        if (pos >= 3) { for (int c = 0; c < 4; ++c) x0[c] = h0[c]; } else hist(pos, x0);
+        if (pos >= 2) { for (int c = 0; c < 4; ++c) x1[c] = h1[c]; } else hist(pos + 1, x1);
+        if (pos >= 1) { for (int c = 0; c < 4; ++c) x2[c] = h2[c]; } else hist(pos + 2, x2);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          y[c] = silu_f(m0 * w[c][0] * h0[c] + m1 * w[c][1] * h1[c] + m2 * w[c][2] * h2[c] +
-                        w[c][3] * x3[c]);
+          y[c] = silu_f(w[c][0] * x0[c] + w[c][1] * x1[c] + w[c][2] * x2[c] + w[c][3] * x3[c]);
       }
       if (is_qk) {
         float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
@@ -129,7 +145,32 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
       h1[c] = h2[c];
       h2[c] = x3[c];
     }
-    pos = pos + 1 == L ? 0 : pos + 1;
+    if (++pos == L) {
+      pos = 0;
+      ++req;
+    }
+  }
+}
+
+// The conv input carried to the next chunk: for request b, the last three rows (oldest first)
+// of the q | k | v projection over the carried rows and this chunk's L rows.  In place: each
+// thread reads the old rows it needs before writing.
+__global__ void conv_state_kernel(const __half* __restrict__ proj, int64_t ldp, __half* state,
+                                  int64_t B, int L) {
+  const int64_t n = B * (8192 / 8);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / (8192 / 8);
+    const int c8 = (int)(i % (8192 / 8)) * 8;
+    uint4 r[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int p = L - 3 + j;               // position of the new row j within the chunk
+      r[j] = p >= 0 ? *reinterpret_cast<const uint4*>(proj + (b * L + p) * ldp + c8)
+                    : *reinterpret_cast<const uint4*>(state + (b * 3 + (3 + p)) * 8192 + c8);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) *reinterpret_cast<uint4*>(state + (b * 3 + j) * 8192 + c8) = r[j];
   }
 }
 
@@ -509,8 +550,9 @@ static clef_status gdn_set_attrs() {
   return CLEF_OK;
 }
 
-clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
-                            __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream) {
+clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w,
+                            const __half* conv_in, __half* q, __half* k, __half* v, int64_t M,
+                            int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
   static bool attr = false;
@@ -520,7 +562,19 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
     attr = true;
   }
   dim3 grid(8192 / gdn::PREP_CH, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
-  gdn::gdn_prep_kernel<<<grid, 256, gdn::PREP_SMEM, stream>>>(proj, ldp, conv_w, q, k, v, M, (int)L);
+  gdn::gdn_prep_kernel<<<grid, 256, gdn::PREP_SMEM, stream>>>(proj, ldp, conv_w, conv_in, q, k, v,
+                                                               M, (int)L);
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status conv_state_launch(const __half* proj, int64_t ldp, __half* state, int64_t B,
+                              int64_t L, cudaStream_t stream) {
+  if (B == 0) return CLEF_OK;
+  TraceScope ts(stream, "conv_state", 0.0, (double)B * 3 * 8192 * 2 * 2);
+  const int64_t n = B * (8192 / 8);
+  gdn::conv_state_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
+      proj, ldp, state, B, (int)L);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

@@ -11,9 +11,17 @@ constexpr int HV = 32;         // value heads
 constexpr int HK = 16;         // key heads
 }  // namespace gdn
 
-// conv(4) + SiLU + q/k L2 norm, for M tokens of requests of L positions.
-clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w, __half* q,
-                            __half* k, __half* v, int64_t M, int64_t L, cudaStream_t stream);
+// conv(4) + SiLU + q/k L2 norm, for M tokens of request chunks of L positions.  Taps before a
+// chunk's first position read conv_in [B][3][8192] (the carried last three rows of the conv
+// input, oldest first), or zero when conv_in is NULL.
+clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_w,
+                            const __half* conv_in, __half* q, __half* k, __half* v, int64_t M,
+                            int64_t L, cudaStream_t stream);
+
+// state [B][3][8192] <- the last three rows of the conv input (carried rows, then the chunk's L
+// rows of proj q | k | v), in place.
+clef_status conv_state_launch(const __half* proj, int64_t ldp, __half* state, int64_t B,
+                              int64_t L, cudaStream_t stream);
 
 // with_norm: room for o before the output gate (decoder layer path, z != NULL)
 size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm);

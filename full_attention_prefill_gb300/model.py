@@ -14,8 +14,8 @@ import ctypes
 import numpy as np
 import torch
 
-from . import (HIDDEN, SWIGLU_BLOCK, Layer, Lut6, Model, _check, _ptr, _stream, _workspace, lib,
-               lut6_tile, prefill_workspace_size)
+from . import (HIDDEN, SWIGLU_BLOCK, Layer, Lut6, Model, State, _check, _ptr, _stream, _workspace,
+               lib, lut6_tile, prefill_workspace_size)
 
 GDN, ATTENTION = 0, 1
 
@@ -125,6 +125,45 @@ class DeviceModel:
         _check(lib().clef_prefill_forward(ctypes.byref(self.struct), _ptr(ids), B, L, _ptr(out), _ptr(ws),
                                           ws.numel(), _stream(stream)), "clef_prefill_forward")
         return out
+
+    def forward_chunk(self, ids, state, out=None, stream=None):
+        """ids [B, L] int32 (device): positions state.pos .. state.pos + L - 1 of the state's
+        requests -> their final-norm hidden [B, L, 4096] fp16; the state moves on by L."""
+        if not (ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous()):
+            raise ValueError("ids must be a contiguous int32 CUDA tensor")
+        B, L = ids.shape
+        if B != state.B:
+            raise ValueError(f"ids carry {B} requests, the state {state.B}")
+        if out is None:
+            out = torch.empty((B, L, HIDDEN), dtype=torch.float16, device=ids.device)
+        ws = self.workspace(B, L)
+        _check(lib().clef_prefill_forward_chunk(ctypes.byref(self.struct), _ptr(ids), B, L,
+                                                ctypes.byref(state.struct), _ptr(out), _ptr(ws), ws.numel(),
+                                                _stream(stream)), "clef_prefill_forward_chunk")
+        return out
+
+
+class PrefillState:
+    """The carried state of B requests for DeviceModel.forward_chunk: torch-allocated, zeroed
+    (an empty state), in the layouts of clef_state."""
+
+    def __init__(self, model, B, ctx, device="cuda"):
+        n_gdn = sum(1 for l in model.layers if l.kind == GDN)
+        n_attn = len(model.layers) - n_gdn
+        self.conv = torch.zeros((max(n_gdn, 1), B, 3, 8192), dtype=torch.float16, device=device)
+        self.rec = torch.zeros((max(n_gdn, 1), B, 32, 128, 128), dtype=torch.float32, device=device)
+        self.kcache = torch.zeros((max(n_attn, 1), B, ctx, 4, 256), dtype=torch.float16, device=device)
+        self.vcache = torch.zeros_like(self.kcache)
+        st = State()
+        st.conv, st.rec = _ptr(self.conv), _ptr(self.rec)
+        st.kcache, st.vcache = _ptr(self.kcache), _ptr(self.vcache)
+        st.ctx, st.pos = ctx, 0
+        self.struct = st
+        self.B = B
+
+    @property
+    def pos(self):
+        return self.struct.pos
 
 
 def synth_model(seed=0, n_layers=32, device="cuda", embed=None):

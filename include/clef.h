@@ -227,6 +227,46 @@ CLEF_API clef_status clef_prefill_forward(const clef_model* model, const int32_t
                                  uint16_t* hidden, void* workspace, size_t workspace_bytes,
                                  clef_stream stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Chunked prefill with carried state ("clef-flash - Core AI" README, section "Core AI shape": a
+ * request is prefilled as successive calls of 64 positions from zeroed states, each carrying the
+ * key and value caches of the attention layers and the conv and recurrent states of the Gated
+ * DeltaNet layers to the next; "clef-flash-LiteRT" card, section "Other forms measured": a chunk
+ * step of 128 positions carrying caches of 4,096 positions).  Any chunk length works here.  The
+ * state of B requests, all device buffers owned by the caller:
+ *   conv    fp16 [n_gdn][B][3][8192]      the last three rows of each GDN layer's conv input
+ *                                         (the q | k | v projection), oldest first
+ *   rec     fp32 [n_gdn][B][32][128][128] each GDN layer's state S (value rows x key columns)
+ *   kcache  fp16 [n_attn][B][ctx][4][256] each attention layer's keys after rotary
+ *   vcache  fp16 [n_attn][B][ctx][4][256] each attention layer's values
+ * n_gdn / n_attn count the model's layers of each kind in order.  Layouts differ from the pages'
+ * Core ML states ([.., 8192, 3] conv, fp16 rec, [.., 4, ctx, 256] caches): these are this
+ * library's own.  pos = positions already in the state, the same for every request; a state of
+ * zeros with pos = 0 is an empty one.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  uint16_t* conv;
+  float* rec;
+  uint16_t* kcache;
+  uint16_t* vcache;
+  int64_t ctx;   /* capacity of the caches in positions, 1..CLEF_MAX_LEN */
+  int64_t pos;   /* positions already in the state */
+} clef_state;
+
+/* Bytes of workspace clef_prefill_forward_chunk needs for B requests of chunks of L positions. */
+CLEF_API size_t clef_prefill_chunk_workspace_size(int64_t B, int64_t L);
+
+/* device: positions pos .. pos + L - 1 of B requests.  ids [B, L] int32 (device) -> hidden
+   [B, L, 4096] fp16 (final-norm hidden states of these positions), reading and updating the
+   state; on success state->pos += L (host side, before any device work completes).  Calls with
+   pos = 0, L1, L1 + L2, .. give the rows of one clef_prefill_forward of the whole request (up
+   to rounding).  pos + L > ctx: CLEF_E_TOO_LONG; L < 1 or B < 1: CLEF_E_INVALID.  Calls on one
+   state must not overlap on the device. */
+CLEF_API clef_status clef_prefill_forward_chunk(const clef_model* model, const int32_t* ids,
+                                                int64_t B, int64_t L, clef_state* state,
+                                                uint16_t* hidden, void* workspace,
+                                                size_t workspace_bytes, clef_stream stream);
+
 /* device: one decoder layer on the fp32 residual stream x [B, L, 4096], updated in place:
    x <- h + mlp(rmsnorm(h)),  h = x + mixer(rmsnorm(x)).  Same workspace as the forward. */
 CLEF_API clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64_t B, int64_t L,

@@ -65,3 +65,20 @@ def test_batch_32x512_requests_are_independent(model):
         assert e < SAME_TOL
     # different requests give different hidden states
     assert rel_rmse(batch[0], batch[1]) > 0.1
+
+
+def test_l512_as_64_position_calls(model):
+    """The pages' serving mode: a 512-position request as 8 calls of 64 carrying the state."""
+    from full_attention_prefill_gb300.model import PrefillState
+    ids = synth.token_ids(0, 1, 512)
+    whole = _run(model, ids)[0]
+    st = PrefillState(model, 1, 512)
+    rows = []
+    for c in range(8):
+        out = model.forward_chunk(torch.from_numpy(np.ascontiguousarray(ids[:, 64 * c:64 * c + 64])).cuda(), st)
+        rows.append(out.double().cpu().numpy()[0])
+    clef.sync_status()
+    got = np.concatenate(rows, axis=0)
+    e = rel_rmse(got, whole)
+    print(f"32-layer L=512 as 8 x 64 calls vs one call: rel-RMSE {e:.2e}")
+    assert e < SAME_TOL and min_row_cosine(got, whole) > 0.9999
