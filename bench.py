@@ -322,7 +322,8 @@ def run_micro(args):
 
     gemm: clef_lut6_gemm at M x N x K (fp16 out); attn: clef_gqa_attn_prefill at L (gated);
     gdn: clef_gdn_prefill at L; layer: clef_decoder_layer of layer --layer at L (the residual
-    copy-in is part of each iteration).  Prints one JSON line with the per-kernel times of the
+    copy-in is part of each iteration); chunk: one request of L positions as calls of --chunk
+    positions through clef_prefill_forward_chunk (zeroing the state is part of each iteration).  Prints one JSON line with the per-kernel times of the
     library's trace; not the headline metric.
     """
     import numpy as np
@@ -333,6 +334,7 @@ def run_micro(args):
 
     dev = torch.device("cuda", 0)
     pk = peaks()
+    extra_fn = None
     if args.micro == "gemm":
         M, N, K = args.m, args.n, args.k
         x = torch.from_numpy(synth.normal_f16(0, "micro.x", 0, (M, K))).to(dev)
@@ -350,6 +352,22 @@ def run_micro(args):
         g = torch.from_numpy(synth.normal_f16(0, "g", 0, (1, L, 16, 256))).to(dev)
         fn = lambda: clef.gqa_attn_prefill(q, k, v, g)  # noqa: E731
         flops, desc = 4.0 * 256 * 16 * L * (L + 1) / 2, f"gqa_attn L={L}"
+    elif args.micro == "chunk":
+        # one request of --L positions prefilled as calls of --chunk positions on a carried state
+        from full_attention_prefill_gb300.model import PrefillState, synth_model
+        L, C = args.L, args.chunk
+        model = synth_model(0, 32, device=dev)
+        ids = torch.from_numpy(synth.token_ids(1000, 1, L)).to(dev)
+        calls = [ids[:, p:p + C].contiguous() for p in range(0, L, C)]
+        st_box = []
+
+        def fn():
+            st = PrefillState(model, 1, L, dev)
+            st_box[:] = [st]
+            for c in calls:
+                model.forward_chunk(c, st)
+        flops, desc = 0.0, f"chunked prefill L={L} in calls of {C}"
+        extra_fn = lambda ms: {"tokens_per_s": L / (ms / 1000.0), "ms_per_call": ms / len(calls)}  # noqa: E731
     elif args.micro == "layer":
         # one decoder layer (GDN for --layer 0, attention for --layer 3) on an fp32 residual
         from full_attention_prefill_gb300.model import DeviceLayer, DeviceModel
@@ -399,14 +417,17 @@ def run_micro(args):
                                         "GB/s": round(e.bytes / (e.ms * 1e6), 1) if e.ms > 0 else None}
         if flops == 0.0:
             flops = sum(entries[i].flops for i in range(n.value)) / args.steps
-    print(json.dumps({"micro": desc, "ms": ms, "tflops": flops / ms / 1e9,
-                      "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"], "kernels": kernels}),
-          flush=True)
+    line = {"micro": desc, "ms": ms, "tflops": flops / ms / 1e9,
+            "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"], "kernels": kernels}
+    if extra_fn is not None:
+        line.update(extra_fn(ms))
+    print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer"], default=None)
+    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk"], default=None)
+    ap.add_argument("--chunk", type=int, default=64)
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--n", type=int, default=24576)
