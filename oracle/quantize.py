@@ -11,7 +11,9 @@ Readings where the card is silent (each is a plain choice the rest of the card a
     h = p (n - 1), lo = floor(h), f = h - lo.  For fp16 weights every step is exact in float64;
   * evenly spread: min + i * step, step = (max - min) / 31, i = 0..30, rounded after the
     division, the product and the sum; the 32nd value is max itself;
-  * the 64 starting values are sorted ascending; k-means keeps them ascending;
+  * the 64 starting values (quantiles first, then the spread values) are sorted ascending by a
+    stable sort, so equal values (-0 and +0 among them) keep that order; k-means keeps the
+    centroids ascending;
   * a round assigns each weight to its nearest centroid.  With ascending centroids that is the
     cell between the midpoints of neighbouring centroids, each midpoint fl(c_j + c_j+1) / 2;
     a weight exactly on a midpoint goes to the lower index, and a weight whose nearest value is
@@ -61,7 +63,7 @@ def spread(values: np.ndarray) -> np.ndarray:
 
 def initial_table(values: np.ndarray) -> np.ndarray:
     """64 starting centroids of one group (float64, ascending)."""
-    return np.sort(np.concatenate([quantiles(values), spread(values)]))
+    return np.sort(np.concatenate([quantiles(values), spread(values)]), kind="stable")
 
 
 def assign(values: np.ndarray, centroids: np.ndarray) -> np.ndarray:
