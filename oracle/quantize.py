@@ -12,8 +12,10 @@ Readings where the card is silent (each is a plain choice the rest of the card a
   * evenly spread: min + i * step, step = (max - min) / 31, i = 0..30, rounded after the
     division, the product and the sum; the 32nd value is max itself;
   * the 64 starting values (quantiles first, then the spread values) are sorted ascending by a
-    stable sort, so equal values (-0 and +0 among them) keep that order; k-means keeps the
-    centroids ascending;
+    stable sort, so equal values (-0 and +0 among them) keep that order.  After every round the
+    centroids are sorted again the same way: equal seeds share their members with the first of
+    them, which moves while the others stay, so order is not kept by itself.  Sorting changes
+    only the labels (the set of centroids, and so every later round, is the same);
   * a round assigns each weight to its nearest centroid.  With ascending centroids that is the
     cell between the midpoints of neighbouring centroids, each midpoint fl(c_j + c_j+1) / 2;
     a weight exactly on a midpoint goes to the lower index, and a weight whose nearest value is
@@ -77,7 +79,7 @@ def assign(values: np.ndarray, centroids: np.ndarray) -> np.ndarray:
 
 
 def kmeans_round(values: np.ndarray, centroids: np.ndarray) -> np.ndarray:
-    """One round: assign, then move each centroid with members to their mean."""
+    """One round: assign, move each centroid with members to their mean, sort (stable)."""
     v = np.asarray(values, dtype=np.float64).ravel()
     c = np.array(centroids, dtype=np.float64)
     a = assign(v, c)
@@ -88,7 +90,7 @@ def kmeans_round(values: np.ndarray, centroids: np.ndarray) -> np.ndarray:
         if count:
             total = int(fixed[members].sum())               # exact integer sum
             c[j] = (float(total) / float(count)) / FIX
-    return c
+    return np.sort(c, kind="stable")
 
 
 def quantize_group(values: np.ndarray, rounds: int = ROUNDS):

@@ -106,16 +106,16 @@ def test_round_means_are_the_correctly_rounded_rational_means():
     c0 = Q.initial_table(v)
     c1 = Q.kmeans_round(v, c0)
     a = _nearest_exact(v, c0)
+    expect = []
     for j in range(64):
         members = [Fraction(float(t)) for t in v[a == j]]
-        if members:
-            assert c1[j] == float(sum(members) / len(members))
-        else:
-            assert c1[j] == c0[j]
+        expect.append(float(sum(members) / len(members)) if members else c0[j])
+    assert np.array_equal(c1, np.sort(expect))
 
 
 def _kmeans_brute(values, rounds):
-    """The card's k-means in rationals: exact nearest, exact mean rounded once to float64."""
+    """The card's k-means in rationals: exact nearest, exact mean rounded once to float64, the
+    centroids kept in ascending order (stable)."""
     c = [float(t) for t in Q.initial_table(values)]
     vals = [Fraction(float(t)) for t in values]
     for _ in range(rounds):
@@ -124,6 +124,7 @@ def _kmeans_brute(values, rounds):
             members = [vals[i] for i in range(len(vals)) if a[i] == j]
             if members:
                 c[j] = float(sum(members) / len(members))
+        c = [c[j] for j in sorted(range(len(c)), key=lambda j: c[j])]   # Python's sort is stable
     table = np.array(c).astype(np.float16)
     return table, _nearest_exact(values, table.astype(np.float64))
 
@@ -136,6 +137,19 @@ def test_quantize_group_matches_rational_brute_force(seed):
     bt, bidx = _kmeans_brute(v, Q.ROUNDS)
     assert np.array_equal(table.view(np.uint16), bt.view(np.uint16))
     assert np.array_equal(idx, bidx)
+
+
+def test_repeated_seeds_match_rational_brute_force():
+    """Many equal quantile seeds (a few values repeated, zeros of both signs): the case where the
+    first of several equal centroids moves alone."""
+    rng = np.random.default_rng(21)
+    v = rng.choice(np.array([-0.0, 0.0, 2.0 ** -24, 3 * 2.0 ** -24, -2.0 ** -23, 0.5]), size=16 * 8)
+    v = np.concatenate([v, _fp16(rng, 16 * 4, 1e-6)])
+    table, idx = Q.quantize_group(v)
+    bt, bidx = _kmeans_brute(v, Q.ROUNDS)
+    assert np.array_equal(table.view(np.uint16), bt.view(np.uint16))
+    assert np.array_equal(idx, bidx)
+    assert np.all(np.diff(table.astype(np.float64)) >= 0)
 
 
 def test_constant_group():
