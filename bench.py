@@ -323,8 +323,9 @@ def run_micro(args):
     gemm: clef_lut6_gemm at M x N x K (fp16 out); attn: clef_gqa_attn_prefill at L (gated);
     gdn: clef_gdn_prefill at L; layer: clef_decoder_layer of layer --layer at L (the residual
     copy-in is part of each iteration); chunk: one request of L positions as calls of --chunk
-    positions through clef_prefill_forward_chunk (zeroing the state is part of each iteration).  Prints one JSON line with the per-kernel times of the
-    library's trace; not the headline metric.
+    positions through clef_prefill_forward_chunk (zeroing the state is part of each iteration);
+    quantize: clef_lut6_quantize of an N x K fp16 weight.  Prints one JSON line with the
+    per-kernel times of the library's trace; not the headline metric.
     """
     import numpy as np
     import torch
@@ -368,6 +369,15 @@ def run_micro(args):
                 model.forward_chunk(c, st)
         flops, desc = 0.0, f"chunked prefill L={L} in calls of {C}"
         extra_fn = lambda ms: {"tokens_per_s": L / (ms / 1000.0), "ms_per_call": ms / len(calls)}  # noqa: E731
+    elif args.micro == "quantize":
+        # LUT-6 quantisation of one fp16 weight [--n, --k] (default: the MLP down projection)
+        N, K = args.n, args.k
+        w = torch.from_numpy(synth.normal_f16(0, "micro.qw", 0, (N, K), std=0.02)).to(dev)
+        fn = lambda: clef.lut6_quantize(w)  # noqa: E731
+        flops, desc = 0.0, f"lut6_quantize N={N} K={K}"
+        extra_fn = lambda ms: {"weights_per_s": N * K / (ms / 1000.0),  # noqa: E731
+                               "groups_per_s": N / 16 / (ms / 1000.0),
+                               "weight_GB_per_s": 2.0 * N * K / (ms * 1e6)}
     elif args.micro == "layer":
         # one decoder layer (GDN for --layer 0, attention for --layer 3) on an fp32 residual
         from full_attention_prefill_gb300.model import DeviceLayer, DeviceModel
@@ -417,8 +427,9 @@ def run_micro(args):
                                         "GB/s": round(e.bytes / (e.ms * 1e6), 1) if e.ms > 0 else None}
         if flops == 0.0:
             flops = sum(entries[i].flops for i in range(n.value)) / args.steps
-    line = {"micro": desc, "ms": ms, "tflops": flops / ms / 1e9,
-            "frac_of_sustained": flops / ms / 1e9 / pk["tc_sust"], "kernels": kernels}
+    line = {"micro": desc, "ms": ms, "kernels": kernels}
+    if flops > 0:
+        line.update(tflops=flops / ms / 1e9, frac_of_sustained=flops / ms / 1e9 / pk["tc_sust"])
     if extra_fn is not None:
         line.update(extra_fn(ms))
     print(json.dumps(line), flush=True)
@@ -426,7 +437,7 @@ def run_micro(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk"], default=None)
+    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk", "quantize"], default=None)
     ap.add_argument("--chunk", type=int, default=64)
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--m", type=int, default=4096)

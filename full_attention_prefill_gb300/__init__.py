@@ -90,6 +90,8 @@ _SIGS = {
                                          ctypes.c_void_p, ctypes.c_void_p]),
     "clef_lut6_tile": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                       ctypes.c_void_p]),
+    "clef_lut6_quantize": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]),
     "clef_lut6_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p]),
@@ -196,6 +198,21 @@ def lut6_tile(packed, k, stream=None):
     tiled = torch.empty_like(packed)
     _check(lib().clef_lut6_tile(_ptr(packed), n, k, _ptr(tiled), _stream(stream)), "clef_lut6_tile")
     return tiled
+
+
+def lut6_quantize(w, stream=None):
+    """Device: LUT-6 quantisation of an fp16 weight w [n, k] -> (packed [n, k*3/4] uint8 in the
+    canonical row-major layout, lut [n/16, 64] fp16)."""
+    _need_cuda(w)
+    if w.dtype != torch.float16 or w.dim() != 2:
+        raise ValueError("w must be a 2-D fp16 tensor")
+    w = w.contiguous()
+    n, k = w.shape
+    packed = torch.empty((n, k * 3 // 4), dtype=torch.uint8, device=w.device)
+    lut = torch.empty((n // 16, 64), dtype=torch.float16, device=w.device)
+    _check(lib().clef_lut6_quantize(_ptr(w), n, k, _ptr(packed), _ptr(lut), _stream(stream)),
+           "clef_lut6_quantize")
+    return packed, lut
 
 
 def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None, tiled=False):

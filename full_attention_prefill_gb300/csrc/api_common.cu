@@ -227,6 +227,10 @@ clef_status clef_sync_status(clef_stream stream) {
     set_error("a token id was outside [0, vocab)");
     return CLEF_E_BAD_TOKEN;
   }
+  if (v == DEV_NONFINITE) {
+    set_error("a weight given to the quantiser was not finite");
+    return CLEF_E_NONFINITE;
+  }
   set_error("a device wait ran out (code 0x%x)", v);
   return CLEF_E_DEVICE_TIMEOUT;
 }

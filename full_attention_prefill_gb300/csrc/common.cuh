@@ -23,6 +23,7 @@ enum DeviceCode : unsigned {
   DEV_TIMEOUT_DEQUANT = 0x103,
   DEV_TIMEOUT_EPILOGUE = 0x104,
   DEV_BAD_TOKEN = 0x201,
+  DEV_NONFINITE = 0x202,
 };
 
 unsigned* status_word_ptr();          // device address of the status word (host side)

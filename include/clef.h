@@ -50,7 +50,7 @@ typedef enum {
   CLEF_E_ALIGN = 4,            /* a device pointer not 16-byte aligned                       */
   CLEF_E_CUDA = 5,             /* a CUDA runtime/driver call failed                          */
   CLEF_E_DEVICE_TIMEOUT = 6,   /* a device wait ran out (from clef_sync_status)              */
-  CLEF_E_NONFINITE = 7,        /* reserved                                                   */
+  CLEF_E_NONFINITE = 7,        /* a non-finite weight given to the quantiser (sync_status)   */
   CLEF_E_WORKSPACE = 8,        /* workspace smaller than the size query returned             */
   CLEF_E_BAD_TOKEN = 9         /* a token id outside [0, vocab) (from clef_sync_status)      */
 } clef_status;
@@ -107,6 +107,24 @@ CLEF_API clef_status clef_lut6_dequant(const uint8_t* packed, const uint16_t* lu
    row 16G + t/4 + 8.  No bit changes; only whole quadruples move.  Done once per weight. */
 CLEF_API clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
                                     clef_stream stream);
+
+/* device: quantise an fp16 weight w [n, k] (row-major, k fastest) into the LUT-6 format above:
+   packed [n, k*3/4] (the row-major bit stream of clef_lut6_pack) and lut [n/16, 64] fp16
+   ("Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": per 16-row group a 64-value
+   table from 40 rounds of one-dimensional k-means, seeded with 32 quantiles of the group and 32
+   values spread evenly from its minimum to its maximum).  Arithmetic, fixed so that the result
+   is one exact function of w: quantile i (p = (i + 1/2) / 32) interpolates linearly between the
+   order statistics around p (n - 1); spread value i is min + i * ((max - min) / 31), the last
+   one max; each round sends a weight to the nearest centroid (cells between midpoints
+   fl(c_j + c_j+1) / 2 of the ascending centroids; a tie, or several equal centroids, to the
+   lowest index) and moves each centroid with members to fl(S / count), S their exact sum; a
+   centroid without members stays; the centroids are then sorted again (stable).  The table is the centroids rounded to fp16, ascending; each
+   index points at the nearest table entry (ties to the lowest index).  n % 16 == 0, k % 4 == 0,
+   0 < k <= 262144 (CLEF_E_SHAPE otherwise); device pointers, 16-byte aligned, caller owned.
+   A non-finite weight is left out of the tables and reported as CLEF_E_NONFINITE by
+   clef_sync_status.  Asynchronous on `stream`. */
+CLEF_API clef_status clef_lut6_quantize(const uint16_t* w, int64_t n, int64_t k, uint8_t* packed,
+                                        uint16_t* lut, clef_stream stream);
 
 /* device: y [m, n] = x [m, k] . W^T, fp32 accumulation; y is fp16 (y_is_fp32 = 0) or fp32
    (y_is_fp32 = 1); W given as `tiled` (clef_lut6_tile) and lut.  The weights are dequantised
