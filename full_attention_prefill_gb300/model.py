@@ -165,6 +165,20 @@ class PrefillState:
     def pos(self):
         return self.struct.pos
 
+    def clone(self):
+        """An independent copy (device-to-device) at the same position: a shared part prefilled
+        once can then be continued by several question parts, each on its own copy."""
+        c = PrefillState.__new__(PrefillState)
+        c.conv, c.rec = self.conv.clone(), self.rec.clone()
+        c.kcache, c.vcache = self.kcache.clone(), self.vcache.clone()
+        st = State()
+        st.conv, st.rec = _ptr(c.conv), _ptr(c.rec)
+        st.kcache, st.vcache = _ptr(c.kcache), _ptr(c.vcache)
+        st.ctx, st.pos = self.struct.ctx, self.struct.pos
+        c.struct = st
+        c.B = self.B
+        return c
+
 
 def synth_model(seed=0, n_layers=32, device="cuda", embed=None):
     """The synthetic model (seeded random weights, the recipe of the `synth` module)."""

@@ -80,3 +80,33 @@ def test_chunk_past_the_state_is_refused(small):
     assert e.value.code == 3          # CLEF_E_TOO_LONG: refused, never cut
     assert st.pos == 64               # a refused call leaves the state where it was
     clef.sync_status()
+
+
+def test_shared_state_reused_by_two_question_parts(small):
+    """Shared-state pair ("clef-flash-LiteRT" card, "Other forms measured"): the shared part is
+    prefilled once, then two different question parts each continue their own copy of its state;
+    each must equal the one-call prefill of shared part + its questions, and the shared state must
+    stay untouched."""
+    seed, n_layers, m, ids, whole = small
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    shared = ids[:, :100]
+    st = PrefillState(m, 2, 192)
+    m.forward_chunk(dev(shared), st)
+    before = [t.clone() for t in (st.conv, st.rec, st.kcache, st.vcache)]
+    qa = ids[:, 100:130]
+    qb = synth.uniform_int(seed, "chunk-ids-b", -1, (2, 45), 4000)
+    sa, sb = st.clone(), st.clone()
+    out_a = m.forward_chunk(dev(qa), sa).double().cpu().numpy()
+    out_b = m.forward_chunk(dev(qb), sb).double().cpu().numpy()
+    clef.sync_status()
+    assert (st.pos, sa.pos, sb.pos) == (100, 130, 145)
+    assert all(torch.equal(a, b) for a, b in zip(before, (st.conv, st.rec, st.kcache, st.vcache)))
+    whole_b = m.forward(dev(np.concatenate([shared, qb], axis=1))).double().cpu().numpy()
+    clef.sync_status()
+    for b in range(2):
+        ea = rel_rmse(out_a[b], whole[b, 100:])
+        eb = rel_rmse(out_b[b], whole_b[b, 100:])
+        print(f"shared state b={b}: questions A vs whole {ea:.2e}, questions B vs whole {eb:.2e}")
+        assert ea < SAME_TOL and eb < SAME_TOL
+        assert min_row_cosine(out_a[b], whole[b, 100:]) > 0.9999
+    assert rel_rmse(out_a[0], out_b[0, :30]) > 0.1      # different questions, different rows
