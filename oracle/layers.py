@@ -147,6 +147,63 @@ def rope(x, positions, rot_dims=ROPE_DIMS, theta=ROPE_THETA):
     return x
 
 
+MROPE_SECTIONS = (11, 11, 10)   # frequency pairs on the t, h and w planes
+
+
+def mrope_planes(rot_dims=ROPE_DIMS):
+    """Plane (0 = t, 1 = h, 2 = w) of each of the 32 frequency pairs.
+
+    "clef-flash-LiteRT" §Host contract step 5: three planes, sections 11 / 11 / 10, interleaved.
+    Reading: pair j takes plane j mod 3, which gives exactly 11, 11 and 10 pairs.
+    """
+    return np.arange(rot_dims // 2) % 3
+
+
+def mrope_positions(L, image_start=0, grid_h=0, grid_w=0):
+    """[L, 3] integer positions (t, h, w) of a request holding at most one picture block.
+
+    "clef-flash-LiteRT" §Host contract step 5: a text token at index i has position (i, i, i),
+    a picture's tokens take their row and column in the picture's grid, padding continues the
+    positions.  "clef-flash - Core AI" §Core AI shape: image token k sits at row k // W, column
+    k % W, and from the <|vision_end|> index (picture start + N) on the positions move back by
+    N - max(H, W).  Reading (the plainest one those numbers allow): image token k at index s + k
+    has (s, s + k // W, s + k % W), so the token after the block continues at s + max(H, W), one
+    past the largest picture position.
+    """
+    n = grid_h * grid_w
+    pos = np.empty((L, 3), dtype=np.int64)
+    for i in range(L):
+        if n == 0 or i < image_start:
+            pos[i] = (i, i, i)
+        elif i < image_start + n:
+            k = i - image_start
+            pos[i] = (image_start, image_start + k // grid_w, image_start + k % grid_w)
+        else:
+            p = i - (n - max(grid_h, grid_w))
+            pos[i] = (p, p, p)
+    return pos
+
+
+def mrope(x, pos3, rot_dims=ROPE_DIMS, theta=ROPE_THETA):
+    """Multimodal rotary: as :func:`rope`, with pair j rotated by pos3[:, plane(j)] * theta^(-2j/64).
+
+    "clef-flash-LiteRT" §Host contract step 5 (cos and sin [L, 64] of the three-plane positions,
+    theta = 1e7).  With pos3 = (i, i, i) it is :func:`rope` at position i.
+    """
+    x = f64(x).copy()
+    half = rot_dims // 2
+    inv_freq = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / rot_dims)
+    pos3 = np.asarray(pos3)
+    ang = f64(pos3[:, mrope_planes(rot_dims)]) * inv_freq[None, :]     # [L, half]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    x1 = x[..., :half].copy()
+    x2 = x[..., half:rot_dims].copy()
+    x[..., :half] = x1 * c - x2 * s
+    x[..., half:rot_dims] = x2 * c + x1 * s
+    return x
+
+
 def causal_attention(q, k, v):
     """Causal softmax attention with grouped keys/values, one explicit softmax per query row.
 

@@ -74,13 +74,14 @@ def attention_mixer(xn, w, positions=None, return_parts=False):
     xn = Lr.f64(xn)
     L = xn.shape[0]
     pos = np.arange(L) if positions is None else np.asarray(positions)
+    rot = Lr.mrope if pos.ndim == 2 else Lr.rope       # [L, 3] M-RoPE planes or [L] positions
     qg = _lin(xn, w["q"])
     q = qg[:, :ATT_HQ * ATT_D].reshape(L, ATT_HQ, ATT_D)
     gate = qg[:, ATT_HQ * ATT_D:]
     k = _lin(xn, w["k"]).reshape(L, ATT_HKV, ATT_D)
     v = _lin(xn, w["v"]).reshape(L, ATT_HKV, ATT_D)
-    qr = Lr.rope(q, pos)
-    kr = Lr.rope(k, pos)
+    qr = rot(q, pos)
+    kr = rot(k, pos)
     o = Lr.causal_attention(qr, kr, v).reshape(L, ATT_HQ * ATT_D)
     og = o * Lr.sigmoid(gate)
     out = _lin(og, w["o"])
@@ -89,11 +90,13 @@ def attention_mixer(xn, w, positions=None, return_parts=False):
     return out
 
 
-def decoder_layer(x, w, attention: bool):
-    """One pre-norm residual decoder layer on one request: x [L, 4096] -> [L, 4096]."""
+def decoder_layer(x, w, attention: bool, positions=None):
+    """One pre-norm residual decoder layer on one request: x [L, 4096] -> [L, 4096].
+    `positions`: rotary positions of the attention layers ([L], or [L, 3] M-RoPE planes;
+    default 0 .. L - 1)."""
     x = Lr.f64(x)
     xn = Lr.rmsnorm(x, w["attn_norm"])
-    h = x + (attention_mixer(xn, w) if attention else gdn_mixer(xn, w))
+    h = x + (attention_mixer(xn, w, positions) if attention else gdn_mixer(xn, w))
     return h + swiglu_mlp(Lr.rmsnorm(h, w["mlp_norm"]), w)
 
 
@@ -101,16 +104,18 @@ def is_attention_layer(layer: int) -> bool:
     return layer % 4 == 3
 
 
-def prefill(ids, embed_rows, layer_weights, final_norm, n_layers=32):
+def prefill(ids, embed_rows, layer_weights, final_norm, n_layers=32, positions=None):
     """The hybrid prefill of one request: ids [L] -> final-norm hidden [L, 4096] (float64).
 
     "clef-flash-LiteRT" §Host contract steps 4-6: embedding rows at the request's ids in, the
     hidden states after the final RMSNorm at every position out, no state carried between
     calls.  `embed_rows` is [L, 4096] (the table's rows at `ids`, gathered by the caller);
-    `layer_weights(l)` returns layer l's weight dict.
+    `layer_weights(l)` returns layer l's weight dict.  A request with a picture passes the
+    picture's rows in place of the table's rows at its <|image_pad|> positions (step 4) and its
+    M-RoPE positions ([L, 3], :func:`oracle.layers.mrope_positions`; step 5).
     """
     x = Lr.f64(embed_rows)
     assert x.shape[0] == len(ids)
     for layer in range(n_layers):
-        x = decoder_layer(x, layer_weights(layer), is_attention_layer(layer))
+        x = decoder_layer(x, layer_weights(layer), is_attention_layer(layer), positions)
     return Lr.rmsnorm(x, final_norm)
