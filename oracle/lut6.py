@@ -43,11 +43,14 @@ def unpack(packed: np.ndarray, k: int) -> np.ndarray:
     n = packed.shape[0]
     if k % 4 or packed.shape[1] != k * 3 // 4:
         raise ValueError("packed row length must be k*3/4 with k % 4 == 0")
-    b = packed.reshape(n, k // 4, 3).astype(np.uint32)
-    w = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16)
+    # index j is bits 6j .. 6j + 5 of the word w = b0 | b1 << 8 | b2 << 16, read byte by byte
+    b = packed.reshape(n, k // 4, 3)
+    b0, b1, b2 = b[..., 0], b[..., 1], b[..., 2]
     out = np.empty((n, k // 4, 4), dtype=np.uint8)
-    for j in range(4):
-        out[..., j] = (w >> (6 * j)) & 0x3F
+    out[..., 0] = b0 & 0x3F
+    out[..., 1] = (b0 >> 6) | ((b1 & 0x0F) << 2)
+    out[..., 2] = (b1 >> 4) | ((b2 & 0x03) << 4)
+    out[..., 3] = b2 >> 2
     return out.reshape(n, k)
 
 
@@ -57,8 +60,13 @@ def dequant(packed: np.ndarray, lut: np.ndarray, n: int, k: int) -> np.ndarray:
     if n % GROUP_ROWS or lut.shape != (n // GROUP_ROWS, TABLE_SIZE):
         raise ValueError("lut must be [n/16, 64] with n % 16 == 0")
     idx = unpack(packed, k)
-    group = (np.arange(n) // GROUP_ROWS)[:, None]
-    return lut.astype(np.float64)[group, idx]
+    table = lut.astype(np.float64)
+    out = np.empty((n, k))
+    for g in range(n // GROUP_ROWS):
+        rows = slice(GROUP_ROWS * g, GROUP_ROWS * (g + 1))
+        # table[g][idx[rows]]; 6-bit indices never reach the clip
+        np.take(table[g], idx[rows], out=out[rows], mode="clip")
+    return out
 
 
 def dequant_f16(packed: np.ndarray, lut: np.ndarray, n: int, k: int) -> np.ndarray:
