@@ -108,6 +108,11 @@ _SIGS = {
     "clef_prefill_forward": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_size_t, ctypes.c_void_p]),
+    "clef_mrope_positions": (ctypes.c_int, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
+    "clef_prefill_forward_image": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "clef_prefill_chunk_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "clef_prefill_forward_chunk": (ctypes.c_int, [ctypes.POINTER(Model), ctypes.c_void_p, ctypes.c_int64,
                                                   ctypes.c_int64, ctypes.POINTER(State), ctypes.c_void_p,
@@ -169,6 +174,15 @@ def lut6_pack(idx):
     n, k = a.shape
     out = np.empty((n, k * 3 // 4), dtype=np.uint8)
     _check(lib().clef_lut6_pack(a.ctypes.data, n, k, out.ctypes.data), "clef_lut6_pack")
+    return out
+
+
+def mrope_positions(L, image_start=0, grid=(0, 0)):
+    """Host: [L, 3] int32 M-RoPE positions (t, h, w) of a request with at most one picture."""
+    import numpy as np
+    out = np.empty((L, 3), dtype=np.int32)
+    _check(lib().clef_mrope_positions(L, image_start, grid[0], grid[1], out.ctypes.data),
+           "clef_mrope_positions")
     return out
 
 

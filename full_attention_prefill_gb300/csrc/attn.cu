@@ -7,7 +7,11 @@
 // query heads of a group, causal additive mask.
 //
 //   rope_kernel   rotates dims 0..63 of every q and k head (rotate-half pairs (j, j+32), angle
-//                 pos * 1e7^(-j/32), computed in fp64), in place or into a copy.
+//                 pos * 1e7^(-j/32), computed in fp64), in place or into a copy.  With a picture
+//                 block (M-RoPE, "Host contract" step 5: three planes, sections 11 / 11 / 10
+//                 interleaved, so pair j reads plane j mod 3), a picture token k at index s + k
+//                 has planes (s, s + k / W, s + k % W) and tokens after the block move back by
+//                 N - max(H, W) ("clef-flash - Core AI" README, "Core AI shape").
 //   flash_tc_kernel  one CTA = 32 positions x the 4 query heads of one kv head (128 rows), so
 //                 each K/V tile is read once for the group; tcgen05 MMAs with S and O in tensor
 //                 memory; online softmax over 64-key tiles; epilogue o * sigmoid(gate).
@@ -28,15 +32,31 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
                                                    __half* __restrict__ qout, int64_t ldqo,
                                                    const __half* __restrict__ kin, int64_t ldki,
                                                    __half* __restrict__ kout, int64_t ldko, int L,
-                                                   int pos0, int64_t kctx) {
+                                                   int pos0, int64_t kctx, int mstart, int mh,
+                                                   int mw) {
   __shared__ float cs[32], sn[32];
   const int64_t tok = blockIdx.x;
   const int64_t t = tok % L;
-  const int pos = pos0 + (int)t;
-  // k goes to row (request * kctx + pos) of kout (kctx = L, pos0 = 0: the token's own row)
-  const int64_t krow = (tok / L) * kctx + pos;
+  const int idx = pos0 + (int)t;   // token index in the request
+  // k goes to row (request * kctx + idx) of kout (kctx = L, pos0 = 0: the token's own row)
+  const int64_t krow = (tok / L) * kctx + idx;
   const int tid = threadIdx.x;
   if (tid < 32) {
+    // M-RoPE planes of this token (all equal to idx for text)
+    const int n = mh * mw;
+    int pt = idx, ph = idx, pw = idx;
+    if (n > 0 && idx >= mstart) {
+      if (idx < mstart + n) {
+        const int k = idx - mstart;
+        pt = mstart;
+        ph = mstart + k / mw;
+        pw = mstart + k % mw;
+      } else {
+        pt = ph = pw = idx - (n - max(mh, mw));
+      }
+    }
+    const int plane = tid % 3;
+    const int pos = plane == 0 ? pt : (plane == 1 ? ph : pw);
     // angle = pos * theta^(-j/32), reduced and evaluated in fp64 (ln 1e7 = 16.118...)
     const double inv_freq = exp(-(double)tid * (16.11809565095832 / 32.0));
     double s, c;
@@ -430,11 +450,13 @@ __global__ void kv_store_kernel(const __half* __restrict__ src, int64_t lds, __h
 
 clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t ldqo,
                         const __half* kin, int64_t ldki, __half* kout, int64_t ldko, int64_t M,
-                        int64_t L, int64_t pos0, int64_t kctx, cudaStream_t stream) {
+                        int64_t L, int64_t pos0, int64_t kctx, cudaStream_t stream,
+                        const MRope& mr) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
   attn::rope_kernel<<<(unsigned)M, 128, 0, stream>>>(qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
-                                                     (int)L, (int)pos0, kctx);
+                                                     (int)L, (int)pos0, kctx, (int)mr.start,
+                                                     (int)mr.h, (int)mr.w);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

@@ -84,6 +84,7 @@ struct LayerState {
   __half* vc = nullptr;
   int64_t ctx = 0;
   int64_t pos0 = 0;
+  MRope mr;                 // picture block of every request (M-RoPE); h * w == 0: text only
 };
 
 static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, int64_t L,
@@ -118,12 +119,13 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
       // positions 0 .. pos0 + L - 1 from there
       constexpr int64_t KV = 4 * 256;
       CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, st.kc, KV, M, L, st.pos0,
-                           st.ctx, s));
+                           st.ctx, s, st.mr));
       CLEF_TRY(kv_store_launch(vp, ATT_PROJ, st.vc, KV, M, L, st.pos0, st.ctx, (int)KV, s));
       CLEF_TRY(flash_launch(qp, ATT_PROJ, st.kc, KV, st.vc, KV, gp, ATT_PROJ, w.mix, H, B, L,
                             st.pos0, st.ctx, s));
     } else {
-      CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, kp, ATT_PROJ, M, L, 0, L, s));
+      CLEF_TRY(rope_launch(qp, ATT_PROJ, qp, ATT_PROJ, kp, ATT_PROJ, kp, ATT_PROJ, M, L, 0, L, s,
+                           st.mr));
       CLEF_TRY(flash_launch(qp, ATT_PROJ, kp, ATT_PROJ, vp, ATT_PROJ, gp, ATT_PROJ, w.mix, H, B, L,
                             0, L, s));
     }
@@ -187,6 +189,43 @@ static clef_status check_bl(int64_t B, int64_t L) {
     return CLEF_E_SHAPE;
   }
   return CLEF_OK;
+}
+
+// The whole prefill of B requests (ids [B][L]); with image_rows, rows mr.start .. of every
+// request are the picture's rows ([B][h * w][4096] fp16) and the rotary uses M-RoPE planes.
+static clef_status prefill_impl(const char* who, const clef_model* model, const int32_t* ids,
+                                int64_t B, int64_t L, const __half* image_rows, const MRope& mr,
+                                uint16_t* hidden, void* workspace, size_t workspace_bytes,
+                                clef_stream stream) {
+  CLEF_TRY(check_bl(B, L));
+  if (!model || !model->layers || model->n_layers < 1 || model->n_layers > 64 ||
+      model->vocab < 1) {
+    set_error("%s: bad model (layers, n_layers in 1..64, vocab >= 1)", who);
+    return CLEF_E_INVALID;
+  }
+  if (bad_ptr(ids) || bad_ptr(hidden) || bad_ptr(workspace) || bad_ptr(model->embed) ||
+      bad_ptr(model->final_norm)) {
+    set_error("%s: a pointer is NULL or not 16-byte aligned", who);
+    return CLEF_E_INVALID;
+  }
+  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(check_layer(&model->layers[i], i));
+  if (workspace_bytes < fwd_layout(B, L, nullptr, nullptr)) {
+    set_error("%s: workspace of %zu bytes, need %zu", who, workspace_bytes,
+              fwd_layout(B, L, nullptr, nullptr));
+    return CLEF_E_WORKSPACE;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FwdWs w;
+  fwd_layout(B, L, workspace, &w);
+  const int64_t M = B * L;
+  CLEF_TRY(embed_launch(ids, reinterpret_cast<const __half*>(model->embed), model->vocab, w.x, M, s));
+  if (image_rows) CLEF_TRY(image_rows_launch(image_rows, w.x, B, L, mr.start, mr.h * mr.w, s));
+  LayerState ls;
+  ls.mr = mr;
+  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+  return rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
+                        reinterpret_cast<__half*>(hidden), M, s);
 }
 
 }  // namespace clef
@@ -300,32 +339,66 @@ clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64_t B, int
 clef_status clef_prefill_forward(const clef_model* model, const int32_t* ids, int64_t B, int64_t L,
                                  uint16_t* hidden, void* workspace, size_t workspace_bytes,
                                  clef_stream stream) {
-  CLEF_TRY(check_bl(B, L));
-  if (!model || !model->layers || model->n_layers < 1 || model->n_layers > 64 ||
-      model->vocab < 1) {
-    set_error("clef_prefill_forward: bad model (layers, n_layers in 1..64, vocab >= 1)");
+  return prefill_impl("clef_prefill_forward", model, ids, B, L, nullptr, MRope(), hidden,
+                      workspace, workspace_bytes, stream);
+}
+
+clef_status clef_prefill_forward_image(const clef_model* model, const int32_t* ids, int64_t B,
+                                       int64_t L, const uint16_t* image_rows, int64_t image_start,
+                                       int64_t grid_h, int64_t grid_w, uint16_t* hidden,
+                                       void* workspace, size_t workspace_bytes,
+                                       clef_stream stream) {
+  if (grid_h < 0 || grid_w < 0 || (grid_h == 0) != (grid_w == 0) || image_start < 0) {
+    set_error("clef_prefill_forward_image: need grid_h, grid_w both 0 or both >= 1 and "
+              "image_start >= 0");
     return CLEF_E_INVALID;
   }
-  if (bad_ptr(ids) || bad_ptr(hidden) || bad_ptr(workspace) || bad_ptr(model->embed) ||
-      bad_ptr(model->final_norm)) {
-    set_error("clef_prefill_forward: a pointer is NULL or not 16-byte aligned");
+  const int64_t n = grid_h * grid_w;
+  if (n > 0 && (image_start + n > L)) {
+    set_error("clef_prefill_forward_image: the picture's %lld tokens from index %lld do not fit "
+              "in L = %lld", (long long)n, (long long)image_start, (long long)L);
+    return CLEF_E_SHAPE;
+  }
+  if (n > 0 && bad_ptr(image_rows)) {
+    set_error("clef_prefill_forward_image: image_rows NULL or not 16-byte aligned");
     return CLEF_E_INVALID;
   }
-  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(check_layer(&model->layers[i], i));
-  if (workspace_bytes < fwd_layout(B, L, nullptr, nullptr)) {
-    set_error("clef_prefill_forward: workspace of %zu bytes, need %zu", workspace_bytes,
-              fwd_layout(B, L, nullptr, nullptr));
-    return CLEF_E_WORKSPACE;
+  MRope mr;
+  mr.start = n > 0 ? image_start : 0;
+  mr.h = grid_h;
+  mr.w = grid_w;
+  return prefill_impl("clef_prefill_forward_image", model, ids, B, L,
+                      n > 0 ? reinterpret_cast<const __half*>(image_rows) : nullptr, mr, hidden,
+                      workspace, workspace_bytes, stream);
+}
+
+clef_status clef_mrope_positions(int64_t L, int64_t image_start, int64_t grid_h, int64_t grid_w,
+                                 int32_t* pos3) {
+  if (!pos3 || L < 0 || grid_h < 0 || grid_w < 0 || (grid_h == 0) != (grid_w == 0) ||
+      image_start < 0) {
+    set_error("clef_mrope_positions: NULL output or bad sizes");
+    return CLEF_E_INVALID;
   }
-  if (debug_should_fail()) return CLEF_E_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  FwdWs w;
-  fwd_layout(B, L, workspace, &w);
-  const int64_t M = B * L;
-  CLEF_TRY(embed_launch(ids, reinterpret_cast<const __half*>(model->embed), model->vocab, w.x, M, s));
-  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(run_layer(model->layers[i], w, B, L, s));
-  return rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
-                        reinterpret_cast<__half*>(hidden), M, s);
+  const int64_t n = grid_h * grid_w;
+  if (n > 0 && image_start + n > L) {
+    set_error("clef_mrope_positions: the picture does not fit in L");
+    return CLEF_E_SHAPE;
+  }
+  for (int64_t i = 0; i < L; ++i) {
+    int64_t p[3] = {i, i, i};
+    if (n > 0 && i >= image_start) {
+      if (i < image_start + n) {
+        const int64_t k = i - image_start;
+        p[0] = image_start;
+        p[1] = image_start + k / grid_w;
+        p[2] = image_start + k % grid_w;
+      } else {
+        p[0] = p[1] = p[2] = i - (n - std::max(grid_h, grid_w));
+      }
+    }
+    for (int c = 0; c < 3; ++c) pos3[3 * i + c] = (int32_t)p[c];
+  }
+  return CLEF_OK;
 }
 
 size_t clef_prefill_chunk_workspace_size(int64_t B, int64_t L) {

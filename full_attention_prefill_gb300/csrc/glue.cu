@@ -14,6 +14,25 @@ namespace glue {
 
 constexpr int H = 4096;
 
+// One picture row per CTA: fp16 row r = b * n + k of `rows` widens into row b * L + start + k of x.
+__global__ void __launch_bounds__(256) image_rows_kernel(const __half* __restrict__ rows,
+                                                         float* __restrict__ x, int64_t L,
+                                                         int64_t start, int64_t n) {
+  const int64_t r = blockIdx.x, b = r / n, k = r % n;
+  const int c0 = threadIdx.x * 16;
+  const uint4* src = reinterpret_cast<const uint4*>(rows + r * H + c0);
+  float4* dst = reinterpret_cast<float4*>(x + (b * L + start + k) * H + c0);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint4 u = src[i];
+    const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+    const float2 a = __half22float2(h2[0]), c = __half22float2(h2[1]);
+    const float2 d = __half22float2(h2[2]), e = __half22float2(h2[3]);
+    dst[2 * i] = make_float4(a.x, a.y, c.x, c.y);
+    dst[2 * i + 1] = make_float4(d.x, d.y, e.x, e.y);
+  }
+}
+
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ ids,
                                                     const __half* __restrict__ table,
                                                     int64_t vocab, float* __restrict__ x,
@@ -190,6 +209,15 @@ clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab,
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "embed", 0.0, M * (4096.0 * 2 + 4096.0 * 4));
   glue::embed_kernel<<<(unsigned)M, 256, 0, stream>>>(ids, table, vocab, x, status_word_ptr());
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status image_rows_launch(const __half* rows, float* x, int64_t B, int64_t L, int64_t start,
+                              int64_t n, cudaStream_t stream) {
+  if (B == 0 || n == 0) return CLEF_OK;
+  TraceScope ts(stream, "image_rows", 0.0, B * n * (4096.0 * 2 + 4096.0 * 4));
+  glue::image_rows_kernel<<<(unsigned)(B * n), 256, 0, stream>>>(rows, x, L, start, n);
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

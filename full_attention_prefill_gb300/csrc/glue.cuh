@@ -9,6 +9,11 @@ namespace clef {
 clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab, float* x,
                          int64_t M, cudaStream_t stream);
 
+// Picture rows: rows start .. start + n - 1 of each of B requests of L tokens in the fp32 residual
+// x take rows [b][0 .. n) of `rows` (fp16 [B][n][4096]) in place of the embedding rows.
+clef_status image_rows_launch(const __half* rows, float* x, int64_t B, int64_t L, int64_t start,
+                              int64_t n, cudaStream_t stream);
+
 // y [M, 4096] fp16 = x * rsqrt(mean(x^2) + 1e-6) * w.
 clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
                            cudaStream_t stream);

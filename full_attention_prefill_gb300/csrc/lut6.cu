@@ -390,8 +390,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tok0 + 32 + i < M) out[(int64_t)(tok0 + 32 + i) * ldy] = __uint_as_float(r1[i]);
           }
         } else {
-          // residual add, done by L2 (each element receives exactly one add per launch, so
-          // the result is the same as load + add + store); no load latency on this path
+          // residual add, done by L2; no load latency on this path.  Without a K split each
+          // element receives exactly one add per launch (the same as load + add + store); with
+          // one, the parts' adds land in any order, so such launches repeat only to fp32
+          // rounding
           float* out = reinterpret_cast<float*>(y) + col;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {

@@ -126,6 +126,26 @@ class DeviceModel:
                                           ws.numel(), _stream(stream)), "clef_prefill_forward")
         return out
 
+    def forward_image(self, ids, image_rows, image_start, grid, out=None, stream=None):
+        """ids [B, L] int32 (device) with a picture block of grid = (H, W) tokens at image_start
+        in every request; image_rows [B, H*W, 4096] fp16 (device) -> hidden [B, L, 4096] fp16
+        (M-RoPE positions in the attention layers)."""
+        if not (ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous()):
+            raise ValueError("ids must be a contiguous int32 CUDA tensor")
+        B, L = ids.shape
+        n = grid[0] * grid[1]
+        if n and not (image_rows.is_cuda and image_rows.dtype == torch.float16 and
+                      tuple(image_rows.shape) == (B, n, HIDDEN) and image_rows.is_contiguous()):
+            raise ValueError("image_rows must be a contiguous fp16 CUDA tensor [B, H*W, 4096]")
+        if out is None:
+            out = torch.empty((B, L, HIDDEN), dtype=torch.float16, device=ids.device)
+        ws = self.workspace(B, L)
+        _check(lib().clef_prefill_forward_image(ctypes.byref(self.struct), _ptr(ids), B, L,
+                                                _ptr(image_rows) if n else None, image_start,
+                                                grid[0], grid[1], _ptr(out), _ptr(ws), ws.numel(),
+                                                _stream(stream)), "clef_prefill_forward_image")
+        return out
+
     def forward_chunk(self, ids, state, out=None, stream=None):
         """ids [B, L] int32 (device): positions state.pos .. state.pos + L - 1 of the state's
         requests -> their final-norm hidden [B, L, 4096] fp16; the state moves on by L."""

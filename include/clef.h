@@ -245,6 +245,33 @@ CLEF_API clef_status clef_prefill_forward(const clef_model* model, const int32_t
                                  uint16_t* hidden, void* workspace, size_t workspace_bytes,
                                  clef_stream stream);
 
+/* M-RoPE positions of one request of L tokens holding at most one picture block
+   ("clef-flash-LiteRT" README, "Host contract" step 5: three planes, theta = 1e7, a text token at
+   index i has position (i, i, i), picture tokens take their row and column in the grid;
+   "clef-flash - Core AI" README, "Core AI shape": image token k at row k / W, column k % W, and
+   from the <|vision_end|> index image_start + N on the positions move back by N - max(H, W)).
+   host: pos3 [L][3] int32 (t, h, w), caller owned: image token k (index image_start + k,
+   k < N = grid_h * grid_w) gets (image_start, image_start + k / grid_w, image_start + k % grid_w).
+   grid_h = grid_w = 0: text only.  CLEF_E_INVALID for bad sizes or a NULL pos3, CLEF_E_SHAPE if
+   the picture does not fit in L. */
+CLEF_API clef_status clef_mrope_positions(int64_t L, int64_t image_start, int64_t grid_h,
+                                          int64_t grid_w, int32_t* pos3);
+
+/* device: clef_prefill_forward for B requests that each hold one picture block of
+   grid_h x grid_w tokens at token indices image_start .. image_start + N - 1 (the
+   <|image_pad|> tokens; "clef-flash-LiteRT" README, "Host contract" steps 4-5).  Those rows take
+   image_rows [B, N, 4096] fp16 (device; the vision tower's merged rows, request-major) instead of
+   embedding rows, and the attention layers' rotary uses the M-RoPE positions of
+   clef_mrope_positions: frequency pair j (of 32) turns by the position on plane j mod 3
+   (sections 11 / 11 / 10, interleaved).  grid_h = grid_w = 0 (image_rows may be NULL) is
+   clef_prefill_forward.  Same workspace as clef_prefill_forward.  CLEF_E_INVALID for bad grid
+   sizes or a NULL / misaligned image_rows, CLEF_E_SHAPE if the picture does not fit in L. */
+CLEF_API clef_status clef_prefill_forward_image(const clef_model* model, const int32_t* ids,
+                                                int64_t B, int64_t L, const uint16_t* image_rows,
+                                                int64_t image_start, int64_t grid_h,
+                                                int64_t grid_w, uint16_t* hidden, void* workspace,
+                                                size_t workspace_bytes, clef_stream stream);
+
 /* ------------------------------------------------------------------------------------------
  * Chunked prefill with carried state ("clef-flash - Core AI" README, section "Core AI shape": a
  * request is prefilled as successive calls of 64 positions from zeroed states, each carrying the

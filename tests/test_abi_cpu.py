@@ -72,3 +72,21 @@ def test_gate_up_interleave_layout():
         t = b // 16
         assert np.array_equal(l[2 * j * t:(2 * j + 1) * t], gl[j * t:(j + 1) * t])
         assert np.array_equal(l[(2 * j + 1) * t:(2 * j + 2) * t], ul[j * t:(j + 1) * t])
+
+
+@pytest.mark.parametrize("L,s,h,w", [(46, 37, 2, 3), (50, 0, 0, 0), (300, 37, 14, 14),
+                                     (120, 37, 8, 8), (20, 3, 1, 7), (64, 0, 8, 8)])
+def test_host_mrope_positions_match_oracle(lib, L, s, h, w):
+    import full_attention_prefill_gb300 as clef
+    from oracle import layers as Lr
+    assert np.array_equal(clef.mrope_positions(L, s, (h, w)), Lr.mrope_positions(L, s, h, w))
+
+
+def test_host_mrope_positions_errors(lib):
+    import full_attention_prefill_gb300 as clef
+    with pytest.raises(clef.ClefError) as e:
+        clef.mrope_positions(40, 37, (2, 3))          # the picture does not fit
+    assert e.value.code == 2
+    with pytest.raises(clef.ClefError) as e:
+        clef.mrope_positions(40, 0, (2, 0))           # half a grid
+    assert e.value.code == 1
