@@ -324,7 +324,8 @@ def run_micro(args):
     gdn: clef_gdn_prefill at L; layer: clef_decoder_layer of layer --layer at L (the residual
     copy-in is part of each iteration); chunk: one request of L positions as calls of --chunk
     positions through clef_prefill_forward_chunk (zeroing the state is part of each iteration);
-    quantize: clef_lut6_quantize of an N x K fp16 weight.  Prints one JSON line with the
+    quantize: clef_lut6_quantize of an N x K fp16 weight; image: a prefill of L positions with a
+    14 x 14 picture block through clef_prefill_forward_image.  Prints one JSON line with the
     per-kernel times of the library's trace; not the headline metric.
     """
     import numpy as np
@@ -369,6 +370,18 @@ def run_micro(args):
                 model.forward_chunk(c, st)
         flops, desc = 0.0, f"chunked prefill L={L} in calls of {C}"
         extra_fn = lambda ms: {"tokens_per_s": L / (ms / 1000.0), "ms_per_call": ms / len(calls)}  # noqa: E731
+    elif args.micro == "image":
+        # one request of --L positions holding a 14 x 14 picture block (196 tokens, the pages'
+        # 448-pixel tile) at index 37, through clef_prefill_forward_image (M-RoPE rotary)
+        from full_attention_prefill_gb300.model import synth_model
+        L, grid = args.L, (14, 14)
+        model = synth_model(0, 32, device=dev)
+        ids = torch.from_numpy(synth.token_ids(1000, 1, L)).to(dev)
+        rows = torch.from_numpy(synth.normal_f16(0, "micro.image", -1, (1, 196, 4096), 0.0, 0.05)).to(dev)
+        out = torch.empty((1, L, 4096), dtype=torch.float16, device=dev)
+        fn = lambda: model.forward_image(ids, rows, 37, grid, out=out)  # noqa: E731
+        flops, desc = 0.0, f"picture prefill L={L}, 14x14 block at 37"
+        extra_fn = lambda ms: {"tokens_per_s": L / (ms / 1000.0)}  # noqa: E731
     elif args.micro == "quantize":
         # LUT-6 quantisation of one fp16 weight [--n, --k] (default: the MLP down projection)
         N, K = args.n, args.k
@@ -437,7 +450,7 @@ def run_micro(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk", "quantize"], default=None)
+    ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk", "quantize", "image"], default=None)
     ap.add_argument("--chunk", type=int, default=64)
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--m", type=int, default=4096)
