@@ -22,6 +22,7 @@
 // The chunk phase's products run on mma.sync (m16n8k16, fp16 inputs, fp32 accumulation); the
 // state and the scalars stay fp32.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "gdn.cuh"
@@ -216,12 +217,13 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const __half* __restrict__ qq, const __half* __restrict__ kk, const __half* __restrict__ vv,
     const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ ef,
     __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Kdout,
-    __half* __restrict__ AqkT, int L, int nch) {
+    __half* __restrict__ AqkT, int L, int nch, int c0, int ncl) {
   extern __shared__ __align__(16) uint8_t smraw[];
   WySmem& s = *reinterpret_cast<WySmem*>(smraw);
-  const int cg = blockIdx.x;           // global chunk index = b * nch + c
+  // this launch covers chunks c0 .. c0 + ncl - 1 of every request
+  const int b = blockIdx.x / ncl, c = c0 + (int)(blockIdx.x % ncl);
+  const int cg = b * nch + c;          // global chunk index
   const int h = blockIdx.y;            // value head
-  const int b = cg / nch, c = cg % nch;
   const int64_t t0 = (int64_t)b * L + (int64_t)c * C;
   const int64_t blk = (int64_t)cg * HV + h;   // output block
   const int nvalid = min(C, L - c * C);
@@ -501,6 +503,15 @@ __global__ void __launch_bounds__(256) gdn_gated_norm_kernel(const __half* __res
 
 static inline size_t al256g(size_t x) { return (x + 255) & ~size_t(255); }
 
+// A long scan of few requests runs in pieces of chunks: the chunk phase of piece p + 1 (many
+// CTAs) overlaps the sequential state pass of piece p (one CTA per request and value head, which
+// leaves most SMs idle), on two streams ordered by events.  Pieces of at least 32 chunks.
+int gdn_pieces(int64_t B, int64_t L) {
+  const int64_t nch = (L + gdn::C - 1) / gdn::C;
+  if (B > 2 || nch < 64) return 1;
+  return (int)std::min<int64_t>(8, nch / 32);
+}
+
 size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   const int64_t M = B * L;
   const int64_t nch = (L + gdn::C - 1) / gdn::C;
@@ -513,6 +524,7 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   n += al256g(rows * gdn::HV * gdn::D * 2);              // decayed keys
   n += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);  // Aqk
   if (with_norm) n += al256g(M * gdn::HV * gdn::D * 2);  // o before the output gate
+  if (gdn_pieces(B, L) > 1) n += al256g(B * gdn::HV * gdn::D * gdn::D * 4);   // carried state
   return n;
 }
 
@@ -524,6 +536,7 @@ struct GdnWs {
   __half* Kt;
   __half* Aqk;
   __half* o;
+  float* state;
 };
 static GdnWs carve(void* ws, int64_t B, int64_t L) {
   const int64_t M = B * L;
@@ -537,7 +550,8 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   w.U1 = reinterpret_cast<float*>(p); p += al256g(rows * gdn::HV * gdn::D * 4);
   w.Kt = reinterpret_cast<__half*>(p); p += al256g(rows * gdn::HV * gdn::D * 2);
   w.Aqk = reinterpret_cast<__half*>(p); p += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);
-  w.o = reinterpret_cast<__half*>(p);
+  w.o = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
+  w.state = reinterpret_cast<float*>(p);   // only when the scan runs in pieces
   return w;
 }
 
@@ -579,6 +593,38 @@ clef_status conv_state_launch(const __half* proj, int64_t ldp, __half* state, in
   return CLEF_OK;
 }
 
+// Two internal streams per device (high priority for the latency-bound state pass, low for the
+// chunk phase) and the events that order them, created on first use and kept for the process.
+// The caller holds `lock` while it enqueues, so the events are never re-recorded by another
+// thread before the waits on them have been enqueued.
+struct SideStreams {
+  cudaStream_t hi = nullptr, lo = nullptr;
+  cudaEvent_t ev[12] = {};
+};
+static std::mutex g_side_mu;
+static clef_status side_streams(SideStreams** out, std::unique_lock<std::mutex>* lock) {
+  static SideStreams per_dev[64];
+  static bool made[64] = {};
+  int dev = 0;
+  CLEF_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) {
+    set_error("device index %d out of range", dev);
+    return CLEF_E_CUDA;
+  }
+  *lock = std::unique_lock<std::mutex>(g_side_mu);
+  if (!made[dev]) {
+    int least = 0, greatest = 0;
+    CLEF_CUDA_CHECK(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+    SideStreams& s = per_dev[dev];
+    CLEF_CUDA_CHECK(cudaStreamCreateWithPriority(&s.hi, cudaStreamNonBlocking, greatest));
+    CLEF_CUDA_CHECK(cudaStreamCreateWithPriority(&s.lo, cudaStreamNonBlocking, least));
+    for (auto& e : s.ev) CLEF_CUDA_CHECK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    made[dev] = true;
+  }
+  *out = &per_dev[dev];
+  return CLEF_OK;
+}
+
 clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, const float* g,
                             const float* alpha, const float* beta, const float* s0, float* s_out,
                             const __half* z, int64_t ldz, const __half* o_norm, __half* out,
@@ -596,19 +642,49 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     CLEF_LAUNCH_CHECK();
     g = w.g;
   }
-  dim3 g1((unsigned)(B * nch), gdn::HV);
-  const double C = gdn::C, D = gdn::D, HVd = gdn::HV, nchunks = (double)B * nch;
-  {
-    TraceScope ts(stream, "gdn_chunk_wy", nchunks * HVd * 8.0 * C * C * D,
-                  (double)M * HVd * D * (2 + 2 + 2 + 2 + 4) + nchunks * HVd * C * C * 2);
-    gdn::gdn_chunk_wy_kernel<<<g1, 128, sizeof(gdn::WySmem), stream>>>(
-        q, k, v, g, beta, w.ef, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch);
-    CLEF_LAUNCH_CHECK();
-  }
   __half* o = z ? w.o : out;
   const int64_t ldo_pass = z ? (int64_t)gdn::HV * gdn::D : ldo;
-  st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, s0, s_out, o, ldo_pass, B, L, stream);
-  if (st != CLEF_OK) return st;
+  auto chunk_phase = [&](int64_t c0, int64_t ncl, cudaStream_t s) -> clef_status {
+    const double C = gdn::C, D = gdn::D, HVd = gdn::HV, nchunks = (double)B * ncl;
+    TraceScope ts(s, "gdn_chunk_wy", nchunks * HVd * 8.0 * C * C * D,
+                  nchunks * C * HVd * D * (2 + 2 + 2 + 2 + 4) + nchunks * HVd * C * C * 2);
+    gdn::gdn_chunk_wy_kernel<<<dim3((unsigned)(B * ncl), gdn::HV), 128, sizeof(gdn::WySmem), s>>>(
+        q, k, v, g, beta, w.ef, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch, (int)c0, (int)ncl);
+    CLEF_LAUNCH_CHECK();
+    return CLEF_OK;
+  };
+  const int pieces = gdn_pieces(B, L);
+  if (pieces <= 1) {
+    st = chunk_phase(0, nch, stream);
+    if (st != CLEF_OK) return st;
+    st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, s0, s_out, o, ldo_pass, B, L, stream);
+    if (st != CLEF_OK) return st;
+  } else {
+    SideStreams* ss = nullptr;
+    std::unique_lock<std::mutex> lock;
+    st = side_streams(&ss, &lock);
+    if (st != CLEF_OK) return st;
+    float* s_eff = s_out ? s_out : w.state;
+    // fork: both side streams start after everything already queued on `stream`
+    CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[0], stream));
+    CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->lo, ss->ev[0], 0));
+    CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->hi, ss->ev[0], 0));
+    for (int p = 0; p < pieces; ++p) {
+      const int64_t c0 = (int64_t)p * nch / pieces, c1 = (int64_t)(p + 1) * nch / pieces;
+      st = chunk_phase(c0, c1 - c0, ss->lo);
+      if (st != CLEF_OK) return st;
+      CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + p], ss->lo));
+      CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->hi, ss->ev[1 + p], 0));
+      st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, p == 0 ? s0 : s_eff, s_eff, o,
+                            ldo_pass, B, L, ss->hi, c0, c1 - c0);
+      if (st != CLEF_OK) return st;
+    }
+    // join
+    CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + pieces], ss->hi));
+    CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[2 + pieces], ss->lo));
+    CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[1 + pieces], 0));
+    CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[2 + pieces], 0));
+  }
   if (z) {
     TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);
     gdn::gdn_gated_norm_kernel<<<(unsigned)M, 256, 0, stream>>>(o, z, ldz, o_norm, out, ldo);

@@ -25,6 +25,8 @@ clef_status conv_state_launch(const __half* proj, int64_t ldp, __half* state, in
 
 // with_norm: room for o before the output gate (decoder layer path, z != NULL)
 size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm);
+// Pieces a scan of B requests of L positions runs in (1: one chunk phase, one state pass).
+int gdn_pieces(int64_t B, int64_t L);
 
 // The chunked scan.  Exactly one of g (log alpha) / alpha is non-NULL.  With z != NULL the
 // output is the z-gated RMSNorm (weight o_norm) of o; otherwise o itself.  out [M, ldo] fp16.
@@ -37,8 +39,11 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
 // one block per (chunk, head) in [B * nch, 32] order: W and decayed keys Kd [64][128] fp16, U'
 // [64][128] fp32, Aqk^T [64][64] fp16 ([s][r]), ef [64] fp32 (exp of the in-chunk cumulative
 // log alpha); and q [B, L, 16, 128] fp16.  out [B * L, ldo] fp16 (head h at columns 128 h ..).
+// One launch walks chunks c0 .. c0 + ncl - 1 of every request (ncl < 0: to the end), entering
+// from s0 (or zero) and leaving the state in s_out (may be s0).
 clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W, const float* U1,
                              const __half* Aqk, const float* ef, const float* s0, float* s_out,
-                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream);
+                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream,
+                             int64_t c0 = 0, int64_t ncl = -1);
 
 }  // namespace clef

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tQ,
     const __grid_constant__ CUtensorMap tKd, const __grid_constant__ CUtensorMap tA,
     const __grid_constant__ CUtensorMap tO, const float* __restrict__ U1, const float* __restrict__ ef, const float* __restrict__ s0, float* __restrict__ s_out, int L,
-    int nch, unsigned* status) {
+    int nch, int c0, int ncl, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x % HV;
   const int b = blockIdx.x / HV;
+  // this launch walks chunks c0 .. c0 + ncl - 1 of each request (i counts them: stages and
+  // barrier phases follow i, data addresses follow c)
   const float* efh = ef + ((int64_t)b * nch * HV + h) * C;   // chunk c at efh + c * HV * C
 
   const uint32_t bar_fa = sb + OFF_BAR;            // [2] part A landed
@@ -125,11 +127,12 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued_a = 0, issued_b = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
+      for (int i = 0; i < ncl; ++i) {
+        const int c = c0 + i;
+        const int st = i & 1;
         const int t0 = c * C;
-        if (c >= NSTAGE &&
-            !mbar_wait(bar_ea + 8 * st, ((c - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
+        if (i >= NSTAGE &&
+            !mbar_wait(bar_ea + 8 * st, ((i - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
           break;
         {
           const uint32_t base = sb + OFF_A + st * A_BYTES;
@@ -142,10 +145,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
             tma_load_4d(base + A_WQ + kb * 2 * BLK + BLK, &tQ, fb, kb * 64, h >> 1, t0, b);
           }
           bulk_copy_g2s(base + A_U, U1 + blk * C * D, C * D * 4, fb);
-          issued_a = c + 1;
+          issued_a = i + 1;
         }
-        if (c >= NSTAGE &&
-            !mbar_wait(bar_eb + 8 * st, ((c - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
+        if (i >= NSTAGE &&
+            !mbar_wait(bar_eb + 8 * st, ((i - NSTAGE) >> 1) & 1, status, DEV_TIMEOUT_TMA))
           break;
         {
           const uint32_t base = sb + OFF_B + st * B_BYTES;
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
           tma_load_2d(base, &tKd, fb, 0, (int)(blk * C));
           tma_load_2d(base + BLK, &tKd, fb, 64, (int)(blk * C));
           tma_load_2d(base + 2 * BLK, &tA, fb, 0, (int)(blk * C));
-          issued_b = c + 1;
+          issued_b = i + 1;
         }
       }
       // copies still in flight land before the CTA may exit (no later phase of these barriers
@@ -171,15 +174,15 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
       constexpr uint32_t id_1 = idesc_f16_f32(128, 128);          // [W ; Q] K-major
       constexpr uint32_t id_2 = idesc_f16_f32(128, 192, 0, 1);    // [Kd | Aqk^T] MN-major
       bool any = false;
-      for (int c = 0; c < nch; ++c) {
-        const int st = c & 1;
-        const uint32_t ph = (uint32_t)c & 1;
+      for (int i = 0; i < ncl; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (uint32_t)i & 1;
         const uint32_t pa = sb + OFF_A + st * A_BYTES;
         const uint32_t pb = sb + OFF_B + st * B_BYTES;
         // [U^T | O1^T] = S0h . [W ; Q]^T, once the previous chunk's O has been drained
-        if (!mbar_wait(bar_fa + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
+        if (!mbar_wait(bar_fa + 8 * st, (i >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
             !mbar_wait(bar_s0, ph, status, DEV_TIMEOUT_MMA) ||
-            (c >= 1 && !mbar_wait(bar_oe, (c - 1) & 1, status, DEV_TIMEOUT_MMA)))
+            (i >= 1 && !mbar_wait(bar_oe, (i - 1) & 1, status, DEV_TIMEOUT_MMA)))
           break;
         tc_fence_after();
 #pragma unroll
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         tc_commit(bar_ea + 8 * st);   // W, Q no longer read (the row threads add theirs for U')
         any = true;
         // [S | O2^T] += U^T . [Kd | Aqk^T]
-        if (!mbar_wait(bar_fb + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
+        if (!mbar_wait(bar_fb + 8 * st, (i >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
             !mbar_wait(bar_uh, ph, status, DEV_TIMEOUT_MMA))
           break;
         tc_fence_after();
@@ -242,15 +245,16 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
       tmem_st_32x32b_x32(tl + COL_O2 + half * 32, z);
     }
     tc_wait_st();
-    float eC_next = __ldg(efh + (C - 1));
+    float eC_next = __ldg(efh + (int64_t)c0 * HV * C + (C - 1));
     bool ok = true;
-    for (int c = 0; c < nch; ++c) {
-      const int st = c & 1;
+    for (int i = 0; i < ncl; ++i) {
+      const int c = c0 + i;
+      const int st = i & 1;
       // exp(g_C) of this chunk; the next chunk's is fetched now, its latency hidden by the chunk
       const float eC = eC_next;
-      if (c + 1 < nch) eC_next = __ldg(efh + (int64_t)(c + 1) * HV * C + (C - 1));
-      ok = ok && mbar_wait(bar_fa + 8 * st, (c >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
-      ok = ok && (c == 0 || mbar_wait(bar_s, (c - 1) & 1, status, DEV_TIMEOUT_EPILOGUE));
+      if (i + 1 < ncl) eC_next = __ldg(efh + (int64_t)(c + 1) * HV * C + (C - 1));
+      ok = ok && mbar_wait(bar_fa + 8 * st, (i >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
+      ok = ok && (i == 0 || mbar_wait(bar_s, (i - 1) & 1, status, DEV_TIMEOUT_EPILOGUE));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
       float up[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) up[j] = us[j * D];
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)i & 1, status, DEV_TIMEOUT_EPILOGUE));
       if (!ok) break;
       tc_fence_after();
       // U = U' - W S0^T (rows past the request's end have W = U' = 0 from the zero-filled
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     }
     if (ok && s_out) {
       // the state after the last chunk
-      if (mbar_wait(bar_s, (nch - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
+      if (mbar_wait(bar_s, (ncl - 1) & 1, status, DEV_TIMEOUT_EPILOGUE)) {
         tc_fence_after();
         float* dst = s_out + (((int64_t)b * HV + h) * D + v) * D;
 #pragma unroll 1
@@ -331,16 +335,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     // staging [64 tok][32 v] fp16 for this warp's 32 value rows
     const uint32_t stg = sb + OFF_EPI + quarter * EPI_BYTES;
     // exp(g) of the chunk's rows: lane j holds rows j and 32 + j (fetched one chunk ahead)
-    float fa_next = __ldg(efh + lane), fb_next = __ldg(efh + 32 + lane);
+    const float* efc = efh + (int64_t)c0 * HV * C;
+    float fa_next = __ldg(efc + lane), fb_next = __ldg(efc + 32 + lane);
     bool ok = true;
-    for (int c = 0; c < nch; ++c) {
+    for (int i = 0; i < ncl; ++i) {
+      const int c = c0 + i;
       const float fa = fa_next * inv_sqrt_d, fb = fb_next * inv_sqrt_d;
-      if (c + 1 < nch) {
+      if (i + 1 < ncl) {
         fa_next = __ldg(efh + (int64_t)(c + 1) * HV * C + lane);
         fb_next = __ldg(efh + (int64_t)(c + 1) * HV * C + 32 + lane);
       }
       // O1 is complete with [U | O1]: read and scale it while U is converted and S updated
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_u, (uint32_t)i & 1, status, DEV_TIMEOUT_EPILOGUE));
       if (!ok) break;
       tc_fence_after();
       float fo[64];
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         for (int j = 0; j < 32; ++j) fo[32 + j] = __shfl_sync(0xffffffffu, fb, j) * u2f(o1[j]);
       }
       // O2 with [S | O2]; O = exp(g)/sqrt(128) O1 + O2, kept as fp16 pairs
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)c & 1, status, DEV_TIMEOUT_EPILOGUE));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)i & 1, status, DEV_TIMEOUT_EPILOGUE));
       if (!ok) break;
       tc_fence_after();
       uint32_t y[32];
@@ -414,7 +420,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
 
 clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W, const float* U1,
                              const __half* Aqk, const float* ef, const float* s0, float* s_out,
-                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream) {
+                             __half* out, int64_t ldo, int64_t B, int64_t L, cudaStream_t stream,
+                             int64_t c0, int64_t ncl) {
   using namespace gdn;
   if (B == 0 || L == 0) return CLEF_OK;
   if ((ldo % 8) != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) {
@@ -422,6 +429,8 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
     return CLEF_E_ALIGN;
   }
   const int64_t nch = (L + C - 1) / C;
+  if (ncl < 0) ncl = nch - c0;
+  if (c0 < 0 || ncl < 1 || c0 + ncl > nch) return CLEF_E_INVALID;
   static bool attr = false;
   if (!attr) {
     CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn_state_tc_kernel,
@@ -453,12 +462,14 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
                    CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
       return CLEF_E_CUDA;
   }
-  const double Cd = C, Dd = D, chunks = (double)B * nch * HV;
+  const double Cd = C, Dd = D, chunks = (double)B * ncl * HV;
   TraceScope ts(stream, "gdn_state_pass", chunks * (6.0 * Cd * Dd * Dd + 2.0 * Cd * Cd * Dd),
-                (double)B * L * HV * D * (2 + 2 + 4 + 2) + (double)B * L * HK * D * 2 +
-                    chunks * Cd * Cd * 2);
+                // per (chunk, value head): W, Kd, U', out rows (2 + 2 + 4 + 2 bytes x D), its
+                // share of the q rows (a key head serves two value heads), Aqk^T
+                chunks * Cd * (Dd * (2 + 2 + 4 + 2) + Dd * 2.0 * HK / HV + Cd * 2));
   gdn_state_tc_kernel<<<(unsigned)(B * HV), ST_THREADS, ST_SMEM, stream>>>(
-      tW, tQ, tKd, tA, tO, U1, ef, s0, s_out, (int)L, (int)nch, status_word_ptr());
+      tW, tQ, tKd, tA, tO, U1, ef, s0, s_out, (int)L, (int)nch, (int)c0, (int)ncl,
+      status_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

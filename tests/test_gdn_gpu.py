@@ -108,3 +108,23 @@ def test_scan_deterministic():
     a = run_gpu(q, k, v, alpha, beta)
     b = run_gpu(q, k, v, alpha, beta)
     assert torch.equal(a, b)
+
+
+# A scan of one or two requests with at least 64 chunks runs in pieces (the chunk phase of the
+# next piece overlapping the state pass of this one, on two streams); three requests run in one
+# pass.  The state crosses pieces in fp32, exactly as it stays in tensor memory in one pass, so the
+# same request must come out bit for bit the same either way, with or without an entering state.
+@pytest.mark.parametrize("L,with_s0", [(4096, False), (8192, True), (4150, True)])
+def test_pieces_equal_one_pass(L, with_s0):
+    q, k, v, alpha, beta = scan_inputs(L + int(with_s0), 1, L)
+    s0 = synth.normal_f32(L, "gdn.s0p", 0, (1, 32, 128, 128), 0.0, 0.3) if with_s0 else None
+    rep = lambda a: np.concatenate([a, a, a], axis=0)  # noqa: E731
+    o1, S1 = run_gpu(q, k, v, alpha, beta, s0=s0, want_state=True)
+    o3, S3 = run_gpu(rep(q), rep(k), rep(v), rep(alpha), rep(beta),
+                     s0=None if s0 is None else rep(s0), want_state=True)
+    assert torch.equal(o1[0], o3[0]) and torch.equal(o1[0], o3[2])
+    assert torch.equal(S1[0], S3[0])
+    # and against the recurrence on the first 256 positions (their own prefix)
+    o_ref, _ = Lr.gated_delta_rule(q[0, :256], k[0, :256], v[0, :256], alpha[0, :256], beta[0, :256],
+                                   s0=None if s0 is None else s0[0])
+    assert rel_rmse(o1[0, :256].double().cpu().numpy(), o_ref) < TOL
