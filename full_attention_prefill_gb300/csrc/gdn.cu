@@ -523,8 +523,8 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t L, bool with_norm) {
   n += al256g(rows * gdn::HV * gdn::D * 4);              // U'
   n += al256g(rows * gdn::HV * gdn::D * 2);              // decayed keys
   n += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);  // Aqk
-  if (with_norm) n += al256g(M * gdn::HV * gdn::D * 2);  // o before the output gate
   if (gdn_pieces(B, L) > 1) n += al256g(B * gdn::HV * gdn::D * gdn::D * 4);   // carried state
+  if (with_norm) n += al256g(M * gdn::HV * gdn::D * 2);  // o before the output gate (last)
   return n;
 }
 
@@ -550,8 +550,14 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   w.U1 = reinterpret_cast<float*>(p); p += al256g(rows * gdn::HV * gdn::D * 4);
   w.Kt = reinterpret_cast<__half*>(p); p += al256g(rows * gdn::HV * gdn::D * 2);
   w.Aqk = reinterpret_cast<__half*>(p); p += al256g(B * nch * gdn::HV * gdn::C * gdn::C * 2);
-  w.o = reinterpret_cast<__half*>(p); p += al256g(M * gdn::HV * gdn::D * 2);
-  w.state = reinterpret_cast<float*>(p);   // only when the scan runs in pieces
+  // same order as gdn_scan_workspace_bytes: the carried state only when the scan runs in pieces,
+  // o (only with the gated norm) last
+  w.state = nullptr;
+  if (gdn_pieces(B, L) > 1) {
+    w.state = reinterpret_cast<float*>(p);
+    p += al256g(B * gdn::HV * gdn::D * gdn::D * 4);
+  }
+  w.o = reinterpret_cast<__half*>(p);
   return w;
 }
 
@@ -678,6 +684,18 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
       st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, p == 0 ? s0 : s_eff, s_eff, o,
                             ldo_pass, B, L, ss->hi, c0, c1 - c0);
       if (st != CLEF_OK) return st;
+      if (z) {
+        // the z-gated norm of this piece's rows, in the state stream's wait for the next
+        // chunk phase
+        const int64_t t0 = c0 * gdn::C, t1 = std::min<int64_t>(c1 * gdn::C, L);
+        for (int64_t b = 0; b < B; ++b) {
+          const int64_t r0 = b * L + t0;
+          TraceScope ts(ss->hi, "gdn_gated_norm", 0.0, (double)(t1 - t0) * 4096 * 2 * 3);
+          gdn::gdn_gated_norm_kernel<<<(unsigned)(t1 - t0), 256, 0, ss->hi>>>(
+              o + r0 * ldo_pass, z + r0 * ldz, ldz, o_norm, out + r0 * ldo, ldo);
+          CLEF_LAUNCH_CHECK();
+        }
+      }
     }
     // join
     CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + pieces], ss->hi));
@@ -685,7 +703,7 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[1 + pieces], 0));
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[2 + pieces], 0));
   }
-  if (z) {
+  if (z && pieces <= 1) {
     TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);
     gdn::gdn_gated_norm_kernel<<<(unsigned)M, 256, 0, stream>>>(o, z, ldz, o_norm, out, ldo);
     CLEF_LAUNCH_CHECK();

@@ -124,6 +124,9 @@ def test_pieces_equal_one_pass(L, with_s0):
                      s0=None if s0 is None else rep(s0), want_state=True)
     assert torch.equal(o1[0], o3[0]) and torch.equal(o1[0], o3[2])
     assert torch.equal(S1[0], S3[0])
+    # without a state output the pieces carry the state through the workspace's scratch
+    o0 = run_gpu(q, k, v, alpha, beta, s0=s0, want_state=False)
+    assert torch.equal(o0[0], o1[0])
     # and against the recurrence on the first 256 positions (their own prefix)
     o_ref, _ = Lr.gated_delta_rule(q[0, :256], k[0, :256], v[0, :256], alpha[0, :256], beta[0, :256],
                                    s0=None if s0 is None else s0[0])

@@ -41,7 +41,8 @@ def run_layer(layer_index, L, B=1, seed=0):
         assert e_delta < DELTA_TOL
 
 
-@pytest.mark.parametrize("L,B", [(1024, 1), (70, 2)])
+# (4096, 1): the scan runs in pieces on two streams, with the z-gated norm per piece
+@pytest.mark.parametrize("L,B", [(1024, 1), (70, 2), (4096, 1)])
 def test_gdn_layer(L, B):
     run_layer(0, L, B)
 
