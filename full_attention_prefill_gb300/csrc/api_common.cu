@@ -166,7 +166,7 @@ extern "C" {
 
 const char* clef_last_error(void) { return g_err; }
 
-int32_t clef_version(void) { return (1 << 16) | 0; }
+int32_t clef_version(void) { return (1 << 16) | 1; }
 
 clef_status clef_trace_begin(void) {
   std::lock_guard<std::mutex> lock(g_trace_mu);

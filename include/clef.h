@@ -75,7 +75,8 @@ typedef void* clef_stream; /* a cudaStream_t */
 /* Message of the last failing call on this thread ("" if none). */
 CLEF_API const char* clef_last_error(void);
 
-/* ABI version: (major << 16) | minor. */
+/* ABI version: (major << 16) | minor.  1.1 adds the chunked prefill with carried state, the
+   LUT-6 quantiser and the picture prefill with M-RoPE to 1.0; nothing of 1.0 changed. */
 CLEF_API int32_t clef_version(void);
 
 /* ------------------------------------------------------------------------------------------
