@@ -58,10 +58,15 @@ struct Smem {
   uint32_t wcnt[THREADS / 32];          // scan scratch
   long long wsum[THREADS / 32];
   double xval[2 * (TS / 2) + 2];        // order statistics for the seeds
+  uint32_t pcnt[TS];                    // the (count, sum) each centroid was last computed from
+  long long psum[TS];                   // (count ~0: none, or its slot has changed since)
   uint16_t tkey[TS];                    // final thresholds
   uint8_t first[TS];                    // first index of each run of equal table values
   int nonfinite;
 };
+
+// three CTAs per SM: 233,472 bytes of shared memory per SM, 1 KB reserved per CTA
+static_assert(sizeof(Smem) + 1024 <= 233472 / 3, "three CTAs per SM");
 
 // ---- keys ----
 __device__ __forceinline__ uint32_t key_of(uint32_t h) {
@@ -86,16 +91,41 @@ __device__ __forceinline__ long long key_step(uint32_t key0) {
 __device__ __forceinline__ double key_value(uint32_t key) {
   return (double)__half2float(__ushort_as_half((unsigned short)bits_of(key)));
 }
-// The first key whose value is above b.  r = fp16(b) is b itself or one of its two fp16
-// neighbours, so the answer is r's key or the next one; -0 and +0 share one value.
+// The first key whose value is above b (|b| <= 65504), from the bits of b with integer
+// operations only: t = the largest fp16 magnitude <= |b| (the significand cut to 10 bits, or to
+// units of 2^-24 below 2^-14), exact when nothing was cut.  b > 0: the key after +t.  b < 0: the
+// key of -t (its value is above b) unless -t == b, then the one after; -0 and +0 share one value.
 __device__ __forceinline__ uint32_t first_key_above(double b) {
-  const __half r = __double2half(b);
-  const uint32_t h = __half_as_ushort(r);
-  const double vr = (double)__half2float(r);
-  if (vr > b) return vr == 0.0 ? 0x7FFFu : key_of(h);
-  uint32_t key = key_of(h) + 1u;
-  if (key == 0x8000u) key = 0x8001u;
-  return key;
+  const unsigned long long bits = (unsigned long long)__double_as_longlong(b);
+  const unsigned long long m52 = bits & ((1ull << 52) - 1);
+  const int ebits = (int)((bits >> 52) & 0x7FF);
+  if (ebits == 0 && m52 == 0) return 0x8001u;
+  const int E = ebits - 1023;
+  uint32_t t;
+  bool exact;
+  if (E >= -14) {
+    if (E > 15) {
+      t = 0x7BFFu;
+      exact = false;
+    } else {
+      t = ((uint32_t)(E + 15) << 10) | (uint32_t)(m52 >> 42);
+      exact = (m52 & ((1ull << 42) - 1)) == 0;
+    }
+  } else {
+    const unsigned long long sig = (1ull << 52) | m52;
+    const int shift = 28 - E;
+    if (shift >= 64) {
+      t = 0;
+      exact = false;
+    } else {
+      t = (uint32_t)(sig >> shift);
+      exact = (sig & ((1ull << shift) - 1)) == 0;
+    }
+  }
+  if (!(bits >> 63)) return t + 0x8000u + 1u;
+  if (t == 0) return 0x7FFFu;
+  const uint32_t k = 0xFFFFu - (0x8000u | t);
+  return exact ? k + 1u : k;
 }
 
 // Integer key ordered like the double x, with -0 and +0 equal (sorting on the fp64 pipe of
@@ -312,6 +342,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 3)
         }
         sm.c[0][pos] = sm.seed[tid];
         sm.okey[0][pos] = o;
+        sm.pcnt[tid] = 0xFFFFFFFFu;
       }
       __syncthreads();
 
@@ -340,13 +371,23 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 3)
           const double cj = c[tid];
           const long long kj = sm.okey[0][tid];
           double out = cj;
+          uint32_t pc = 0xFFFFFFFFu;
+          long long ps = 0;
           if (tid == 0 || sm.okey[0][tid - 1] != kj) {
             int e = tid;
             while (e < TS - 1 && sm.okey[0][e + 1] == kj) ++e;
             const uint32_t cnt = sm.fcnt[e + 1] - sm.fcnt[tid];
             const long long sum = sm.fsum[e + 1] - sm.fsum[tid];
-            if (cnt) out = __dmul_rn(__ddiv_rn(__ll2double_rn(sum), (double)cnt), 0x1p-24);
+            if (cnt) {
+              // the same members as when this centroid was computed give the same bits
+              if (cnt != sm.pcnt[tid] || sum != sm.psum[tid])
+                out = __dmul_rn(__ddiv_rn(__ll2double_rn(sum), (double)cnt), 0x1p-24);
+              pc = cnt;
+              ps = sum;
+            }
           }
+          sm.pcnt[tid] = pc;
+          sm.psum[tid] = ps;
           cn[tid] = out;
           sm.okey[1][tid] = order_key(out);
         }
@@ -360,6 +401,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 3)
             sm.okey[0][tid] = sm.okey[1][tid];
           }
         } else if (tid < TS) {
+          sm.pcnt[tid] = 0xFFFFFFFFu;   // centroids change slots: compute every mean again
           const long long o = sm.okey[1][tid];
           int pos = 0;
           for (int i = 0; i < TS; ++i) {
