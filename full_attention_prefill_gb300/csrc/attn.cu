@@ -1,6 +1,7 @@
 // Causal GQA attention of the gated full-attention layers.
 //
-// "Clef-Flash-ANE-LUT6" model card, "Model architecture": 16 query and 4 key-value heads of 256.
+// "Clef-Flash-ANE-LUT6" model card, "Model architecture": heads of size 256, 16 for queries and
+// 4 shared key/value heads.
 // "clef-flash-LiteRT" README, "Host contract" step 5: rotary with theta = 1e7 and, for text, the
 // position (i, i, i) on all three planes, i.e. a 1-D rotary; "clef-flash-coreml" README: cos/sin
 // tables [L, 64], i.e. 64 rotated dims per head.  "Provenance": grouped keys/values shared by the

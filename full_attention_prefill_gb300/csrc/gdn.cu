@@ -4,8 +4,8 @@
 // README, "Core AI shape": a [32, 128, 128] state per GDN layer), for value head h reading key
 // head h/2:
 //     S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,   o_t = S_t q_t / sqrt(128)
-// is evaluated in chunks of C = 64 positions ("clef-flash-LiteRT" README, "Provenance": the
-// recurrence re-expressed as a chunked kernel of 64 positions).  With g the cumulative
+// is evaluated in chunks of C = 64 positions ("clef-flash-LiteRT" README, "Provenance": there
+// the recurrence is exported in 64-position chunks).  With g the cumulative
 // log(alpha) inside a chunk and S0 the state entering it:
 //     A = strict_tril(diag(beta) (exp(g_r - g_s)) o K K^T),   T = (I + A)^-1
 //     W = T diag(beta exp(g)) K,   U' = T diag(beta) V,   U = U' - W S0^T

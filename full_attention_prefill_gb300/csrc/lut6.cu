@@ -1,8 +1,9 @@
 // LUT-6 weights: host pack/unpack, a dense dequant kernel (parity aid) and the LUT-6 GEMM.
 //
 // Format ("Clef-Flash-ANE-LUT6" model card, sections "Weight precision" and "LUT-6 text
-// weights"): 6-bit indices, one 64-entry fp16 table per 16 output channels, four indices packed
-// into three bytes as one little-endian (LSB-first) bit stream, rows of W in order, k fastest.
+// weights"): a 6-bit index per weight, an fp16 table of 64 values for each block of 16 output
+// channels, 4 indices to 3 bytes as one little-endian (LSB-first) bit stream, rows of W in
+// order, k fastest.
 //
 // GEMM design (sm_103a): Y[m, n] = sum_k X[m, k] * T[n/16][idx[n, k]], computed as the
 // transposed product D[n, m] = W X^T so that the weights are the MMA's A operand, held in tensor

@@ -1,7 +1,7 @@
-// LUT-6 quantiser: fp16 weight W [n, k] -> packed 6-bit indices + one 64-entry fp16 table per 16
-// output channels ("Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": 40 rounds of
-// one-dimensional k-means per 16-row group, half of the 64 seeds quantiles of the group, half
-// spread evenly between its minimum and maximum).
+// LUT-6 quantiser: fp16 weight W [n, k] -> packed 6-bit indices + an fp16 table of 64 values for
+// each block of 16 output channels ("Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": per 16-row
+// group, 40 k-means iterations in one dimension from 64 initial centroids, 32 quantiles of the
+// group and 32 equal steps from its smallest to its largest weight).
 //
 // GB300 design.  Every fp16 value maps to a 16-bit key that orders like the value (negative
 // patterns reversed below the positive ones), so a group's weights are summarised exactly by a

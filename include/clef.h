@@ -5,10 +5,10 @@
  * architecture"): 32 layers of hidden size 4,096 and MLP size 12,288; 24 Gated DeltaNet layers
  * (16 key / 32 value heads of 128) and 8 gated full-attention layers (16 query / 4 kv heads of
  * 256), full attention every fourth layer.  Every large linear is LUT-6 (section "LUT-6 text
- * weights"): 6-bit indices, one 64-entry FP16 table per 16 output channels, four indices in
- * three bytes.  One call of clef_prefill_forward is one single prefill: token ids in, the
- * final-norm hidden state at every position out ("clef-flash-LiteRT" README, section "Host
- * contract", steps 3-6; no state carries over between calls).
+ * weights"): a 6-bit index per weight, an fp16 table of 64 values for each block of 16 output
+ * channels, 4 indices to 3 bytes.  One call of clef_prefill_forward is one single prefill: token
+ * ids in, every position's output of the final RMSNorm out ("clef-flash-LiteRT" README, section "Host
+ * contract", steps 3-6; each call starts from an empty state).
  *
  * Conventions of every entry point:
  *   - All buffers are owned by the caller.  The library never allocates device memory; calls
@@ -111,9 +111,9 @@ CLEF_API clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k,
 
 /* device: quantise an fp16 weight w [n, k] (row-major, k fastest) into the LUT-6 format above:
    packed [n, k*3/4] (the row-major bit stream of clef_lut6_pack) and lut [n/16, 64] fp16
-   ("Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": per 16-row group a 64-value
-   table from 40 rounds of one-dimensional k-means, seeded with 32 quantiles of the group and 32
-   values spread evenly from its minimum to its maximum).  Arithmetic, fixed so that the result
+   ("Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": per 16-row group, 40 k-means
+   iterations in one dimension from 64 initial centroids, 32 quantiles of the group and 32 equal
+   steps from its smallest to its largest weight).  Arithmetic, fixed so that the result
    is one exact function of w: quantile i (p = (i + 1/2) / 32) interpolates linearly between the
    order statistics around p (n - 1); spread value i is min + i * ((max - min) / 31), the last
    one max; each round sends a weight to the nearest centroid (cells between midpoints
@@ -236,8 +236,8 @@ typedef struct {
    positions. */
 CLEF_API size_t clef_prefill_workspace_size(int64_t B, int64_t L);
 
-/* device: the hybrid prefill.  ids [B, L] int32 (device) -> hidden [B, L, 4096] fp16, the hidden
-   states after the final RMSNorm at every position.  B independent requests of L positions each
+/* device: the hybrid prefill.  ids [B, L] int32 (device) -> hidden [B, L, 4096] fp16, the final
+   RMSNorm's output for each position.  B independent requests of L positions each
    (right-padded to a bucket by the caller: padding rows are computed like real tokens and, by
    causality, never change the real rows).  1 <= L <= CLEF_MAX_LEN (CLEF_E_TOO_LONG above),
    B >= 1.  Ids outside [0, vocab) set CLEF_E_BAD_TOKEN in the device status (their rows are
@@ -247,8 +247,8 @@ CLEF_API clef_status clef_prefill_forward(const clef_model* model, const int32_t
                                  clef_stream stream);
 
 /* M-RoPE positions of one request of L tokens holding at most one picture block
-   ("clef-flash-LiteRT" README, "Host contract" step 5: three planes, theta = 1e7, a text token at
-   index i has position (i, i, i), picture tokens take their row and column in the grid;
+   ("clef-flash-LiteRT" README, "Host contract" step 5: three planes, theta = 1e7; text tokens sit
+   at (i, i, i) for their index i, picture tokens at their grid row and column;
    "clef-flash - Core AI" README, "Core AI shape": image token k at row k / W, column k % W, and
    from the <|vision_end|> index image_start + N on the positions move back by N - max(H, W)).
    host: pos3 [L][3] int32 (t, h, w), caller owned: image token k (index image_start + k,

@@ -36,7 +36,7 @@ def rmsnorm(x, w, eps=RMS_EPS):
     """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * w.
 
     "Clef-Flash-ANE-LUT6" §Weight precision lists normalization weights among the FP16 text
-    weights; "clef-flash-LiteRT" §Host contract step 6 returns the hidden states after the final
+    weights; "clef-flash-LiteRT" §Host contract step 6 returns the output of the final
     RMSNorm.  eps = 1e-6 and the plain x * r * w form are the adopted reading (no page gives them).
     """
     x = f64(x)
@@ -76,8 +76,8 @@ def causal_conv_silu(x, w):
 def gdn_gates(a, b, A_log, dt_bias):
     """Per-value-head decay and write strength of the Gated DeltaNet.
 
-    "Clef-Flash-ANE-LUT6" §Weight precision lists the small gate projections and decay
-    parameters (FP16).  Adopted reading (standard Gated DeltaNet gating):
+    "Clef-Flash-ANE-LUT6" §Weight precision keeps the gates' projection weights and the decay
+    parameters in FP16.  Adopted reading (standard Gated DeltaNet gating):
       alpha = exp(-exp(A_log) * softplus(a + dt_bias)),  beta = sigmoid(b).
     a, b: [L, Hv];  A_log, dt_bias: [Hv].
     """
@@ -130,7 +130,7 @@ def rope(x, positions, rot_dims=ROPE_DIMS, theta=ROPE_THETA):
     """Rotary embedding on the first `rot_dims` dims of each head (rotate-half pairing).
 
     "clef-flash-coreml" README: decoder parts take cos/sin [L, 64]; "clef-flash-LiteRT" §Host
-    contract step 5: theta = 1e7 and a text token at index i has position (i, i, i), so the three
+    contract step 5: theta = 1e7 and text tokens sit at (i, i, i) for their index i, so the three
     M-RoPE planes collapse to one 1-D rotary.  Pairs (j, j + 32) for j < 32 rotate by angle
     pos * theta^(-2j/64); dims 64.. pass through.  x: [L, H, D]; positions: [L].
     """
@@ -162,9 +162,9 @@ def mrope_planes(rot_dims=ROPE_DIMS):
 def mrope_positions(L, image_start=0, grid_h=0, grid_w=0):
     """[L, 3] integer positions (t, h, w) of a request holding at most one picture block.
 
-    "clef-flash-LiteRT" §Host contract step 5: a text token at index i has position (i, i, i),
-    a picture's tokens take their row and column in the picture's grid, padding continues the
-    positions.  "clef-flash - Core AI" §Core AI shape: image token k sits at row k // W, column
+    "clef-flash-LiteRT" §Host contract step 5: text tokens sit at (i, i, i) for their index i,
+    picture tokens at their row and column of the picture's grid, and padding goes on from the
+    last position.  "clef-flash - Core AI" §Core AI shape: image token k sits at row k // W, column
     k % W, and from the <|vision_end|> index (picture start + N) on the positions move back by
     N - max(H, W).  Reading (the plainest one those numbers allow): image token k at index s + k
     has (s, s + k // W, s + k % W), so the token after the block continues at s + max(H, W), one

@@ -1,9 +1,9 @@
 """LUT-6 weight format, oracle side (numpy; integer work exact, products in float64).
 
 Source: "Clef-Flash-ANE-LUT6" model card, §Weight precision and §LUT-6 text weights:
-every large linear keeps 6-bit indices, one 64-entry FP16 table per 16 output channels, and four
-6-bit indices are packed into three bytes in a little-endian layout; with the tables a
-4,096-input layer costs about 6.02 bits per weight.
+each large linear stores a 6-bit index per weight and an fp16 table of 64 values for each block
+of 16 output channels, 4 indices to 3 bytes in the little-endian order Core ML uses; tables included,
+a layer with 4,096 inputs comes to about 6.02 bits per weight.
 
 Reading of "little-endian" (the page gives no byte dump): the indices form one LSB-first bit
 stream over the weight matrix in row-major order (input index k fastest).  Indices i0..i3 of a

@@ -107,11 +107,10 @@ def is_attention_layer(layer: int) -> bool:
 def prefill(ids, embed_rows, layer_weights, final_norm, n_layers=32, positions=None):
     """The hybrid prefill of one request: ids [L] -> final-norm hidden [L, 4096] (float64).
 
-    "clef-flash-LiteRT" §Host contract steps 4-6: embedding rows at the request's ids in, the
-    hidden states after the final RMSNorm at every position out, no state carried between
-    calls.  `embed_rows` is [L, 4096] (the table's rows at `ids`, gathered by the caller);
+    "clef-flash-LiteRT" §Host contract steps 4-6: embedding rows at the request's ids in, every
+    position's output of the final RMSNorm out, each call from an empty state.  `embed_rows` is [L, 4096] (the table's rows at `ids`, gathered by the caller);
     `layer_weights(l)` returns layer l's weight dict.  A request with a picture passes the
-    picture's rows in place of the table's rows at its <|image_pad|> positions (step 4) and its
+    picture's rows in place of the table's rows where its <|image_pad|> tokens sit (step 4) and its
     M-RoPE positions ([L, 3], :func:`oracle.layers.mrope_positions`; step 5).
     """
     x = Lr.f64(embed_rows)

@@ -1,9 +1,9 @@
 """LUT-6 quantiser, oracle side (numpy, float64 with exact integer sums).  Test infrastructure only.
 
-Source: "Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": each group of 16 output
-channels gets its own 64-value table, found by 40 rounds of one-dimensional k-means; half of the
-starting values are quantiles of the group's weights, the other half are spread evenly between
-the group's minimum and maximum.
+Source: "Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": a 64-entry table per 16
+output channels, fitted by k-means in one dimension for 40 iterations, whose initial centroids are
+32 quantiles of the channels' weights and 32 points at equal steps from their smallest to their
+largest weight.
 
 Readings where the card is silent (each is a plain choice the rest of the card allows):
   * quantiles: the 32 probabilities (i + 1/2) / 32, i = 0..31, each taken between the two
@@ -11,7 +11,7 @@ Readings where the card is silent (each is a plain choice the rest of the card a
     h = p (n - 1), lo = floor(h), f = h - lo.  For fp16 weights every step is exact in float64;
   * evenly spread: min + i * step, step = (max - min) / 31, i = 0..30, rounded after the
     division, the product and the sum; the 32nd value is max itself;
-  * the 64 starting values (quantiles first, then the spread values) are sorted ascending by a
+  * the 64 initial centroids (quantiles first, then the equal-step points) are sorted ascending by a
     stable sort, so equal values (-0 and +0 among them) keep that order.  After every round the
     centroids are sorted again the same way: equal seeds share their members with the first of
     them, which moves while the others stay, so order is not kept by itself.  Sorting changes

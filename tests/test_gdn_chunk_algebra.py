@@ -1,7 +1,7 @@
 """The chunked (WY) form of the gated delta rule equals the per-token recurrence (CPU, fp64).
 
-The CUDA scan evaluates the recurrence chunk by chunk ("clef-flash-LiteRT" §Provenance: the
-GatedDeltaNet recurrence re-expressed as a chunked kernel of 64 positions).  This test writes the
+The CUDA scan evaluates the recurrence chunk by chunk ("clef-flash-LiteRT" §Provenance: there the
+GatedDeltaNet recurrence is exported in 64-position chunks).  This test writes the
 chunk algebra out in numpy and checks it against the oracle's token-by-token recurrence for
 chunk widths 1, 16 and 64 (width 1 reduces the chunk algebra to the recurrence itself).
 

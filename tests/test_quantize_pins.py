@@ -1,8 +1,8 @@
 """Pins of the LUT-6 quantiser oracle (CPU).
 
-"Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": one 64-value table per 16 output
-channels, 40 rounds of one-dimensional k-means, half the seeds quantiles and half spread evenly
-between the group's minimum and maximum.  The oracle is pinned to things outside itself: numpy's
+"Clef-Flash-ANE-LUT6" model card, section "LUT-6 text weights": a 64-entry table per 16 output
+channels, 40 k-means iterations in one dimension, initial centroids 32 quantiles and 32 equal
+steps from the smallest to the largest weight.  The oracle is pinned to things outside itself: numpy's
 own quantile and linspace, exact rational arithmetic (Python fractions) for nearest centroids,
 means and a whole brute-force k-means on small groups, special cases with known answers, the
 k-means descent invariant, and the Panter-Dite high-resolution distortion of a Gaussian source.
