@@ -83,6 +83,8 @@ _SIGS = {
     "clef_last_error": (ctypes.c_char_p, []),
     "clef_version": (ctypes.c_int32, []),
     "clef_debug_fail_next": (None, [ctypes.c_int32]),
+    "clef_debug_gdn_workspace_layout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                                       ctypes.c_void_p, ctypes.c_void_p]),
     "clef_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
     "clef_lut6_pack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "clef_lut6_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),

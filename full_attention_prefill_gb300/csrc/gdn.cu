@@ -712,3 +712,20 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
 }
 
 }  // namespace clef
+
+// Host only: where the scan's workspace regions start (bytes from the workspace base), for
+// checking the carving against the size query without a GPU.
+extern "C" clef_status clef_debug_gdn_workspace_layout(int64_t B, int64_t L, int32_t with_norm,
+                                                       int64_t* offsets, int64_t* total) {
+  using namespace clef;
+  if (!offsets || !total || B < 1 || L < 1) return CLEF_E_INVALID;
+  uint8_t* const base = reinterpret_cast<uint8_t*>(uintptr_t(1) << 20);   // never dereferenced
+  const GdnWs w = carve(base, B, L);
+  const void* regions[8] = {w.g, w.ef, w.W, w.U1, w.Kt, w.Aqk, w.state, w.o};
+  for (int i = 0; i < 8; ++i)
+    offsets[i] = regions[i] ? (int64_t)(static_cast<const uint8_t*>(regions[i]) - base) : -1;
+  if (!with_norm) offsets[7] = -1;
+  *total = (int64_t)gdn_scan_workspace_bytes(B, L, with_norm != 0);
+  return CLEF_OK;
+}
+

@@ -342,6 +342,15 @@ CLEF_API clef_status clef_trace_end(clef_trace_entry* entries, int32_t max_entri
    with CLEF_E_CUDA before launching anything.  Affects the calling process only. */
 CLEF_API void clef_debug_fail_next(int32_t n_calls);
 
+/* Host only, no device call: the byte offsets from the workspace base at which the gated delta
+   rule scan (clef_gdn_prefill, and each GDN layer of the prefill with with_norm = 1) places its
+   regions for B requests of L positions, in the order g, exp(g), W, U', decayed keys, Aqk^T,
+   carried state (only when the scan runs in pieces), o (only with_norm); -1 for a region not
+   used.  offsets: 8 int64, caller owned; *total = the workspace bytes the scan needs.  For tests
+   of the carving against the size query.  CLEF_E_INVALID for NULL outputs or B, L < 1. */
+CLEF_API clef_status clef_debug_gdn_workspace_layout(int64_t B, int64_t L, int32_t with_norm,
+                                                     int64_t* offsets, int64_t* total);
+
 #ifdef __cplusplus
 }
 #endif

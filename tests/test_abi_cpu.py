@@ -90,3 +90,31 @@ def test_host_mrope_positions_errors(lib):
     with pytest.raises(clef.ClefError) as e:
         clef.mrope_positions(40, 0, (2, 0))           # half a grid
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 32])
+@pytest.mark.parametrize("L", [1, 64, 1024, 4095, 4096, 4150, 8192, 16384])
+def test_gdn_workspace_regions_fit(lib, B, L):
+    """The scan's workspace carving stays inside the size it reports and no regions overlap, for
+    every shape class (one pass, pieces with the carried-state scratch, with and without the
+    gated norm's o).  A mismatch of the two once let a pieced scan write past its workspace."""
+    nch, M = -(-L // 64), B * L
+    sizes = [M * 32 * 4,                      # g
+             B * nch * 32 * 64 * 4,           # exp(g)
+             B * nch * 64 * 32 * 128 * 2,     # W
+             B * nch * 64 * 32 * 128 * 4,     # U'
+             B * nch * 64 * 32 * 128 * 2,     # decayed keys
+             B * nch * 32 * 64 * 64 * 2,      # Aqk^T
+             B * 32 * 128 * 128 * 4,          # carried state
+             M * 32 * 128 * 2]                # o
+    for with_norm in (0, 1):
+        offs = (ctypes.c_int64 * 8)()
+        total = ctypes.c_int64()
+        assert lib.clef_debug_gdn_workspace_layout(B, L, with_norm, offs, ctypes.byref(total)) == 0
+        regions = sorted((o, sz) for o, sz in zip(offs, sizes) if o >= 0)
+        for o, sz in regions:
+            assert 0 <= o and o + sz <= total.value, (B, L, with_norm, o, sz, total.value)
+        for (a, sa), (b, _) in zip(regions, regions[1:]):
+            assert a + sa <= b
+        assert (offs[6] >= 0) == (B <= 2 and nch >= 64)     # the scan runs in pieces
+        assert (offs[7] >= 0) == bool(with_norm)
