@@ -20,7 +20,9 @@
 //                   O = exp(g) Q S0^T / sqrt(128) + Aqk U, all on tcgen05
 //   gdn_gated_norm  (decoder layer only): y = RMSNorm_128(O) * w_o * SiLU(z)
 // The chunk phase's products run on mma.sync (m16n8k16, fp16 inputs, fp32 accumulation); the
-// state and the scalars stay fp32.
+// state and the scalars stay fp32.  A long scan of one or two requests runs in pieces of chunks:
+// the chunk phase of the next piece on a low-priority stream beside the state pass of this one
+// on a high-priority stream (events order them; the state crosses pieces in fp32).
 #include <algorithm>
 #include <mutex>
 

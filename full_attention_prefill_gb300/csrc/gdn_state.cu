@@ -8,6 +8,8 @@
 //     S  <- exp(g_C) S + U^T Kd                 (Kd = exp(g_C - g) K, the decayed keys)
 // W, U', Kd, Aqk and exp(g) come from the parallel chunk phase.  Only U and S depend on the
 // previous chunk, so the pass is a chain of two products per chunk; the O products hang off it.
+// One launch walks a range of chunks (all of them, or one piece of a pieced scan), entering from
+// s0 and leaving the state in s_out.
 //
 // Everything transposed so that the 128 value rows are the MMA's M dimension (TMEM lanes), and
 // the products that share an A operand merged into one MMA chain:
