@@ -371,3 +371,43 @@ def test_lut_model_mixers_are_causal():
         moved = mixer(x2, w)
         np.testing.assert_array_equal(moved[:6], full[:6])
         assert np.abs(moved[6:] - full[6:]).max() > 1e-3
+
+
+def _const_lut6(n, k, value, seed):
+    """A LUT-6 weight whose every entry is `value` (random indices into a constant table)."""
+    rng = np.random.default_rng(seed)
+    packed = rng.integers(0, 256, size=(n, k * 3 // 4), dtype=np.uint8)
+    return packed, np.full((n // 16, 64), value, dtype=np.float16)
+
+
+def test_swiglu_mlp_closed_form():
+    """Constant weights gate = a, up = b, down = d give y_i = d * I * silu(a s) * b s with s the
+    row sum of x: swapped gate/up operands or a missing SiLU factor would fail."""
+    a, b, d, H, I = 0.25, -0.5, 0.125, 32, 48
+    w = {"gate": _const_lut6(I, H, a, 1), "up": _const_lut6(I, H, b, 2),
+         "down": _const_lut6(H, I, d, 3)}
+    x = np.random.default_rng(4).standard_normal((5, H))
+    s = x.sum(axis=1)
+    expect = d * I * (a * s / (1 + np.exp(-a * s))) * (b * s)
+    got = model.swiglu_mlp(x, w)
+    assert np.allclose(got, np.repeat(expect[:, None], H, axis=1), rtol=1e-12, atol=0)
+
+
+def test_decoder_layer_is_prenorm_residual():
+    """A GDN layer whose mixer weights are zero is x + mlp(rmsnorm(x) * w_mlp): the residual
+    carries x unchanged, and the MLP reads the normalised stream (the pre-norm block)."""
+    import synth
+    w = synth.gdn_layer_weights(5, 0)
+    for name in ("qkv", "z", "out"):
+        packed, lut = w[name]
+        w[name] = (packed, np.zeros_like(lut))
+    a, b, d = 2.0 ** -5, 2.0 ** -6, 2.0 ** -7          # exact in the fp16 tables
+    w["gate"] = _const_lut6(12288, 4096, a, 6)
+    w["up"] = _const_lut6(12288, 4096, b, 7)
+    w["down"] = _const_lut6(4096, 12288, d, 8)
+    x = synth.normal_f16(5, "x", 0, (3, 4096)).astype(np.float64)
+    got = model.decoder_layer(x, w, attention=False)
+    xn = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + 1e-6) * w["mlp_norm"].astype(np.float64)
+    s = xn.sum(axis=1)
+    mlp = d * 12288 * (a * s / (1 + np.exp(-a * s))) * (b * s)
+    assert np.allclose(got, x + mlp[:, None], rtol=1e-10, atol=1e-12)
