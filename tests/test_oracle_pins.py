@@ -411,3 +411,23 @@ def test_decoder_layer_is_prenorm_residual():
     s = xn.sum(axis=1)
     mlp = d * 12288 * (a * s / (1 + np.exp(-a * s))) * (b * s)
     assert np.allclose(got, x + mlp[:, None], rtol=1e-10, atol=1e-12)
+
+
+def test_attention_output_gate_closed_form():
+    """Zero query/key weights make the causal softmax uniform (row t averages v over 0..t); with
+    constant v = c_v, gate block (Q-proj rows 4096..8191) = c_g and O-proj = c_o, output row t is
+    c_o * 4096 * c_v * mean_{p<=t} s_p * sigmoid(c_g * s_t), s the row sum of x.  Taking the gate
+    from the first half of the Q-proj, or dropping the sigmoid, fails."""
+    c_v, c_g, c_o = 2.0 ** -6, 2.0 ** -4, 2.0 ** -9                 # exact in the fp16 tables
+    rng = np.random.default_rng(9)
+    q_packed = rng.integers(0, 256, size=(8192, 3072), dtype=np.uint8)
+    q_lut = np.zeros((512, 64), dtype=np.float16)
+    q_lut[256:] = c_g                                                # gate heads only
+    w = {"q": (q_packed, q_lut), "k": _const_lut6(1024, 4096, 0.0, 10),
+         "v": _const_lut6(1024, 4096, c_v, 11), "o": _const_lut6(4096, 4096, c_o, 12)}
+    x = rng.standard_normal((6, 4096)) * 0.05
+    s = x.sum(axis=1)
+    prefix_mean = np.cumsum(s) / np.arange(1, 7)
+    expect = c_o * 4096 * c_v * prefix_mean / (1 + np.exp(-c_g * s))
+    got = model.attention_mixer(x, w)
+    assert np.allclose(got, np.repeat(expect[:, None], 4096, axis=1), rtol=1e-10, atol=0)
