@@ -10,14 +10,15 @@ definitions.  A numpy matmul is used as the library primitive for dense products
 
 Sources (cited by page title and section in each function):
   * "Clef-Flash-ANE-LUT6" (Hugging Face model card) - Model architecture; Weight precision;
-    LUT-6 text weights.
+    LUT-6 text weights (the format in ``lut6``, the quantiser in ``quantize``).
   * "clef-flash - Core AI" (README) - Core AI shape (decoder inputs, states, hidden output).
   * "clef-flash-coreml" (README) - decoder parts with cos/sin [L, 64] rotary inputs.
-  * "clef-flash-LiteRT" (README) - Host contract (rotary theta 1e7, text positions (i, i, i),
-    right padding, final-norm hidden at every position); Provenance (chunked GatedDeltaNet
-    kernel of 64 positions, grouped keys/values repeated, gated full-attention layers).
+  * "clef-flash-LiteRT" (README) - Host contract (rotary theta 1e7 and the three M-RoPE planes,
+    text positions (i, i, i), right padding, the final norm's output per position); Provenance
+    (the GatedDeltaNet recurrence in 64-position chunks, grouped keys/values repeated, gated
+    full-attention layers).
 
 Functions whose result no page or closed form fixes are marked "parity unpinned" in their
 docstring (the end-to-end activations: no page prints any).
 """
-from . import lut6, layers, model  # noqa: F401
+from . import lut6, layers, model, quantize  # noqa: F401
