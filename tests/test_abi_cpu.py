@@ -118,3 +118,22 @@ def test_gdn_workspace_regions_fit(lib, B, L):
             assert a + sa <= b
         assert (offs[6] >= 0) == (B <= 2 and nch >= 64)     # the scan runs in pieces
         assert (offs[7] >= 0) == bool(with_norm)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """The product path has no fallback: with the library's file absent the binding raises."""
+    import subprocess
+    import sys
+    code = (
+        "import full_attention_prefill_gb300 as clef\n"
+        f"clef.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+        "clef._lib = None\n"
+        "try:\n"
+        "    clef.lib()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', e)\n"
+        "else:\n"
+        "    print('no error')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT,
+                       timeout=300)
+    assert "raised:" in r.stdout and "no fallback" in r.stdout, r.stdout + r.stderr
