@@ -431,3 +431,42 @@ def test_attention_output_gate_closed_form():
     expect = c_o * 4096 * c_v * prefix_mean / (1 + np.exp(-c_g * s))
     got = model.attention_mixer(x, w)
     assert np.allclose(got, np.repeat(expect[:, None], 4096, axis=1), rtol=1e-10, atol=0)
+
+
+def test_gdn_mixer_closed_form():
+    """The GDN mixer end to end on a case with a scalar closed form.  Constant QKV weights c1,
+    conv passing only the current tap, zero a/b projections and A_log = dt_bias = 0 (so
+    alpha = exp(-softplus(0)) = 1/2 and beta = sigmoid(0) = 1/2): every q, k, v row is constant,
+    q = k = u_t 1 after the L2 norm with u_t = sigma_t / sqrt(128 sigma_t^2 + eps), sigma_t =
+    SiLU(c1 s_t), and the state stays m_t 1 1^T with
+        m_t = alpha m_{t-1} + beta u_t (sigma_t - 128 alpha u_t m_{t-1}),
+    so o_t = sqrt(128) u_t m_t 1; the z-gated norm turns that into r_t w_o SiLU(c2 s_t) with
+    r_t = o / sqrt(o^2 + eps) (o the constant entry), and the output projection c3 sums it."""
+    import synth
+    w = synth.gdn_layer_weights(11, 0)
+    c1, c2, c3 = 2.0 ** -10, 2.0 ** -9, 2.0 ** -12
+    w["qkv"] = _const_lut6(8192, 4096, c1, 21)
+    w["z"] = _const_lut6(4096, 4096, c2, 22)
+    w["out"] = _const_lut6(4096, 4096, c3, 23)
+    w["a_w"] = np.zeros_like(w["a_w"])
+    w["b_w"] = np.zeros_like(w["b_w"])
+    w["A_log"] = np.zeros_like(w["A_log"])
+    w["dt_bias"] = np.zeros_like(w["dt_bias"])
+    conv = np.zeros_like(w["conv_w"])
+    conv[:, 3] = 1.0                                          # the current position only
+    w["conv_w"] = conv
+    xn = np.random.default_rng(12).uniform(0.0, 1e-3, size=(6, 4096))
+    s = xn.sum(axis=1)
+    silu = lambda t: t / (1.0 + np.exp(-t))  # noqa: E731
+    sigma = silu(c1 * s)
+    u = sigma / np.sqrt(128 * sigma ** 2 + 1e-6)
+    alpha = beta = 0.5
+    m, expect = 0.0, []
+    for t in range(6):
+        m = alpha * m + beta * u[t] * (sigma[t] - 128 * alpha * u[t] * m)
+        o = np.sqrt(128) * u[t] * m
+        r = o / np.sqrt(o * o + 1e-6)
+        y_sum = 32 * r * silu(c2 * s[t]) * float(np.sum(w["o_norm"].astype(np.float64)))
+        expect.append(c3 * y_sum)
+    got = model.gdn_mixer(xn, w)
+    assert np.allclose(got, np.repeat(np.array(expect)[:, None], 4096, axis=1), rtol=1e-9, atol=0)
