@@ -20,7 +20,7 @@
 //                   O = exp(g) Q S0^T / sqrt(128) + Aqk U, all on tcgen05
 //   gdn_gated_norm  (decoder layer only): y = RMSNorm_128(O) * w_o * SiLU(z)
 // The chunk phase's products run on mma.sync (m16n8k16, fp16 inputs, fp32 accumulation); the
-// state and the scalars stay fp32.  A long scan of one or two requests runs in pieces of chunks:
+// state and the scalars stay fp32.  A long scan of one request runs in pieces of chunks:
 // the chunk phase of the next piece on a low-priority stream beside the state pass of this one
 // on a high-priority stream (events order them; the state crosses pieces in fp32).
 #include <algorithm>
@@ -505,12 +505,12 @@ __global__ void __launch_bounds__(256) gdn_gated_norm_kernel(const __half* __res
 
 static inline size_t al256g(size_t x) { return (x + 255) & ~size_t(255); }
 
-// A long scan of few requests runs in pieces of chunks: the chunk phase of piece p + 1 (many
-// CTAs) overlaps the sequential state pass of piece p (one CTA per request and value head, which
-// leaves most SMs idle), on two streams ordered by events.  Pieces of at least 32 chunks.
+// A long scan of one request runs in pieces of chunks: the chunk phase of piece p + 1 (many
+// CTAs) overlaps the sequential state pass of piece p (one CTA per value head, which leaves most
+// SMs idle), on two streams ordered by events.  Pieces of at least 32 chunks.
 int gdn_pieces(int64_t B, int64_t L) {
   const int64_t nch = (L + gdn::C - 1) / gdn::C;
-  if (B > 2 || nch < 64) return 1;
+  if (B > 1 || nch < 64) return 1;
   return (int)std::min<int64_t>(8, nch / 32);
 }
 

@@ -116,7 +116,7 @@ def test_gdn_workspace_regions_fit(lib, B, L):
             assert 0 <= o and o + sz <= total.value, (B, L, with_norm, o, sz, total.value)
         for (a, sa), (b, _) in zip(regions, regions[1:]):
             assert a + sa <= b
-        assert (offs[6] >= 0) == (B <= 2 and nch >= 64)     # the scan runs in pieces
+        assert (offs[6] >= 0) == (B == 1 and nch >= 64)     # the scan runs in pieces
         assert (offs[7] >= 0) == bool(with_norm)
 
 

@@ -110,9 +110,8 @@ def test_scan_deterministic():
     assert torch.equal(a, b)
 
 
-# A scan of one or two requests with at least 64 chunks runs in pieces (the chunk phase of the
-# next piece overlapping the state pass of this one, on two streams); three requests run in one
-# pass.  The state crosses pieces in fp32, exactly as it stays in tensor memory in one pass, so the
+# A scan of one request with at least 64 chunks runs in pieces (the chunk phase of the next
+# piece overlapping the state pass of this one, on two streams); three requests run in one pass.  The state crosses pieces in fp32, exactly as it stays in tensor memory in one pass, so the
 # same request must come out bit for bit the same either way, with or without an entering state.
 @pytest.mark.parametrize("L,with_s0", [(4096, False), (8192, True), (4150, True)])
 def test_pieces_equal_one_pass(L, with_s0):
