@@ -41,6 +41,36 @@ unsigned* status_word_ptr() {
   return ptrs[dev];
 }
 
+cudaError_t smem_opt_in(const void* func, size_t bytes, std::atomic<uint64_t>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t)1 << dev : 0;
+  if (bit && (done->load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  // setting the same value twice (two threads racing here) is harmless
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done->fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+clef_status check_batch_len(int64_t B, int64_t L) {
+  if (B < 1 || L < 1) {
+    set_error("need B >= 1 and L >= 1 (B=%lld L=%lld)", (long long)B, (long long)L);
+    return CLEF_E_INVALID;
+  }
+  if (L > CLEF_MAX_LEN) {
+    set_error("L = %lld is above the %d-position limit (refused, never cut)", (long long)L,
+              CLEF_MAX_LEN);
+    return CLEF_E_TOO_LONG;
+  }
+  if (B > (((int64_t)1 << 22) / L)) {   // B * L > 2^22, without forming the product
+    set_error("B = %lld requests of L = %lld positions is above the supported 4194304 tokens",
+              (long long)B, (long long)L);
+    return CLEF_E_SHAPE;
+  }
+  return CLEF_OK;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -467,13 +467,8 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
                          int64_t ldo, int64_t B, int64_t L, int64_t pos0, int64_t kv_req,
                          cudaStream_t stream) {
   if (B == 0 || L == 0) return CLEF_OK;
-  static bool attr = false;
-  if (!attr) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(attn::flash_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         attn::FLASH_SMEM));
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)attn::flash_tc_kernel, attn::FLASH_SMEM, &attr));
   // Q rows are read with 16-byte loads; K and V by TMA (row strides a multiple of 16 bytes)
   if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || (ldq & 7) != 0 ||
       (reinterpret_cast<uintptr_t>(k) & 15) != 0 || (ldk & 7) != 0 ||

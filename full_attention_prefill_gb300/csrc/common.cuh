@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/clef.h"
 
 namespace clef {
@@ -36,6 +38,11 @@ cudaError_t tma_encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const
                        CUtensorMapSwizzle swz);
 const char* set_error(const char* fmt, ...);
 int num_sms();
+// Opt the kernel `func` in to `bytes` of dynamic shared memory on the current device, once per
+// device (the attribute is per device); `done` holds one bit per device index.  Thread-safe.
+cudaError_t smem_opt_in(const void* func, size_t bytes, std::atomic<uint64_t>* done);
+// B >= 1, L in 1 .. CLEF_MAX_LEN and B * L <= 2^22 tokens (checked without overflow).
+clef_status check_batch_len(int64_t B, int64_t L);
 bool debug_should_fail();            // host-side fault hook (clef_debug_fail_next)
 
 // Per-kernel-class device timing (clef_trace_begin / clef_trace_end).  A TraceScope around a

@@ -174,22 +174,7 @@ static clef_status check_layer(const clef_layer* ly, int idx) {
   return CLEF_OK;
 }
 
-static clef_status check_bl(int64_t B, int64_t L) {
-  if (B < 1 || L < 1) {
-    set_error("need B >= 1 and L >= 1 (B=%lld L=%lld)", (long long)B, (long long)L);
-    return CLEF_E_INVALID;
-  }
-  if (L > CLEF_MAX_LEN) {
-    set_error("L = %lld is above the %d-position limit (refused, never cut)", (long long)L,
-              CLEF_MAX_LEN);
-    return CLEF_E_TOO_LONG;
-  }
-  if (B * L > (int64_t)1 << 22) {
-    set_error("B * L = %lld tokens is above the supported 4194304", (long long)(B * L));
-    return CLEF_E_SHAPE;
-  }
-  return CLEF_OK;
-}
+static clef_status check_bl(int64_t B, int64_t L) { return check_batch_len(B, L); }
 
 // The whole prefill of B requests (ids [B][L]); with image_rows, rows mr.start .. of every
 // request are the picture's rows ([B][h * w][4096] fp16) and the rotary uses M-RoPE planes.

@@ -563,12 +563,9 @@ static GdnWs carve(void* ws, int64_t B, int64_t L) {
   return w;
 }
 
-static bool g_gdn_attr = false;
 static clef_status gdn_set_attrs() {
-  if (g_gdn_attr) return CLEF_OK;
-  CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_chunk_wy_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(gdn::WySmem)));
-  g_gdn_attr = true;
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)gdn::gdn_chunk_wy_kernel, sizeof(gdn::WySmem), &attr));
   return CLEF_OK;
 }
 
@@ -577,12 +574,8 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
                             int64_t L, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
-  static bool attr = false;
-  if (!attr) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn::gdn_prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::PREP_SMEM));
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)gdn::gdn_prep_kernel, gdn::PREP_SMEM, &attr));
   dim3 grid(8192 / gdn::PREP_CH, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
   gdn::gdn_prep_kernel<<<grid, 256, gdn::PREP_SMEM, stream>>>(proj, ldp, conv_w, conv_in, q, k, v,
                                                                M, (int)L);
@@ -677,33 +670,39 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[0], stream));
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->lo, ss->ev[0], 0));
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->hi, ss->ev[0], 0));
-    for (int p = 0; p < pieces; ++p) {
-      const int64_t c0 = (int64_t)p * nch / pieces, c1 = (int64_t)(p + 1) * nch / pieces;
-      st = chunk_phase(c0, c1 - c0, ss->lo);
-      if (st != CLEF_OK) return st;
-      CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + p], ss->lo));
-      CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->hi, ss->ev[1 + p], 0));
-      st = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, p == 0 ? s0 : s_eff, s_eff, o,
-                            ldo_pass, B, L, ss->hi, c0, c1 - c0);
-      if (st != CLEF_OK) return st;
-      if (z) {
-        // the z-gated norm of this piece's rows, in the state stream's wait for the next
-        // chunk phase
-        const int64_t t0 = c0 * gdn::C, t1 = std::min<int64_t>(c1 * gdn::C, L);
-        for (int64_t b = 0; b < B; ++b) {
-          const int64_t r0 = b * L + t0;
-          TraceScope ts(ss->hi, "gdn_gated_norm", 0.0, (double)(t1 - t0) * 4096 * 2 * 3);
-          gdn::gdn_gated_norm_kernel<<<(unsigned)(t1 - t0), 256, 0, ss->hi>>>(
-              o + r0 * ldo_pass, z + r0 * ldz, ldz, o_norm, out + r0 * ldo, ldo);
-          CLEF_LAUNCH_CHECK();
+    auto run_pieces = [&]() -> clef_status {
+      for (int p = 0; p < pieces; ++p) {
+        const int64_t c0 = (int64_t)p * nch / pieces, c1 = (int64_t)(p + 1) * nch / pieces;
+        clef_status ps = chunk_phase(c0, c1 - c0, ss->lo);
+        if (ps != CLEF_OK) return ps;
+        CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + p], ss->lo));
+        CLEF_CUDA_CHECK(cudaStreamWaitEvent(ss->hi, ss->ev[1 + p], 0));
+        ps = gdn_state_launch(q, w.Kt, w.W, w.U1, w.Aqk, w.ef, p == 0 ? s0 : s_eff, s_eff, o,
+                              ldo_pass, B, L, ss->hi, c0, c1 - c0);
+        if (ps != CLEF_OK) return ps;
+        if (z) {
+          // the z-gated norm of this piece's rows, in the state stream's wait for the next
+          // chunk phase
+          const int64_t t0 = c0 * gdn::C, t1 = std::min<int64_t>(c1 * gdn::C, L);
+          for (int64_t b = 0; b < B; ++b) {
+            const int64_t r0 = b * L + t0;
+            TraceScope ts(ss->hi, "gdn_gated_norm", 0.0, (double)(t1 - t0) * 4096 * 2 * 3);
+            gdn::gdn_gated_norm_kernel<<<(unsigned)(t1 - t0), 256, 0, ss->hi>>>(
+                o + r0 * ldo_pass, z + r0 * ldz, ldz, o_norm, out + r0 * ldo, ldo);
+            CLEF_LAUNCH_CHECK();
+          }
         }
       }
-    }
-    // join
+      return CLEF_OK;
+    };
+    st = run_pieces();
+    // join, also after an error part way: whatever was queued on the side streams is ordered
+    // before later work on the caller's stream (which may free or reuse the workspace)
     CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[1 + pieces], ss->hi));
     CLEF_CUDA_CHECK(cudaEventRecord(ss->ev[2 + pieces], ss->lo));
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[1 + pieces], 0));
     CLEF_CUDA_CHECK(cudaStreamWaitEvent(stream, ss->ev[2 + pieces], 0));
+    if (st != CLEF_OK) return st;
   }
   if (z && pieces <= 1) {
     TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);

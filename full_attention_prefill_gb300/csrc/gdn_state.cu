@@ -433,12 +433,8 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
   const int64_t nch = (L + C - 1) / C;
   if (ncl < 0) ncl = nch - c0;
   if (c0 < 0 || ncl < 1 || c0 + ncl > nch) return CLEF_E_INVALID;
-  static bool attr = false;
-  if (!attr) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(gdn_state_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM));
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)gdn_state_tc_kernel, ST_SMEM, &attr));
   CUtensorMap tW, tQ, tKd, tA, tO;
   {
     // the chunk phase's outputs: one block of 64 rows per (chunk, head)

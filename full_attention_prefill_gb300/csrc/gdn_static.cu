@@ -55,14 +55,10 @@ clef_status clef_gdn_prefill_noalloc(const uint16_t* q, const uint16_t* k, const
                                      const float* alpha, const float* beta, const float* s0,
                                      uint16_t* o, float* s_out, int64_t B, int64_t L,
                                      clef_stream stream) {
-  if (B < 1 || L < 1) {
-    set_error("clef_gdn_prefill_noalloc: need B >= 1 and L >= 1");
-    return CLEF_E_INVALID;
-  }
-  if (L > CLEF_MAX_LEN) {
-    set_error("clef_gdn_prefill_noalloc: L = %lld is above %d", (long long)L, CLEF_MAX_LEN);
-    return CLEF_E_TOO_LONG;
-  }
+  // the same size limits as clef_gdn_prefill (B * L <= 2^22 keeps the scratch size query's
+  // products in range) before the scratch size is computed
+  const clef_status size_st = check_batch_len(B, L);
+  if (size_st != CLEF_OK) return size_st;
   const size_t need = gdn_scan_workspace_bytes(B, L, false);
   if (need > kStaticScratchBytes) {
     set_error("clef_gdn_prefill_noalloc: B=%lld, L=%lld needs %zu bytes of scratch, above the "

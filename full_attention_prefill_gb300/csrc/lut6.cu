@@ -532,12 +532,8 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
                    CU_TENSOR_MAP_SWIZZLE_NONE) != cudaSuccess)
       return CLEF_E_CUDA;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(lut6_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)lut6_gemm_kernel, SMEM_BYTES, &attr));
   // the tables are fetched with 16-byte bulk copies
   if ((reinterpret_cast<uintptr_t>(lut) & 15) != 0) return CLEF_E_ALIGN;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);

@@ -474,12 +474,8 @@ clef_status lut6_quantize_launch(const __half* w, int64_t n, int64_t k, uint8_t*
   const int64_t groups = n / 16;
   if (groups == 0) return CLEF_OK;
   const size_t smem = sizeof(quant::Smem);
-  static bool attr = false;
-  if (!attr) {
-    CLEF_CUDA_CHECK(cudaFuncSetAttribute(quant::quantize_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)quant::quantize_kernel, smem, &attr));
   const int64_t clusters = std::min<int64_t>(groups, (int64_t)num_sms() * 3 / quant::CL);
   TraceScope ts(stream, "lut6_quantize", 0.0, 2.0 * n * k * 2.0 + 0.75 * n * k + 128.0 * groups);
   quant::quantize_kernel<<<(unsigned)(clusters * quant::CL), quant::THREADS, smem, stream>>>(
