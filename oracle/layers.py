@@ -1,230 +1,144 @@
-"""Oracle building blocks of the clef-flash decoder layers (numpy, float64).
-
-Each function states the passage it follows.  Shapes use L = positions of one request.
-Where a page is silent the plainest reading is taken and named in the docstring.
+"""Oracle building blocks of the clef-flash decoder layers: thin marshalling over the C++ oracle
+(oracle/csrc/layers.cpp, fp64).  Each C++ function states the passage it follows; the readings
+(eps, scales, head maps, rotary pairing, M-RoPE planes) are stated there.
 """
 from __future__ import annotations
 
 import numpy as np
 
+from ._lib import check, contig, f64, lib, ptr
+
 RMS_EPS = 1e-6
 L2_EPS = 1e-6
 ROPE_THETA = 1.0e7
 ROPE_DIMS = 64
+MROPE_SECTIONS = (11, 11, 10)   # frequency pairs on the t, h and w planes
 
 
-def f64(a) -> np.ndarray:
-    return np.asarray(a, dtype=np.float64)
+def _elementwise(fn, x):
+    xx = f64(x)
+    out = np.empty_like(xx)
+    fn(ptr(xx), xx.size, ptr(out))
+    return out
 
 
 def silu(x):
-    x = f64(x)
-    return x / (1.0 + np.exp(-x))
+    return _elementwise(lib().orc_silu, x)
 
 
 def sigmoid(x):
-    x = f64(x)
-    return 1.0 / (1.0 + np.exp(-x))
+    return _elementwise(lib().orc_sigmoid, x)
 
 
 def softplus(x):
-    x = f64(x)
-    return np.logaddexp(0.0, x)
+    return _elementwise(lib().orc_softplus, x)
 
 
 def rmsnorm(x, w, eps=RMS_EPS):
-    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * w.
-
-    "Clef-Flash-ANE-LUT6" §Weight precision lists normalization weights among the FP16 text
-    weights; "clef-flash-LiteRT" §Host contract step 6 returns the output of the final
-    RMSNorm.  eps = 1e-6 and the plain x * r * w form are the adopted reading (no page gives them).
-    """
-    x = f64(x)
-    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
-    return x * r * f64(w)
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * w."""
+    xx = f64(x)
+    d = xx.shape[-1]
+    ww = np.broadcast_to(f64(w), (d,)).copy() if w is not None else None
+    out = np.empty_like(xx)
+    lib().orc_rmsnorm(ptr(xx), xx.size // d if d else 0, d, ptr(ww), float(eps), ptr(out))
+    return out
 
 
 def l2norm(x, eps=L2_EPS):
-    """x / sqrt(sum(x^2) + eps) over the last axis (per-head q/k normalisation of the GDN)."""
-    x = f64(x)
-    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    """x / sqrt(sum(x^2) + eps) over the last axis."""
+    xx = f64(x)
+    d = xx.shape[-1]
+    out = np.empty_like(xx)
+    lib().orc_l2norm(ptr(xx), xx.size // d if d else 0, d, float(eps), ptr(out))
+    return out
 
 
 def causal_conv_silu(x, w):
-    """Short causal depthwise convolution (kernel 4) followed by SiLU.
-
-    "Clef-Flash-ANE-LUT6" §Weight precision names the short convolution; "clef-flash - Core AI"
-    §Core AI shape carries a conv state [24, 1, 8192, 3] per GDN layer, i.e. 8,192 channels and a
-    kernel of 3 + 1 = 4.  c[t, ch] = SiLU(sum_{j=0..3} w[ch, j] * x[t - 3 + j, ch]), with zero
-    history before position 0 (a prefill starts from a zeroed state).
-    x: [L, C], w: [C, 4].
-    """
-    x = f64(x)
-    w = f64(w)
-    L, C = x.shape
-    ksz = w.shape[1]
-    acc = np.zeros((L, C))
-    for j in range(ksz):
-        shift = ksz - 1 - j              # tap j reads position t - shift
-        if shift == 0:
-            acc += w[:, j] * x
-        elif shift < L:
-            acc[shift:] += w[:, j] * x[: L - shift]
-    return silu(acc)
+    """Causal depthwise conv (zero history) then SiLU.  x: [L, C], w: [C, taps]."""
+    xx, ww = f64(x), f64(w)
+    L, C = xx.shape
+    out = np.empty_like(xx)
+    lib().orc_conv_silu(ptr(xx), L, C, ptr(ww), ww.shape[1], ptr(out))
+    return out
 
 
 def gdn_gates(a, b, A_log, dt_bias):
-    """Per-value-head decay and write strength of the Gated DeltaNet.
-
-    "Clef-Flash-ANE-LUT6" §Weight precision keeps the gates' projection weights and the decay
-    parameters in FP16.  Adopted reading (standard Gated DeltaNet gating):
-      alpha = exp(-exp(A_log) * softplus(a + dt_bias)),  beta = sigmoid(b).
-    a, b: [L, Hv];  A_log, dt_bias: [Hv].
-    """
-    alpha = np.exp(-np.exp(f64(A_log)) * softplus(f64(a) + f64(dt_bias)))
-    beta = sigmoid(b)
+    """alpha = exp(-exp(A_log) softplus(a + dt_bias)), beta = sigmoid(b); a, b [L, Hv]."""
+    aa, bb = f64(a), f64(b)
+    L, H = aa.shape
+    A, dt = f64(np.broadcast_to(f64(A_log), (H,))), f64(np.broadcast_to(f64(dt_bias), (H,)))
+    alpha, beta = np.empty_like(aa), np.empty_like(aa)
+    lib().orc_gdn_gates(ptr(aa), ptr(bb), L, H, ptr(A), ptr(dt), ptr(alpha), ptr(beta))
     return alpha, beta
 
 
 def gated_delta_rule(q, k, v, alpha, beta, s0=None):
-    """The gated delta rule as a per-token recurrence (no chunking).
-
-    "Clef-Flash-ANE-LUT6" §Model architecture: 24 Gated DeltaNet layers with 16 key and 32 value
-    heads of size 128; "clef-flash - Core AI" §Core AI shape: recurrent state [.., 32, 128, 128]
-    per layer, the recurrence unrolled over positions.  For value head h (key head h // 2):
-        S_t = alpha_t * S_{t-1} + beta_t * (v_t - alpha_t * S_{t-1} k_t) k_t^T
-        o_t = S_t q_t / sqrt(d_k)
-    S is [d_v, d_k], S_0 = s0 (zero by default).  The output is read from the updated state and
-    scaled by 1/sqrt(d_k) (adopted reading).
-    q, k: [L, Hk, dk]; v: [L, Hv, dv]; alpha, beta: [L, Hv].  Returns (o [L, Hv, dv], S_L).
-    """
-    q, k, v = f64(q), f64(k), f64(v)
-    alpha, beta = f64(alpha), f64(beta)
-    L, Hk, dk = k.shape
-    Hv, dv = v.shape[1], v.shape[2]
-    rep = Hv // Hk
-    S = np.zeros((Hv, dv, dk)) if s0 is None else f64(s0).copy()
+    """The per-token gated delta rule.  q, k: [L, Hk, dk]; v: [L, Hv, dv]; alpha, beta: [L, Hv];
+    s0 [Hv, dv, dk] or None.  Returns (o [L, Hv, dv], S_L [Hv, dv, dk])."""
+    qq, kk, vv = f64(q), f64(k), f64(v)
+    aa, bb = f64(alpha), f64(beta)
+    L, Hk, dk = kk.shape
+    Hv, dv = vv.shape[1], vv.shape[2]
+    ss = None if s0 is None else f64(s0)
     o = np.empty((L, Hv, dv))
-    scale = 1.0 / np.sqrt(dk)
-    for t in range(L):
-        kt = np.repeat(k[t], rep, axis=0)            # [Hv, dk]
-        qt = np.repeat(q[t], rep, axis=0)
-        a = alpha[t][:, None, None]
-        Sk = np.einsum("hij,hj->hi", S, kt)          # S_{t-1} k_t  [Hv, dv]
-        u = beta[t][:, None] * (v[t] - alpha[t][:, None] * Sk)
-        S = a * S + u[:, :, None] * kt[:, None, :]
-        o[t] = np.einsum("hij,hj->hi", S, qt) * scale
+    S = np.empty((Hv, dv, dk))
+    check(lib().orc_gated_delta_rule(ptr(qq), ptr(kk), ptr(vv), ptr(aa), ptr(bb), ptr(ss), L, Hk, Hv,
+                                     dk, dv, ptr(o), ptr(S)), "gated_delta_rule")
     return o, S
 
 
 def zgated_norm(o, z, w, eps=RMS_EPS):
-    """Output gate of the GDN mixer: RMSNorm over each head's d_v values, times w, times SiLU(z).
-
-    o, z: [L, Hv, dv]; w: [dv] shared by the heads.  Returns [L, Hv * dv].
-    """
-    y = rmsnorm(o, w, eps) * silu(z)
-    return y.reshape(o.shape[0], -1)
+    """RMSNorm over each head's dv values, times w, times SiLU(z).  o, z: [L, Hv, dv] -> [L, Hv*dv]."""
+    oo, zz, ww = f64(o), f64(z), f64(w)
+    L, H, d = oo.shape
+    out = np.empty_like(oo)
+    lib().orc_zgated_norm(ptr(oo), ptr(zz), L, H, d, ptr(ww), float(eps), ptr(out))
+    return out.reshape(L, H * d)
 
 
 def rope(x, positions, rot_dims=ROPE_DIMS, theta=ROPE_THETA):
-    """Rotary embedding on the first `rot_dims` dims of each head (rotate-half pairing).
-
-    "clef-flash-coreml" README: decoder parts take cos/sin [L, 64]; "clef-flash-LiteRT" §Host
-    contract step 5: theta = 1e7 and text tokens sit at (i, i, i) for their index i, so the three
-    M-RoPE planes collapse to one 1-D rotary.  Pairs (j, j + 32) for j < 32 rotate by angle
-    pos * theta^(-2j/64); dims 64.. pass through.  x: [L, H, D]; positions: [L].
-    """
-    x = f64(x).copy()
-    half = rot_dims // 2
-    inv_freq = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / rot_dims)
-    ang = f64(positions)[:, None] * inv_freq[None, :]          # [L, half]
-    c = np.cos(ang)[:, None, :]
-    s = np.sin(ang)[:, None, :]
-    x1 = x[..., :half].copy()
-    x2 = x[..., half:rot_dims].copy()
-    x[..., :half] = x1 * c - x2 * s
-    x[..., half:rot_dims] = x2 * c + x1 * s
-    return x
-
-
-MROPE_SECTIONS = (11, 11, 10)   # frequency pairs on the t, h and w planes
+    """1-D rotary on the first `rot_dims` dims of each head.  x: [L, H, D]; positions: [L]."""
+    xx = f64(x)
+    L, H, D = xx.shape
+    pos = f64(positions).reshape(L)
+    out = np.empty_like(xx)
+    lib().orc_rope(ptr(xx), L, H, D, ptr(pos), rot_dims, float(theta), ptr(out))
+    return out
 
 
 def mrope_planes(rot_dims=ROPE_DIMS):
-    """Plane (0 = t, 1 = h, 2 = w) of each of the 32 frequency pairs.
-
-    "clef-flash-LiteRT" §Host contract step 5: three planes, sections 11 / 11 / 10, interleaved.
-    Reading: pair j takes plane j mod 3, which gives exactly 11, 11 and 10 pairs.
-    """
-    return np.arange(rot_dims // 2) % 3
+    """Plane (0 = t, 1 = h, 2 = w) of each of the rot_dims / 2 frequency pairs."""
+    out = np.empty(rot_dims // 2, dtype=np.int64)
+    lib().orc_mrope_planes(rot_dims, ptr(out))
+    return out
 
 
 def mrope_positions(L, image_start=0, grid_h=0, grid_w=0):
-    """[L, 3] integer positions (t, h, w) of a request holding at most one picture block.
-
-    "clef-flash-LiteRT" §Host contract step 5: text tokens sit at (i, i, i) for their index i,
-    picture tokens at their row and column of the picture's grid, and padding goes on from the
-    last position.  "clef-flash - Core AI" §Core AI shape: image token k sits at row k // W, column
-    k % W, and from the <|vision_end|> index (picture start + N) on the positions move back by
-    N - max(H, W).  Reading (the plainest one those numbers allow): image token k at index s + k
-    has (s, s + k // W, s + k % W), so the token after the block continues at s + max(H, W), one
-    past the largest picture position.
-    """
-    n = grid_h * grid_w
-    pos = np.empty((L, 3), dtype=np.int64)
-    for i in range(L):
-        if n == 0 or i < image_start:
-            pos[i] = (i, i, i)
-        elif i < image_start + n:
-            k = i - image_start
-            pos[i] = (image_start, image_start + k // grid_w, image_start + k % grid_w)
-        else:
-            p = i - (n - max(grid_h, grid_w))
-            pos[i] = (p, p, p)
-    return pos
+    """[L, 3] integer positions (t, h, w) of a request holding at most one picture block."""
+    out = np.empty((L, 3), dtype=np.int64)
+    check(lib().orc_mrope_positions(L, image_start, grid_h, grid_w, ptr(out)), "mrope_positions")
+    return out
 
 
 def mrope(x, pos3, rot_dims=ROPE_DIMS, theta=ROPE_THETA):
-    """Multimodal rotary: as :func:`rope`, with pair j rotated by pos3[:, plane(j)] * theta^(-2j/64).
-
-    "clef-flash-LiteRT" §Host contract step 5 (cos and sin [L, 64] of the three-plane positions,
-    theta = 1e7).  With pos3 = (i, i, i) it is :func:`rope` at position i.
-    """
-    x = f64(x).copy()
-    half = rot_dims // 2
-    inv_freq = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / rot_dims)
-    pos3 = np.asarray(pos3)
-    ang = f64(pos3[:, mrope_planes(rot_dims)]) * inv_freq[None, :]     # [L, half]
-    c = np.cos(ang)[:, None, :]
-    s = np.sin(ang)[:, None, :]
-    x1 = x[..., :half].copy()
-    x2 = x[..., half:rot_dims].copy()
-    x[..., :half] = x1 * c - x2 * s
-    x[..., half:rot_dims] = x2 * c + x1 * s
-    return x
+    """Multimodal rotary: pair j turns by pos3[:, plane(j)] * theta^(-2j/64)."""
+    xx = f64(x)
+    L, H, D = xx.shape
+    p3 = contig(pos3, np.int64).reshape(L, 3)
+    out = np.empty_like(xx)
+    lib().orc_mrope(ptr(xx), L, H, D, ptr(p3), rot_dims, float(theta), ptr(out))
+    return out
 
 
-def causal_attention(q, k, v):
-    """Causal softmax attention with grouped keys/values, one explicit softmax per query row.
-
-    "clef-flash-LiteRT" §Provenance: attention as batched products with an additive mask, the
-    grouped keys and values repeated to the query heads.  Query head h reads kv head
-    h // (Hq / Hkv); logits are q.k / sqrt(D); row t attends to positions 0..t.
-    q: [L, Hq, D]; k, v: [L, Hkv, D].  Returns [L, Hq, D].
-    """
-    q, k, v = f64(q), f64(k), f64(v)
-    L, Hq, D = q.shape
-    Hkv = k.shape[1]
-    rep = Hq // Hkv
-    out = np.empty((L, Hq, D))
-    scale = 1.0 / np.sqrt(D)
-    mask = np.tril(np.ones((L, L), dtype=bool))
-    for h in range(Hq):
-        g = h // rep
-        logits = (q[:, h, :] @ k[:, g, :].T) * scale          # [L, L]
-        logits = np.where(mask, logits, -np.inf)
-        m = logits.max(axis=1, keepdims=True)
-        p = np.exp(logits - m)
-        p /= p.sum(axis=1, keepdims=True)
-        out[:, h, :] = p @ v[:, g, :]
+def causal_attention(q, k, v, rows=None):
+    """Causal GQA softmax attention, one explicit softmax per query row.
+    q: [L, Hq, D]; k, v: [L, Hkv, D].  Returns [L, Hq, D], or only query rows r0 .. r1 - 1 when
+    rows = (r0, r1)."""
+    qq, kk, vv = f64(q), f64(k), f64(v)
+    L, Hq, D = qq.shape
+    Hkv = kk.shape[1]
+    r0, r1 = (0, L) if rows is None else rows
+    out = np.empty((r1 - r0, Hq, D))
+    check(lib().orc_causal_attention(ptr(qq), ptr(kk), ptr(vv), L, Hq, Hkv, D, r0, r1, ptr(out)),
+          "causal_attention")
     return out

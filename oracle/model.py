@@ -1,120 +1,125 @@
-"""Oracle decoder layers and the 32-layer hybrid prefill (numpy, float64).
+"""Oracle decoder layers and the 32-layer hybrid prefill: thin marshalling over the C++ oracle
+(oracle/csrc/model.cpp, fp64).
 
-Architecture ("Clef-Flash-ANE-LUT6" §Model architecture; "clef-flash-LiteRT" §Provenance):
-32 layers of hidden size 4,096 and MLP size 12,288; 24 Gated DeltaNet layers and 8 gated
-full-attention layers, full attention every fourth layer (layers 3, 7, ..., 31).  Every large
-linear is LUT-6 (§Weight precision).  Each layer is a pre-norm residual block (adopted reading;
-the pages are silent on it):  h = x + mixer(rmsnorm(x)),  y = h + mlp(rmsnorm(h)).
-
-Weights come as a dict per layer: LUT-6 linears as (packed [n, k*3/4] uint8, lut [n/16, 64] fp16)
-pairs, the rest as fp16 arrays.  End-to-end activations are parity unpinned against the pages
-(no page prints one); the layers' parts are pinned piecewise by the oracle's own tests.
+Weights come as a dict per layer (the names of synth's recipe): LUT-6 linears as
+(packed [n, k*3/4] uint8, lut [n/16, 64] fp16) pairs, the rest as fp16 arrays.  This module only
+lays them out as the C structs and passes pointers.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 
-from . import layers as Lr
-from . import lut6
+from ._lib import Layer, Lut6Weight, check, contig, f16_bits, f64, lib, ptr
 
 GDN_HK, GDN_HV, GDN_D = 16, 32, 128
 ATT_HQ, ATT_HKV, ATT_D = 16, 4, 256
 
+_LUT6_NAMES = ("qkv", "z", "out", "q", "k", "v", "o", "gate", "up", "down")
+_F16_NAMES = ("attn_norm", "mlp_norm", "a_w", "b_w", "A_log", "dt_bias", "conv_w", "o_norm")
 
-def _lin(x, wt):
-    packed, lut = wt
-    n = lut.shape[0] * lut6.GROUP_ROWS
-    return lut6.linear(x, packed, lut, n)
+
+def _layer_struct(w, attention, keep):
+    """The orc_layer struct of a weight dict; `keep` holds the arrays the pointers point into."""
+    s = Layer()
+    s.attention = 1 if attention else 0
+    for name in _LUT6_NAMES:
+        if name in w:
+            packed, lut = w[name]
+            p, t = contig(packed, np.uint8), f16_bits(lut)
+            keep += [p, t]
+            setattr(s, name, Lut6Weight(p.ctypes.data, t.ctypes.data, t.shape[0] * 16, p.shape[1] * 4 // 3))
+    for name in _F16_NAMES:
+        if name in w:
+            a = f16_bits(w[name])
+            keep.append(a)
+            setattr(s, name, a.ctypes.data)
+    return s
+
+
+def _positions(L, positions, keep):
+    if positions is None:
+        return None, None
+    pos = np.asarray(positions)
+    if pos.ndim == 2:
+        p3 = contig(pos, np.int64).reshape(L, 3)
+        keep.append(p3)
+        return None, p3
+    p = f64(pos).reshape(L)
+    keep.append(p)
+    return p, None
 
 
 def swiglu_mlp(xn, w):
-    """SwiGLU MLP: down(SiLU(x W_gate^T) * (x W_up^T)); all three LUT-6 ("Clef-Flash-ANE-LUT6"
-    §Weight precision lists MLP gate/up/down among the LUT-6 layers)."""
-    return _lin(Lr.silu(_lin(xn, w["gate"])) * _lin(xn, w["up"]), w["down"])
-
-
-def gdn_mixer(xn, w, return_parts=False):
-    """Gated DeltaNet mixer on one request.  xn: normalised input [L, 4096].
-
-    QKV (4096 -> 8192 = q 2048 | k 2048 | v 4096) and Z (4096 -> 4096) are LUT-6; the gate
-    projections a, b (4096 -> 32 each) are FP16 ("Clef-Flash-ANE-LUT6" §Weight precision).
-    Conv + SiLU on all 8,192 QKV channels, per-head L2 norm of q and k, gates, the delta rule,
-    the z-gated RMSNorm, then the LUT-6 output projection (4096 -> 4096).
-    """
-    xn = Lr.f64(xn)
-    L = xn.shape[0]
-    qkv = _lin(xn, w["qkv"])
-    z = _lin(xn, w["z"])
-    a = xn @ Lr.f64(w["a_w"]).T
-    b = xn @ Lr.f64(w["b_w"]).T
-    c = Lr.causal_conv_silu(qkv, w["conv_w"])
-    qk = GDN_HK * GDN_D
-    q = Lr.l2norm(c[:, :qk].reshape(L, GDN_HK, GDN_D))
-    k = Lr.l2norm(c[:, qk:2 * qk].reshape(L, GDN_HK, GDN_D))
-    v = c[:, 2 * qk:].reshape(L, GDN_HV, GDN_D)
-    alpha, beta = Lr.gdn_gates(a, b, w["A_log"], w["dt_bias"])
-    o, S = Lr.gated_delta_rule(q, k, v, alpha, beta)
-    y = Lr.zgated_norm(o, z.reshape(L, GDN_HV, GDN_D), w["o_norm"])
-    out = _lin(y, w["out"])
-    if return_parts:
-        return out, dict(qkv=qkv, z=z, a=a, b=b, q=q, k=k, v=v, alpha=alpha, beta=beta, o=o,
-                         S=S, y=y)
+    """SwiGLU MLP: down(SiLU(x W_gate^T) * (x W_up^T)); all three LUT-6."""
+    x = f64(xn)
+    L, H = x.shape
+    keep = []
+    s = _layer_struct(w, False, keep)
+    out = np.empty((L, H))
+    check(lib().orc_swiglu_mlp(ptr(x), L, H, ctypes.byref(s), ptr(out)), "swiglu_mlp")
     return out
 
 
-def attention_mixer(xn, w, positions=None, return_parts=False):
-    """Gated full-attention mixer on one request.  xn: [L, 4096].
+def gdn_mixer(xn, w):
+    """Gated DeltaNet mixer on one request.  xn: normalised input [L, 4096] -> [L, 4096]."""
+    x = f64(xn)
+    L, H = x.shape
+    keep = []
+    s = _layer_struct(w, False, keep)
+    out = np.empty((L, H))
+    check(lib().orc_gdn_mixer(ptr(x), L, H, ctypes.byref(s), ptr(out)), "gdn_mixer")
+    return out
 
-    Q-proj 4096 -> 8192 holds the 16 query heads (columns 0..4095) and 16 output-gate heads
-    (4096..8191): adopted reading of "gated full-attention layers" ("clef-flash-LiteRT"
-    §Provenance), the only one that makes the model's stored LUT-6 size match the 4.86 GiB the
-    "Clef-Flash-ANE-LUT6" card gives for its text programs.  K, V 4096 -> 1024 (4 heads x 256),
-    rotary on the first 64 dims of q and k, causal GQA softmax, o * sigmoid(gate), O-proj.
-    """
-    xn = Lr.f64(xn)
-    L = xn.shape[0]
-    pos = np.arange(L) if positions is None else np.asarray(positions)
-    rot = Lr.mrope if pos.ndim == 2 else Lr.rope       # [L, 3] M-RoPE planes or [L] positions
-    qg = _lin(xn, w["q"])
-    q = qg[:, :ATT_HQ * ATT_D].reshape(L, ATT_HQ, ATT_D)
-    gate = qg[:, ATT_HQ * ATT_D:]
-    k = _lin(xn, w["k"]).reshape(L, ATT_HKV, ATT_D)
-    v = _lin(xn, w["v"]).reshape(L, ATT_HKV, ATT_D)
-    qr = rot(q, pos)
-    kr = rot(k, pos)
-    o = Lr.causal_attention(qr, kr, v).reshape(L, ATT_HQ * ATT_D)
-    og = o * Lr.sigmoid(gate)
-    out = _lin(og, w["o"])
-    if return_parts:
-        return out, dict(qg=qg, q=q, k=k, v=v, o=o, og=og)
+
+def attention_mixer(xn, w, positions=None):
+    """Gated full-attention mixer on one request.  xn: [L, 4096]; positions [L] or [L, 3]."""
+    x = f64(xn)
+    L, H = x.shape
+    keep = []
+    s = _layer_struct(w, True, keep)
+    pos, pos3 = _positions(L, positions, keep)
+    out = np.empty((L, H))
+    check(lib().orc_attention_mixer(ptr(x), L, H, ctypes.byref(s), ptr(pos), ptr(pos3), ptr(out)),
+          "attention_mixer")
     return out
 
 
 def decoder_layer(x, w, attention: bool, positions=None):
-    """One pre-norm residual decoder layer on one request: x [L, 4096] -> [L, 4096].
-    `positions`: rotary positions of the attention layers ([L], or [L, 3] M-RoPE planes;
-    default 0 .. L - 1)."""
-    x = Lr.f64(x)
-    xn = Lr.rmsnorm(x, w["attn_norm"])
-    h = x + (attention_mixer(xn, w, positions) if attention else gdn_mixer(xn, w))
-    return h + swiglu_mlp(Lr.rmsnorm(h, w["mlp_norm"]), w)
+    """One pre-norm residual decoder layer on one request: x [L, 4096] -> [L, 4096]."""
+    xx = f64(x)
+    L, H = xx.shape
+    keep = []
+    s = _layer_struct(w, attention, keep)
+    pos, pos3 = _positions(L, positions, keep)
+    out = np.empty((L, H))
+    check(lib().orc_decoder_layer(ptr(xx), L, H, ctypes.byref(s), ptr(pos), ptr(pos3), ptr(out)),
+          "decoder_layer")
+    return out
 
 
 def is_attention_layer(layer: int) -> bool:
-    return layer % 4 == 3
+    return bool(lib().orc_is_attention_layer(layer))
 
 
 def prefill(ids, embed_rows, layer_weights, final_norm, n_layers=32, positions=None):
     """The hybrid prefill of one request: ids [L] -> final-norm hidden [L, 4096] (float64).
 
-    "clef-flash-LiteRT" §Host contract steps 4-6: embedding rows at the request's ids in, every
-    position's output of the final RMSNorm out, each call from an empty state.  `embed_rows` is [L, 4096] (the table's rows at `ids`, gathered by the caller);
-    `layer_weights(l)` returns layer l's weight dict.  A request with a picture passes the
-    picture's rows in place of the table's rows where its <|image_pad|> tokens sit (step 4) and its
-    M-RoPE positions ([L, 3], :func:`oracle.layers.mrope_positions`; step 5).
+    `embed_rows` is [L, 4096] (the table's rows at `ids`, gathered by the caller; a request with a
+    picture passes the picture's rows where its image tokens sit); `layer_weights(l)` returns
+    layer l's weight dict; `positions` are M-RoPE positions [L, 3] (or [L], or None: 0 .. L-1).
     """
-    x = Lr.f64(embed_rows)
-    assert x.shape[0] == len(ids)
+    x = f64(embed_rows)
+    L, H = x.shape
+    assert L == len(ids)
+    keep = []
+    structs = (Layer * n_layers)()
     for layer in range(n_layers):
-        x = decoder_layer(x, layer_weights(layer), is_attention_layer(layer), positions)
-    return Lr.rmsnorm(x, final_norm)
+        structs[layer] = _layer_struct(layer_weights(layer), is_attention_layer(layer), keep)
+    fn = f16_bits(final_norm)
+    pos, pos3 = _positions(L, positions, keep)
+    out = np.empty((L, H))
+    check(lib().orc_prefill(ptr(x), L, H, structs, n_layers, ptr(fn), ptr(pos), ptr(pos3), ptr(out)),
+          "prefill")
+    return out
