@@ -13,8 +13,13 @@ With --gpus N (launched by torchrun, one rank per GPU) every rank runs its own r
 own requests: the path has no exchange step, so there is no collective on the data path
 (weak scaling); the barrier and the max-over-ranks timing are the only communication.
 
---impl reference times the oracle (plain fp64 numpy, CPU) as it stands, on a bounded sample of
-the same workload, in the same metric and unit; rank 0 only.
+The line's headline is --workload (default: one request of 16,384 positions); the metric's other
+workloads (one request of 512 positions, 32 requests of 512 positions in one launch sequence)
+are timed in the same run and reported under "workloads", each with its own step time, rooflines
+and end-to-end number.
+
+--impl reference times the oracle (plain C++ fp64 with OpenMP, CPU) as it stands, on a bounded
+sample of the same workload extrapolated per layer, in the same metric and unit; rank 0 only.
 """
 from __future__ import annotations
 
@@ -124,28 +129,78 @@ def job_tokens_per_s(B, L, steps, world, slowest_ms):
     return B * L * steps * world / (slowest_ms / 1000.0)
 
 
-def cpu_oracle_sample(seed, ids_row, n_tokens):
-    """Oracle seconds for one GDN layer and one attention layer on the first n_tokens of a request,
-    extrapolated to the 32-layer model (24 GDN + 8 attention layers): tokens/s."""
+# Algorithmic work of one prefill: every LUT-6 weight (and every fp16 a/b projection weight) is
+# 2 flops per token, attention 4 * 256 * 16 * L(L+1)/2 per request and layer, the gated delta
+# rule 6 d^2 per token and value head; padded or recomputed work is not counted.
+LUT6_WEIGHTS = 6_912_212_992
+AB_WEIGHTS = 24 * 2 * 32 * 4096          # the fp16 a/b projections of the GDN layers
+
+
+def step_flops(B, L):
+    gemm = 2.0 * (LUT6_WEIGHTS + AB_WEIGHTS) * B * L
+    attn = 8 * 4.0 * 256 * 16 * L * (L + 1) / 2 * B
+    gdn = 24 * 6.0 * 128 * 128 * 32 * B * L
+    return gemm + attn + gdn
+
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_rate(seed, ids_row, B, L, n1=64, n2=192, rows=8):
+    """The oracle (C++, fp64) timed on this host's cores, extrapolated per layer to B requests of
+    L positions.  A decoder layer's oracle time is a fixed part (dequantising its weights) plus a
+    part linear in the positions, plus for an attention layer the softmax over all earlier keys,
+    quadratic in L.  Timed: one GDN layer (layer 0) and one attention layer (layer 3) on the
+    first n1 and on the first n2 positions of the request (the two give the fixed and the
+    per-position parts), and the oracle's attention for the last `rows` query rows of a request
+    of the full length L (16 query heads over L keys: the cost per (row, key) pair).  Returns
+    (tokens/s for B x L, seconds of oracle time spent, description)."""
     import numpy as np
 
     import synth
+    from oracle import _lib
     from oracle import layers as Lr
     from oracle import model as om
 
-    ids = ids_row[:n_tokens]
-    x = synth.embedding_rows(seed, ids).astype(np.float64)
-    t_layer = {}
+    spent = 0.0
+    fit = {}
     for layer in (0, 3):
-        w = synth.layer_weights(seed, layer)
-        t0 = time.perf_counter()
-        om.decoder_layer(x, w, synth.is_attention_layer(layer))
-        t_layer[layer] = time.perf_counter() - t0
+        key = ("w", seed, layer)
+        if key not in _ORACLE_INPUTS:                  # drawn once per process, not timed
+            _ORACLE_INPUTS[key] = synth.layer_weights(seed, layer)
+        w = _ORACLE_INPUTS[key]
+        t = {}
+        for n in (n1, n2):
+            x = synth.embedding_rows(seed, ids_row[:n]).astype(np.float64)
+            t0 = time.perf_counter()
+            om.decoder_layer(x, w, synth.is_attention_layer(layer))
+            t[n] = time.perf_counter() - t0
+            spent += t[n]
+        per_pos = max(t[n2] - t[n1], 0.0) / (n2 - n1)
+        fit[layer] = (t[n1] - n1 * per_pos, per_pos)
+    r = min(rows, L)
+    key = ("qkv", seed, L)
+    if key not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[key] = (synth.normal_f64(seed, "cpu.q", 0, (L, 16, 256)),
+                               synth.normal_f64(seed, "cpu.k", 0, (L, 4, 256)),
+                               synth.normal_f64(seed, "cpu.v", 0, (L, 4, 256)))
+    q, k, v = _ORACLE_INPUTS[key]
     t0 = time.perf_counter()
-    Lr.rmsnorm(x, synth.final_norm_weight(seed))
-    t_final = time.perf_counter() - t0
-    total = 24 * t_layer[0] + 8 * t_layer[3] + t_final
-    return n_tokens / total, t_layer[0] + t_layer[3] + t_final
+    Lr.causal_attention(q, k, v, rows=(L - r, L))
+    t_rows = time.perf_counter() - t0
+    spent += t_rows
+    pairs = sum(L - i for i in range(r))                    # keys seen by the last r rows
+    per_pair = t_rows / pairs
+    c_g, s_g = fit[0]
+    c_a, s_a = fit[3]
+    per_request = (24 * (c_g + L * s_g) + 8 * (c_a + L * s_a + per_pair * L * (L + 1) / 2))
+    total = B * per_request
+    desc = (f"oracle (C++ fp64, {_lib.lib().orc_num_threads()} threads) extrapolated per layer to "
+            f"{B} x {L} positions: GDN layer 0 and attention layer 3 timed on the first {n1} and "
+            f"{n2} positions (fixed + per-position cost), the causal softmax timed on the last "
+            f"{r} query rows of a {L}-position request (its quadratic term at {L} keys); "
+            f"24 GDN + 8 attention layers")
+    return B * L / total, spent, desc
 
 
 def run_reference(args, wl):
@@ -153,49 +208,38 @@ def run_reference(args, wl):
     if rank != 0:
         return
     import synth
-    ids = synth.token_ids(0, wl["B"], wl["L"])
-    n_tok = 64
+    from oracle import _lib
+    ids = synth.token_ids(request_seed(0), wl["B"], wl["L"])
     vals = []
     for _ in range(args.warmup):
-        cpu_oracle_sample(0, ids[0], n_tok)
+        oracle_rate(0, ids[0], wl["B"], wl["L"], n1=32, n2=64, rows=4)
     t_all = 0.0
+    desc = ""
     for _ in range(args.steps):
-        v, t = cpu_oracle_sample(0, ids[0], n_tok)
+        v, t, desc = oracle_rate(0, ids[0], wl["B"], wl["L"], n1=32, n2=64, rows=4)
         vals.append(v)
         t_all += t
     value = statistics.median(vals)
-    cores = os.cpu_count()
-    sample = (f"oracle (fp64 numpy) on the first {n_tok} positions of the workload's first request: "
-              f"one GDN layer (layer 0) and one attention layer (layer 3) timed, scaled to 24 + 8 "
-              f"layers; the quadratic attention term is that of {n_tok} positions")
+    cores = int(_lib.lib().orc_num_threads())
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * t_all / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl["desc"], "global_batch": wl["B"], "seq_len": wl["L"]},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_clef(args, wl):
-    import numpy as np
+def measure(model, ids_np, steps, warmup, world, dev, lib_trace=True):
+    """Time `steps` prefills of the requests ids_np [B, L] (device-resident inputs), then the same
+    steps with the library's per-launch trace, then end to end from pinned host memory."""
     import torch
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
     import full_attention_prefill_gb300 as clef
-    import synth
-    from full_attention_prefill_gb300.model import synth_model
 
-    B, L = wl["B"], wl["L"]
-    model = synth_model(0, 32, device=dev)
-    ids_np = synth.token_ids(request_seed(rank), B, L)   # each rank: its own requests
+    B, L = ids_np.shape
     ids = torch.from_numpy(ids_np).to(dev)
     out = torch.empty((B, L, 4096), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -205,29 +249,29 @@ def run_clef(args, wl):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         model.forward(ids, out=out)
     clef.sync_status()
 
     # ---- timed region: device-resident inputs, no instrumentation
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     clocks.start()
     barrier()
     torch.cuda.synchronize(dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         model.forward(ids, out=out)
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     clef.sync_status()
-    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total_ms = slowest_rank_ms(ev[0].elapsed_time(ev[-1]), world, dev)
 
     # ---- the same steps again with the library's trace on (CUDA events around every launch,
     # on the launch stream): per-kernel times for the roofline and the breakdown
-    import ctypes
     lib = clef.lib()
     lib.clef_trace_begin.restype = ctypes.c_int
     lib.clef_trace_end.argtypes = [ctypes.POINTER(TraceEntry), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
@@ -235,18 +279,15 @@ def run_clef(args, wl):
     lib.clef_trace_begin()
     tv0, tv1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tv0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         model.forward(ids, out=out)
     tv1.record(stream)
     torch.cuda.synchronize(dev)
-    traced_ms = tv0.elapsed_time(tv1) / args.steps
+    traced_ms = tv0.elapsed_time(tv1) / steps
     entries = (TraceEntry * 32)()
     n = ctypes.c_int32(0)
     rc = lib.clef_trace_end(entries, 32, ctypes.byref(n))
     clef.sync_status()
-    total_ms = slowest_rank_ms(ev[0].elapsed_time(ev[-1]), world, dev)
-    tokens = B * L * args.steps * world
-    value = job_tokens_per_s(B, L, args.steps, world, total_ms)
     trace = {}
     if rc == 0:
         for i in range(n.value):
@@ -257,7 +298,7 @@ def run_clef(args, wl):
     ids_host = torch.from_numpy(ids_np).pin_memory()
     out_host = torch.empty((B, L, 4096), dtype=torch.float16).pin_memory()
     ids_dev = torch.empty_like(ids)
-    for _ in range(max(1, args.warmup // 2)):
+    for _ in range(max(1, warmup // 2)):
         ids_dev.copy_(ids_host, non_blocking=True)
         model.forward(ids_dev, out=out)
         out_host.copy_(out, non_blocking=True)
@@ -265,14 +306,66 @@ def run_clef(args, wl):
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         ids_dev.copy_(ids_host, non_blocking=True)
         model.forward(ids_dev, out=out)
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
-    e2e_value = job_tokens_per_s(B, L, args.steps, world, e2e_ms)
+    return dict(B=B, L=L, total_ms=total_ms, step_ms=step_ms, clocks=clk, trace=trace,
+                traced_ms=traced_ms, e2e_ms=e2e_ms, h2d=int(ids_host.numel() * 4),
+                d2h=int(out_host.numel() * 2))
+
+
+def summarize(r, steps, world, pk, traffic=None):
+    """The metric's numbers of one measured workload."""
+    B, L = r["B"], r["L"]
+    value = job_tokens_per_s(B, L, steps, world, r["total_ms"])
+    ms = r["total_ms"] / steps
+    g = r["trace"].get("lut6_gemm")
+    gemm = None
+    if g and g["ms"] > 0:
+        per_launch_flops = g["flops"] / g["launches"]
+        avg_ms = g["ms"] / g["launches"]
+        achieved = per_launch_flops / (avg_ms / 1000.0) / 1e12
+        gemm = {"bound": "tensor", "achieved": achieved, "peak": pk["tc_sust"], "unit": "TFLOP/s",
+                "frac": achieved / pk["tc_sust"], "traffic": traffic, "kernel": "lut6_gemm",
+                "peak_kind": f"bf16 dense sustained ({pk['source']}), fp16 same nominal rate",
+                "algorithmic_flops_per_launch": per_launch_flops, "avg_launch_ms": avg_ms}
+    sf = step_flops(B, L)
+    whole = {"bound": "tensor", "achieved": sf / (ms / 1000.0) / 1e12, "peak": pk["tc_sust"],
+             "unit": "TFLOP/s", "frac": sf / (ms / 1000.0) / 1e12 / pk["tc_sust"],
+             "algorithmic_flops_per_step": sf,
+             "what": "whole prefill: LUT-6 GEMMs + a/b projections + attention + gated delta rule"}
+    return dict(value=value, ms_per_step=ms, gemm=gemm, whole=whole,
+                e2e={"value": job_tokens_per_s(B, L, steps, world, r["e2e_ms"]), "unit": "tokens/s",
+                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+                launches=int(sum(t["launches"] for t in r["trace"].values()) / steps) if r["trace"] else None)
+
+
+def run_clef(args, wl):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import synth
+    from full_attention_prefill_gb300.model import synth_model
+
+    model = synth_model(0, 32, device=dev)
+    pk = peaks()
+    # the headline workload, then the metric's other workloads in the same run
+    names = [args.workload] + [w for w in ("l512", "b32x512", "l16384") if w != args.workload
+                               and not args.only_headline]
+    results = {}
+    for name in names:
+        w = WORKLOADS[name]
+        ids_np = synth.token_ids(request_seed(rank), w["B"], w["L"])   # each rank: its own requests
+        results[name] = measure(model, ids_np, args.steps, args.warmup, world, dev)
 
     if rank != 0:
         if world > 1:
@@ -280,43 +373,50 @@ def run_clef(args, wl):
             dist.destroy_process_group()
         return
 
-    pk = peaks()
-    g = trace.get("lut6_gemm")
-    roofline = None
-    if g and g["ms"] > 0:
-        per_launch_flops = g["flops"] / g["launches"]
-        avg_ms = g["ms"] / g["launches"]
-        achieved = per_launch_flops / (avg_ms / 1000.0) / 1e12
-        peak = pk["tc_sust"]
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak,
-                    "traffic": GEMM_DRAM_BYTES_PER_LAUNCH.get(args.workload), "kernel": "lut6_gemm",
-                    "peak_kind": f"bf16 dense sustained ({pk['source']}), fp16 same nominal rate",
-                    "algorithmic_flops_per_launch": per_launch_flops, "avg_launch_ms": avg_ms}
-    cpu_v, _ = cpu_oracle_sample(0, ids_np[0], 64)
+    head = results[args.workload]
+    hs = summarize(head, args.steps, world, pk, GEMM_DRAM_BYTES_PER_LAUNCH.get(args.workload))
+    ids0 = synth.token_ids(request_seed(0), 1, wl["L"])[0]
+    cpu_v, cpu_s, cpu_desc = oracle_rate(0, ids0, wl["B"], wl["L"])
+    trace = head["trace"]
     step_total = sum(t["ms"] for t in trace.values()) / args.steps if trace else None
+    others = {}
+    for name in names[1:]:
+        r = results[name]
+        sm = summarize(r, args.steps, world, pk, GEMM_DRAM_BYTES_PER_LAUNCH.get(name))
+        others[name] = {
+            "workload": WORKLOADS[name]["desc"], "global_batch": r["B"] * world, "seq_len": r["L"],
+            "value": sm["value"], "unit": "tokens/s", "ms_per_step": sm["ms_per_step"],
+            "step_ms": {"median": statistics.median(r["step_ms"]), "min": min(r["step_ms"]),
+                        "max": max(r["step_ms"])},
+            "roofline": sm["gemm"], "roofline_whole_step": sm["whole"], "e2e": sm["e2e"],
+            "gpu_launches_per_step": sm["launches"], "clocks": r["clocks"],
+            "kernels_ms_per_step": {k: round(v["ms"] / args.steps, 3)
+                                    for k, v in sorted(r["trace"].items(), key=lambda kv: -kv[1]["ms"])},
+            "traced_ms_per_step": r["traced_ms"],
+        }
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": hs["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": hs["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp16 activations, fp32 accumulate, LUT-6 weights",
         "data": "synthetic (seeded random LUT-6 weights and token ids)",
-        "config": {"workload": wl["desc"], "global_batch": B * world, "seq_len": L, "layers": 32,
+        "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["L"], "layers": 32,
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2 (5.2 GB of packed weights streamed per step)"},
-        "roofline": roofline,
-        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": "oracle (fp64 numpy) on the first 64 positions: one GDN and one "
-                                   "attention layer timed, scaled to 24 + 8 layers"},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(ids_host.numel() * 4),
-                "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "roofline": hs["gemm"],
+        "roofline_whole_step": hs["whole"],
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": int(__import__("oracle")._lib.lib().orc_num_threads()),
+                         "kind": "oracle", "sample": cpu_desc, "oracle_seconds": cpu_s},
+        "e2e": hs["e2e"],
         "gpu_launches": int(sum(t["launches"] for t in trace.values())) if trace else None,
-        "clocks": clk,
-        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "clocks": head["clocks"],
+        "step_ms": {"median": statistics.median(head["step_ms"]), "min": min(head["step_ms"]),
+                    "max": max(head["step_ms"])},
         "kernels_ms_per_step": {k: round(v["ms"] / args.steps, 3) for k, v in sorted(trace.items(), key=lambda kv: -kv[1]["ms"])},
         "kernel_time_sum_ms_per_step": step_total,
-        "traced_ms_per_step": traced_ms,
+        "traced_ms_per_step": head["traced_ms"],
         "kernel_times": "per-launch CUDA events on the launch stream, in a pass of the same steps "
                         "right after the timed region (the timed region runs without them)",
+        "workloads": others,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -477,6 +577,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["clef", "reference"], default="clef")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="l16384")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="time only --workload (the line then has no other workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -62,7 +62,11 @@ class Model(ctypes.Structure):
         ("embed", ctypes.c_void_p),
         ("vocab", ctypes.c_int64),
         ("final_norm", ctypes.c_void_p),
+        ("flags", ctypes.c_int32),
     ]
+
+
+MODEL_REPRODUCIBLE = 1
 
 
 class State(ctypes.Structure):
@@ -86,6 +90,8 @@ _SIGS = {
     "clef_debug_gdn_workspace_layout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                                        ctypes.c_void_p, ctypes.c_void_p]),
     "clef_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "clef_check_finite": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_void_p]),
     "clef_lut6_pack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "clef_lut6_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "clef_lut6_dequant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
@@ -97,6 +103,9 @@ _SIGS = {
     "clef_lut6_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                       ctypes.c_void_p]),
+    "clef_lut6_gemm_canonical_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "clef_lut6_gemm_canonical": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int32] + [ctypes.c_int64] * 3 +
+                                 [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "clef_gdn_workspace_size": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "clef_gdn_prefill": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int64, ctypes.c_int64,
                                                                   ctypes.c_void_p, ctypes.c_size_t,
@@ -168,6 +177,19 @@ def sync_status(stream=None):
     _check(lib().clef_sync_status(_stream(stream)), "clef_sync_status")
 
 
+def check_finite(x, stream=None):
+    """Device: per-row flags (uint8 [rows], 1 = the row holds an inf or a NaN) of an fp16 tensor
+    viewed as [rows, last dim]; a flagged row is also reported to sync_status()."""
+    _need_cuda(x)
+    if x.dtype != torch.float16 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous fp16 CUDA tensor")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    flags = torch.empty(rows, dtype=torch.uint8, device=x.device)
+    _check(lib().clef_check_finite(_ptr(x), rows, cols, _ptr(flags), _stream(stream)), "clef_check_finite")
+    return flags
+
+
 # ------------------------------------------------------------------------------------- LUT-6
 def lut6_pack(idx):
     """Host: pack uint8 indices [n, k] (numpy or CPU tensor) into [n, k*3/4] bytes."""
@@ -234,17 +256,21 @@ def lut6_quantize(w, stream=None):
 def lut6_gemm(x, packed, lut, out_fp32=False, out=None, stream=None, tiled=False):
     """Device: y = x . W^T for fp16 x [m, k] and LUT-6 W [n, k]; y fp16 (or fp32) [m, n].
 
-    `packed` is the canonical [n, k*3/4] stream, tiled here first, or (tiled=True) already in
-    the GEMM layout of lut6_tile."""
+    `packed` is the canonical [n, k*3/4] stream (clef_lut6_gemm_canonical, which tiles it into a
+    workspace first), or (tiled=True) already in the GEMM layout of lut6_tile (clef_lut6_gemm)."""
     _need_cuda(x, packed, lut)
     m, k = x.shape
     n = lut.shape[0] * 16
-    if not tiled and k % 64 == 0 and n % 16 == 0:
-        packed = lut6_tile(packed, k, stream)
     if out is None:
         out = torch.empty((m, n), dtype=torch.float32 if out_fp32 else torch.float16, device=x.device)
-    _check(lib().clef_lut6_gemm(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out), 1 if out_fp32 else 0,
-                                m, n, k, _stream(stream)), "clef_lut6_gemm")
+    if tiled:
+        _check(lib().clef_lut6_gemm(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out), 1 if out_fp32 else 0,
+                                    m, n, k, _stream(stream)), "clef_lut6_gemm")
+    else:
+        ws = _workspace(lib().clef_lut6_gemm_canonical_workspace_size(n, k), x.device)
+        _check(lib().clef_lut6_gemm_canonical(_ptr(x), _ptr(packed), _ptr(lut), _ptr(out),
+                                              1 if out_fp32 else 0, m, n, k, _ptr(ws), ws.numel(),
+                                              _stream(stream)), "clef_lut6_gemm_canonical")
     return out
 
 

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "glue.cuh"
 #include "lut6.cuh"
 
 namespace clef {
@@ -69,6 +70,24 @@ clef_status check_batch_len(int64_t B, int64_t L) {
     return CLEF_E_SHAPE;
   }
   return CLEF_OK;
+}
+
+// The lowest non-finite hidden row reported since the last clef_sync_status (one per device).
+__device__ unsigned long long g_bad_row_word = ~0ull;
+
+unsigned long long* bad_row_word_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static unsigned long long* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bad_row_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned long long*>(p);
+  }
+  return ptrs[dev];
 }
 
 int num_sms() {
@@ -261,8 +280,38 @@ clef_status clef_sync_status(clef_stream stream) {
     set_error("a weight given to the quantiser was not finite");
     return CLEF_E_NONFINITE;
   }
+  if (v == DEV_NONFINITE_HIDDEN) {
+    unsigned long long row = ~0ull, none = ~0ull;
+    unsigned long long* rp = bad_row_word_ptr();
+    if (rp) {
+      CLEF_CUDA_CHECK(cudaMemcpy(&row, rp, sizeof row, cudaMemcpyDeviceToHost));
+      CLEF_CUDA_CHECK(cudaMemcpy(rp, &none, sizeof none, cudaMemcpyHostToDevice));
+    }
+    set_error("hidden row %lld (row index b * L + t) is not finite, and maybe later rows: the "
+              "request overflowed fp16 and is rejected", (long long)row);
+    return CLEF_E_NONFINITE;
+  }
   set_error("a device wait ran out (code 0x%x)", v);
   return CLEF_E_DEVICE_TIMEOUT;
+}
+
+clef_status clef_check_finite(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* flags,
+                              clef_stream stream) {
+  if (rows < 0 || cols < 0 || (rows > 0 && !x)) {
+    set_error("clef_check_finite: NULL pointer or negative size");
+    return CLEF_E_INVALID;
+  }
+  if (cols % 8) {
+    set_error("clef_check_finite: cols = %lld is not a multiple of 8", (long long)cols);
+    return CLEF_E_SHAPE;
+  }
+  if (misaligned(x)) {
+    set_error("clef_check_finite: x must be 16-byte aligned");
+    return CLEF_E_ALIGN;
+  }
+  if (debug_should_fail()) return CLEF_E_CUDA;
+  return check_finite_launch(reinterpret_cast<const __half*>(x), rows, cols, flags,
+                             static_cast<cudaStream_t>(stream));
 }
 
 clef_status clef_lut6_pack(const uint8_t* idx, int64_t n, int64_t k, uint8_t* packed) {
@@ -341,6 +390,43 @@ clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k, uint8_t*
   }
   if (debug_should_fail()) return CLEF_E_CUDA;
   return lut6_tile_launch(packed, n, k, tiled, static_cast<cudaStream_t>(stream));
+}
+
+size_t clef_lut6_gemm_canonical_workspace_size(int64_t n, int64_t k) {
+  if (n <= 0 || k <= 0 || n % 16 || k % 64) return 0;
+  return (size_t)n * (size_t)(k / 4 * 3);
+}
+
+clef_status clef_lut6_gemm_canonical(const uint16_t* x, const uint8_t* packed, const uint16_t* lut,
+                                     void* y, int32_t y_is_fp32, int64_t m, int64_t n, int64_t k,
+                                     void* workspace, size_t workspace_bytes, clef_stream stream) {
+  if (m < 0 || n <= 0 || k <= 0) {
+    set_error("clef_lut6_gemm_canonical: bad size");
+    return CLEF_E_INVALID;
+  }
+  if (m == 0) return CLEF_OK;
+  if (!packed || !workspace) {
+    set_error("clef_lut6_gemm_canonical: NULL pointer");
+    return CLEF_E_INVALID;
+  }
+  if (n % 16 || k % 64) {
+    set_error("clef_lut6_gemm_canonical: need n %% 16 == 0 and k %% 64 == 0 (n=%lld k=%lld)",
+              (long long)n, (long long)k);
+    return CLEF_E_SHAPE;
+  }
+  if (workspace_bytes < clef_lut6_gemm_canonical_workspace_size(n, k)) {
+    set_error("clef_lut6_gemm_canonical: workspace of %zu bytes, need %zu", workspace_bytes,
+              clef_lut6_gemm_canonical_workspace_size(n, k));
+    return CLEF_E_WORKSPACE;
+  }
+  if (misaligned(workspace)) {
+    set_error("clef_lut6_gemm_canonical: workspace must be 16-byte aligned");
+    return CLEF_E_ALIGN;
+  }
+  const clef_status st = clef_lut6_tile(packed, n, k, static_cast<uint8_t*>(workspace), stream);
+  if (st != CLEF_OK) return st;
+  return clef_lut6_gemm(x, static_cast<const uint8_t*>(workspace), lut, y, y_is_fp32, m, n, k,
+                        stream);
 }
 
 clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,

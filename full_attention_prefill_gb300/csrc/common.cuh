@@ -26,9 +26,12 @@ enum DeviceCode : unsigned {
   DEV_TIMEOUT_EPILOGUE = 0x104,
   DEV_BAD_TOKEN = 0x201,
   DEV_NONFINITE = 0x202,
+  DEV_NONFINITE_HIDDEN = 0x203,
 };
 
 unsigned* status_word_ptr();          // device address of the status word (host side)
+// device address of the lowest row index reported with DEV_NONFINITE_HIDDEN (all ones: none)
+unsigned long long* bad_row_word_ptr();
 cudaError_t tma_encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
                           uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                           uint32_t box_outer, CUtensorMapSwizzle swz);
@@ -96,6 +99,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ void report(unsigned* status, unsigned code) {
   if (status) atomicCAS(status, 0u, code);
+}
+
+// A non-finite hidden row: the lowest such row index is kept beside the status word.
+__device__ __forceinline__ void report_bad_row(unsigned* status, unsigned long long* bad_row,
+                                               int64_t row) {
+  if (bad_row) atomicMin(bad_row, (unsigned long long)row);
+  report(status, DEV_NONFINITE_HIDDEN);
 }
 
 // ---- mbarrier ----

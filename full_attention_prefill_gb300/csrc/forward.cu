@@ -41,6 +41,7 @@ struct FwdWs {
   __half* mix;
   __half* h;
   void* scan;
+  float* part;     // k-part partial sums of the split residual adds (ordered reduction)
 };
 
 static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
@@ -65,6 +66,12 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
   t.mix = static_cast<__half*>(take(M * H * 2));
   t.h = static_cast<__half*>(take(M * I * 2));
   t.scan = take(gdn_scan_workspace_bytes(B, L, true));
+  {
+    // the residual adds (out-proj K = 4096, down K = 12288, N = 4096) split over k-parts only
+    // when there are few tiles; reproducible prefills keep each part's sums here
+    const int64_t parts = std::max(lut6_add_split(M, H, H), lut6_add_split(M, H, I));
+    t.part = parts > 1 ? static_cast<float*>(take((size_t)parts * M * H * 4)) : nullptr;
+  }
   if (w) *w = t;
   return off;
 }
@@ -88,8 +95,10 @@ struct LayerState {
 };
 
 static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, int64_t L,
-                             cudaStream_t s, const LayerState& st = LayerState()) {
+                             cudaStream_t s, const LayerState& st = LayerState(),
+                             bool reproducible = false) {
   const int64_t M = B * L;
+  float* part = reproducible ? w.part : nullptr;
   const __half* attn_norm = reinterpret_cast<const __half*>(ly.attn_norm);
   CLEF_TRY(rmsnorm_launch(w.x, attn_norm, w.xn, M, s));
   const __half* in_lut = reinterpret_cast<const __half*>(ly.in_proj.lut);
@@ -132,13 +141,13 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
   }
   CLEF_TRY(lut6_gemm_launch(w.mix, ly.out_proj.packed,
                             reinterpret_cast<const __half*>(ly.out_proj.lut), w.x, H, M, H, H,
-                            EPI_ADD_F32, s));
+                            EPI_ADD_F32, s, part));
   // MLP
   CLEF_TRY(rmsnorm_launch(w.x, reinterpret_cast<const __half*>(ly.mlp_norm), w.xn, M, s));
   CLEF_TRY(lut6_gemm_launch(w.xn, ly.gate_up.packed, reinterpret_cast<const __half*>(ly.gate_up.lut),
                             w.h, I, M, 2 * I, H, EPI_SWIGLU_F16, s));
   CLEF_TRY(lut6_gemm_launch(w.h, ly.down.packed, reinterpret_cast<const __half*>(ly.down.lut), w.x,
-                            H, M, H, I, EPI_ADD_F32, s));
+                            H, M, H, I, EPI_ADD_F32, s, part));
   return CLEF_OK;
 }
 
@@ -208,9 +217,11 @@ static clef_status prefill_impl(const char* who, const clef_model* model, const 
   if (image_rows) CLEF_TRY(image_rows_launch(image_rows, w.x, B, L, mr.start, mr.h * mr.w, s));
   LayerState ls;
   ls.mr = mr;
-  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+  const bool repro = (model->flags & CLEF_MODEL_REPRODUCIBLE) != 0;
+  for (int i = 0; i < model->n_layers; ++i)
+    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls, repro));
   return rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
-                        reinterpret_cast<__half*>(hidden), M, s);
+                        reinterpret_cast<__half*>(hidden), M, s, /*check_finite=*/true);
 }
 
 }  // namespace clef
@@ -451,10 +462,11 @@ clef_status clef_prefill_forward_chunk(const clef_model* model, const int32_t* i
       ls.vc = reinterpret_cast<__half*>(state->vcache) + (size_t)ai * per_layer;
       ++ai;
     }
-    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls,
+                       (model->flags & CLEF_MODEL_REPRODUCIBLE) != 0));
   }
   CLEF_TRY(rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
-                          reinterpret_cast<__half*>(hidden), M, s));
+                          reinterpret_cast<__half*>(hidden), M, s, /*check_finite=*/true));
   state->pos += L;
   return CLEF_OK;
 }

@@ -60,9 +60,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
   }
 }
 
+// With `status` set (the final norm) a row whose residual or normalised output is not finite
+// (an fp16 overflow somewhere upstream, or inf / NaN in the inputs) is reported: the status word
+// gets DEV_NONFINITE_HIDDEN and the lowest such row is kept in `bad_row`.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x,
                                                       const __half* __restrict__ w,
-                                                      __half* __restrict__ y) {
+                                                      __half* __restrict__ y, unsigned* status,
+                                                      unsigned long long* bad_row) {
   __shared__ float red[8];
   const int64_t tok = blockIdx.x;
   const int c0 = threadIdx.x * 16;
@@ -100,6 +104,42 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   uint4* dst = reinterpret_cast<uint4*>(y + tok * H + c0);
   dst[0] = out[0];
   dst[1] = out[1];
+  if (status) {
+    // exponent all ones in an fp16 output (inf or NaN), or a sum of squares that is not finite
+    // (which would make a huge but finite row come out as zeros)
+    bool bad = !isfinite(tot);
+    const uint32_t* o32 = reinterpret_cast<const uint32_t*>(out);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      bad |= ((o32[i] & 0x7C00u) == 0x7C00u) || ((o32[i] & 0x7C000000u) == 0x7C000000u);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) report_bad_row(status, bad_row, tok);
+  }
+}
+
+// Rows of fp16 values with an inf or a NaN: flags[row] = 1 (0 otherwise) when flags is set, and
+// the lowest such row is reported as for the final norm.  One warp per row, 8 values per load.
+__global__ void check_finite_kernel(const __half* __restrict__ x, int64_t rows, int64_t cols,
+                                    uint8_t* __restrict__ flags, unsigned* status,
+                                    unsigned long long* bad_row) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * cols);
+    bool bad = false;
+    for (int64_t i = lane; i < cols / 8; i += 32) {
+      const uint4 u = src[i];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        bad |= ((w[j] & 0x7C00u) == 0x7C00u) || ((w[j] & 0x7C000000u) == 0x7C000000u);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      if (flags) flags[row] = bad ? 1 : 0;
+      if (bad) report_bad_row(status, bad_row, row);
+    }
+  }
 }
 
 // ab = xn . W_ab^T: 64 tokens x 64 outputs per CTA, k streamed in blocks of 64 (cp.async double
@@ -223,10 +263,24 @@ clef_status image_rows_launch(const __half* rows, float* x, int64_t B, int64_t L
 }
 
 clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool check_finite) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "rmsnorm", 0.0, M * (4096.0 * 4 + 4096.0 * 2));
-  glue::rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(x, w, y);
+  glue::rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(
+      x, w, y, check_finite ? status_word_ptr() : nullptr,
+      check_finite ? bad_row_word_ptr() : nullptr);
+  CLEF_LAUNCH_CHECK();
+  return CLEF_OK;
+}
+
+clef_status check_finite_launch(const __half* x, int64_t rows, int64_t cols, uint8_t* flags,
+                                cudaStream_t stream) {
+  if (rows == 0) return CLEF_OK;
+  TraceScope ts(stream, "check_finite", 0.0, rows * cols * 2.0 + (flags ? rows : 0));
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+  glue::check_finite_kernel<<<(unsigned)blocks, 256, 0, stream>>>(x, rows, cols, flags,
+                                                                  status_word_ptr(),
+                                                                  bad_row_word_ptr());
   CLEF_LAUNCH_CHECK();
   return CLEF_OK;
 }

@@ -14,9 +14,15 @@ clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab,
 clef_status image_rows_launch(const __half* rows, float* x, int64_t B, int64_t L, int64_t start,
                               int64_t n, cudaStream_t stream);
 
-// y [M, 4096] fp16 = x * rsqrt(mean(x^2) + 1e-6) * w.
+// y [M, 4096] fp16 = x * rsqrt(mean(x^2) + 1e-6) * w.  With check_finite (the final norm), rows
+// whose residual or output is not finite are reported (DEV_NONFINITE_HIDDEN, lowest row kept).
 clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool check_finite = false);
+
+// Rows of an fp16 [rows, cols] array (cols % 8 == 0) holding an inf or a NaN: flags[row] = 1 / 0
+// (flags may be NULL), the lowest such row reported as by the final norm.
+clef_status check_finite_launch(const __half* x, int64_t rows, int64_t cols, uint8_t* flags,
+                                cudaStream_t stream);
 
 // [a | b] = xn [M, 4096] . W_ab^T, W_ab [64, 4096] fp16 (tensor cores), then the GDN gates
 // g [M, 32] = log(alpha) = -exp(A_log) softplus(a + dt_bias) (>= -30), beta [M, 32] = sigmoid(b).

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Drain this warp's 32 lanes x 64 columns of the accumulator of the tile at (n0e, m0e),
     // release it, then write Y from registers.
-    auto epilogue = [&](int n0e, int m0e, int ite) -> bool {
+    auto epilogue = [&](int n0e, int m0e, int ite, int kpart) -> bool {
       const int tok0 = m0e + ecol;
       const int col = n0e + quarter * 32 + lane;
       if (!mbar_wait(bar_accf, (uint32_t)ite & 1, status, DEV_TIMEOUT_EPILOGUE)) return false;
@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tok0 + 32 + i < M)
               out[(int64_t)(tok0 + 32 + i) * ldy] = __float2half_rn(__uint_as_float(r1[i]));
           }
-        } else if (mode == EPI_F32) {
-          float* out = reinterpret_cast<float*>(y) + col;
+        } else if (mode == EPI_F32 || mode == EPI_PART_F32) {
+          // a k-part of a split residual add goes to its own slice [kpart][M][ldy]
+          float* out = reinterpret_cast<float*>(y) + col +
+                       (mode == EPI_PART_F32 ? (int64_t)kpart * M * ldy : 0);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (tok0 + i < M) out[(int64_t)(tok0 + i) * ldy] = __uint_as_float(r0[i]);
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int64_t g = 0;
     int it = 0;
     bool ok = true;
-    int pn0 = -1, pm0 = 0;  // tile whose epilogue is pending
+    int pn0 = -1, pm0 = 0, pkp = 0;  // tile (and k-part) whose epilogue is pending
     for (int u = first; u < num_units && ok; u += stride, ++it) {
       int n0, m0;
       tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = sb + OFF_T + ts * TBL_BYTES + grp * 128;
       for (int kb = 0; kb < nkb; ++kb, ++g) {
         if (kb == lead && pn0 >= 0) {
-          ok = epilogue(pn0, pm0, it - 1);
+          ok = epilogue(pn0, pm0, it - 1, pkp);
           pn0 = -1;
           if (!ok) break;
         }
@@ -462,14 +464,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(bar_tempty + 8 * ts);  // done with this tile's tables
       pn0 = n0;
       pm0 = m0;
+      pkp = u / num_tiles;
     }
-    if (ok && pn0 >= 0) epilogue(pn0, pm0, it - 1);
+    if (ok && pn0 >= 0) epilogue(pn0, pm0, it - 1, pkp);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// y[t][c] += part[0][t][c] + part[1][t][c] + ... added one part at a time in part order (the
+// same sequence of fp32 additions on every run); part is [parts][M][N].  Four columns per thread.
+__global__ void split_reduce_kernel(float* __restrict__ y, int64_t ldy, const float* __restrict__ part,
+                                    int parts, int64_t M, int64_t N) {
+  const int64_t quads = M * (N / 4);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < quads;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / (N / 4), c = 4 * (i % (N / 4));
+    float4 acc = *reinterpret_cast<const float4*>(y + t * ldy + c);
+    for (int p = 0; p < parts; ++p) {
+      const float4 v = *reinterpret_cast<const float4*>(part + ((int64_t)p * M + t) * N + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(y + t * ldy + c) = acc;
   }
 }
 
@@ -514,9 +537,30 @@ __global__ void lut6_tile_kernel(const uint8_t* __restrict__ packed, int64_t n, 
 
 }  // namespace lut
 
+int lut6_add_split(int64_t M, int64_t N, int64_t K) {
+  // When there are too few tiles to fill the GPU, pick the split that minimises the longest
+  // CTA's work, counted in k-steps plus about four steps per unit for its epilogue.
+  using namespace lut;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);
+  const int64_t sms = num_sms();
+  const int64_t nkb = K / BK;
+  int ksplit = 1;
+  int64_t best = -1;
+  for (int s = 1; s <= 8; ++s) {
+    if (nkb % s != 0 || nkb / s < 4) continue;
+    const int64_t rounds = (tiles * s + sms - 1) / sms;
+    const int64_t cost = rounds * (nkb / s + 4);
+    if (best < 0 || cost < best) {
+      best = cost;
+      ksplit = s;
+    }
+  }
+  return ksplit;
+}
+
 clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, float* part_ws) {
   using namespace lut;
   if (M == 0) return CLEF_OK;
   CUtensorMap tx, tp;
@@ -538,34 +582,34 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   if ((reinterpret_cast<uintptr_t>(lut) & 15) != 0) return CLEF_E_ALIGN;
   const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);
   const int sms = num_sms();
-  // Residual-add mode may split K across CTAs (each part adds its partial sum): when there are
-  // too few tiles to fill the GPU, pick the split that minimises the longest CTA's work, counted
-  // in k-steps plus about four steps per unit for its epilogue.
-  int ksplit = 1;
-  if (mode == EPI_ADD_F32) {
-    const int64_t nkb = K / BK;
-    int64_t best = -1;
-    for (int s = 1; s <= 8; ++s) {
-      if (nkb % s != 0 || nkb / s < 4) continue;
-      const int64_t rounds = (tiles * s + sms - 1) / sms;
-      const int64_t cost = rounds * (nkb / s + 4);
-      if (best < 0 || cost < best) {
-        best = cost;
-        ksplit = s;
-      }
-    }
-  }
+  // Residual-add mode may split K across CTAs (each part adds its partial sum, or with part_ws
+  // writes it to its own slice for the ordered reduction below)
+  const int ksplit = mode == EPI_ADD_F32 ? lut6_add_split(M, N, K) : 1;
+  const bool ordered = ksplit > 1 && part_ws != nullptr;
+  if (ordered && (N % 4 != 0 || ldy % 4 != 0 || (reinterpret_cast<uintptr_t>(part_ws) & 15) != 0))
+    return CLEF_E_ALIGN;
   const int64_t units = tiles * ksplit;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
   const double out_bytes = mode == EPI_F16 ? 2.0 * M * N
                            : mode == EPI_F32 ? 4.0 * M * N
                            : mode == EPI_ADD_F32 ? 8.0 * M * N
                                                  : 1.0 * M * N;  // SwiGLU: fp16 [M, N/2]
-  TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
-                0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
-  lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, ksplit, status_word_ptr());
-  CLEF_LAUNCH_CHECK();
+  {
+    TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
+                  0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
+    lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        tx, tp, lut, ordered ? static_cast<void*>(part_ws) : y, ordered ? N : ldy, (int)M, (int)N,
+        (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, status_word_ptr());
+    CLEF_LAUNCH_CHECK();
+  }
+  if (ordered) {
+    TraceScope ts(stream, "split_reduce", 0.0, 4.0 * M * N * (2 + ksplit));
+    const int64_t quads = M * (N / 4);
+    const int64_t blocks = std::min<int64_t>((quads + 255) / 256, (int64_t)sms * 8);
+    split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(y), ldy, part_ws,
+                                                              ksplit, M, N);
+    CLEF_LAUNCH_CHECK();
+  }
   return CLEF_OK;
 }
 

@@ -50,7 +50,8 @@ typedef enum {
   CLEF_E_ALIGN = 4,            /* a device pointer not 16-byte aligned                       */
   CLEF_E_CUDA = 5,             /* a CUDA runtime/driver call failed                          */
   CLEF_E_DEVICE_TIMEOUT = 6,   /* a device wait ran out (from clef_sync_status)              */
-  CLEF_E_NONFINITE = 7,        /* a non-finite weight given to the quantiser (sync_status)   */
+  CLEF_E_NONFINITE = 7,        /* not finite: a quantiser weight, or a prefill's hidden row
+                                  (from clef_sync_status; see clef_check_finite)             */
   CLEF_E_WORKSPACE = 8,        /* workspace smaller than the size query returned             */
   CLEF_E_BAD_TOKEN = 9         /* a token id outside [0, vocab) (from clef_sync_status)      */
 } clef_status;
@@ -136,6 +137,20 @@ CLEF_API clef_status clef_lut6_quantize(const uint16_t* w, int64_t n, int64_t k,
 CLEF_API clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* tiled, const uint16_t* lut,
                                     void* y, int32_t y_is_fp32, int64_t m, int64_t n, int64_t k,
                                     clef_stream stream);
+
+/* device: the same product with W given in the card's own 4-in-3 packing (`packed` [n, k*3/4],
+   the row-major bit stream of clef_lut6_pack).  The GEMM's tensor-memory dequantisation reads a
+   lane's 32 indices of one k-block as 24 contiguous bytes, which the card's row-major stream
+   does not give, so this call first writes the tiled permutation (clef_lut6_tile) into the
+   caller's workspace, then runs clef_lut6_gemm on it: one extra pass over the packed bytes per
+   call.  A caller that multiplies by the same weight many times should tile it once and call
+   clef_lut6_gemm.  workspace: device, >= clef_lut6_gemm_canonical_workspace_size(n, k) bytes,
+   16-byte aligned (CLEF_E_WORKSPACE if smaller).  Other requirements as clef_lut6_gemm. */
+CLEF_API size_t clef_lut6_gemm_canonical_workspace_size(int64_t n, int64_t k);
+CLEF_API clef_status clef_lut6_gemm_canonical(const uint16_t* x, const uint8_t* packed,
+                                              const uint16_t* lut, void* y, int32_t y_is_fp32,
+                                              int64_t m, int64_t n, int64_t k, void* workspace,
+                                              size_t workspace_bytes, clef_stream stream);
 
 /* ------------------------------------------------------------------------------------------
  * Gated DeltaNet scan ("Clef-Flash-ANE-LUT6" section "Model architecture"; "clef-flash - Core
@@ -230,7 +245,16 @@ typedef struct {
   const uint16_t* embed;     /* [vocab, 4096] fp16 token embeddings */
   int64_t vocab;             /* 248320 for clef-flash */
   const uint16_t* final_norm;/* [4096] fp16 */
+  int32_t flags;             /* 0, or CLEF_MODEL_REPRODUCIBLE */
 } clef_model;
+
+/* clef_model.flags: make every run of the same prefill give the same bits.  Short prefills
+   split the residual-add projections (out-proj, MLP down) over k-parts to fill the GPU; by
+   default each part adds its partial sum into the fp32 residual as it finishes, so the order of
+   those fp32 additions (and the last bits of the result) can change from run to run.  With this
+   flag each part writes its sums to the workspace and one more kernel adds them in part order.
+   Long prefills (no split) are reproducible either way. */
+#define CLEF_MODEL_REPRODUCIBLE 1
 
 /* Bytes of workspace clef_prefill_forward / clef_decoder_layer need for B requests of L
    positions. */
@@ -241,7 +265,10 @@ CLEF_API size_t clef_prefill_workspace_size(int64_t B, int64_t L);
    (right-padded to a bucket by the caller: padding rows are computed like real tokens and, by
    causality, never change the real rows).  1 <= L <= CLEF_MAX_LEN (CLEF_E_TOO_LONG above),
    B >= 1.  Ids outside [0, vocab) set CLEF_E_BAD_TOKEN in the device status (their rows are
-   zero).  Residual stream in fp32, activations between kernels in fp16. */
+   zero).  Residual stream in fp32, activations between kernels in fp16.  A hidden row that is
+   not finite (an activation overflowed fp16, or an embedding or picture row held inf / NaN)
+   sets CLEF_E_NONFINITE in the device status, naming the lowest such row: the request is to be
+   rejected, as the pages reject inputs that overflow FP16 (see clef_check_finite). */
 CLEF_API clef_status clef_prefill_forward(const clef_model* model, const int32_t* ids, int64_t B, int64_t L,
                                  uint16_t* hidden, void* workspace, size_t workspace_bytes,
                                  clef_stream stream);
@@ -319,8 +346,20 @@ CLEF_API clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64
                                void* workspace, size_t workspace_bytes, clef_stream stream);
 
 /* Wait for `stream`, then read and clear the device status word.  Returns CLEF_OK,
-   CLEF_E_DEVICE_TIMEOUT, CLEF_E_BAD_TOKEN or CLEF_E_CUDA. */
+   CLEF_E_DEVICE_TIMEOUT, CLEF_E_BAD_TOKEN, CLEF_E_NONFINITE or CLEF_E_CUDA.  For a non-finite
+   hidden row the message names the lowest such row index (b * L + t). */
 CLEF_API clef_status clef_sync_status(clef_stream stream);
+
+/* device: which rows of an fp16 array x [rows, cols] hold an inf or a NaN.  The analogue of the
+   pages' rejection of FP16 overflow ("Clef-Flash-ANE-LUT6", section "Vision weights": the
+   largest residual met, about 12,400, is within FP16's range, and inputs that overflow are
+   rejected rather than answered).  flags [rows] (device, caller owned, may be NULL) receives 1
+   for such a row and 0 otherwise; if any row is flagged, the status word reports
+   CLEF_E_NONFINITE with the lowest row (clef_sync_status).  Every prefill entry point already
+   checks its final-norm output this way (without the per-row flags).  cols % 8 == 0, x 16-byte
+   aligned.  Asynchronous on `stream`. */
+CLEF_API clef_status clef_check_finite(const uint16_t* x, int64_t rows, int64_t cols,
+                                       uint8_t* flags, clef_stream stream);
 
 /* Per-kernel-class device time.  Between clef_trace_begin() and clef_trace_end(), every kernel
    the library launches (from any thread) is bracketed by CUDA events on its own stream.

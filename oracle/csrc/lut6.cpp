@@ -12,6 +12,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <memory>
+
 #include "internal.h"
 
 namespace orc {
@@ -145,8 +147,9 @@ int orc_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_t n, int6
   for (int64_t r = 0; r < n; ++r) {
     std::vector<uint8_t> idx((size_t)k);
     orc_lut6_unpack(packed + r * (k / 4) * 3, 1, k, idx.data());
-    const uint16_t* table = lut + (r / 16) * 64;
-    for (int64_t c = 0; c < k; ++c) w[r * k + c] = half_to_double(table[idx[(size_t)c]]);
+    double table[64];                                       // row r's group table, widened
+    for (int j = 0; j < 64; ++j) table[j] = half_to_double(lut[(r / 16) * 64 + j]);
+    for (int64_t c = 0; c < k; ++c) w[r * k + c] = table[idx[(size_t)c]];
   }
   return 0;
 }
@@ -154,9 +157,9 @@ int orc_lut6_dequant(const uint8_t* packed, const uint16_t* lut, int64_t n, int6
 int orc_lut6_linear(const double* x, int64_t m, int64_t k, const uint8_t* packed,
                     const uint16_t* lut, int64_t n, double* y) {
   if (m < 0 || n < 0 || n % 16 || k < 0 || k % 4) return fail(-1, "linear: bad shape");
-  std::vector<double> W((size_t)(n * k));
-  orc_lut6_dequant(packed, lut, n, k, W.data());
-  dense_linear(x, m, k, W.data(), n, y);
+  std::unique_ptr<double[]> W(new double[(size_t)(n * k)]);  // every entry written below
+  orc_lut6_dequant(packed, lut, n, k, W.get());
+  dense_linear(x, m, k, W.get(), n, y);
   return 0;
 }
 

@@ -90,3 +90,26 @@ def test_tile_layout_moves_whole_quadruples():
                     for j in range(4):
                         expect[G, kb, t, h, j] = trip[16 * G + t // 4 + 8 * h, 16 * kb + 4 * j + t % 4]
     assert np.array_equal(tiled, expect.reshape(-1))
+
+
+def test_canonical_entry_equals_tiled_entry():
+    """clef_lut6_gemm_canonical on the card's own packing gives the same bits as clef_lut6_gemm on
+    the tiled permutation, and refuses a workspace smaller than its size query."""
+    import ctypes
+    m, n, k = 300, 784, 320
+    x = _dev(synth.normal_f16(4, "x", 0, (m, k)))
+    packed, lut = synth.lut6_weight(4, "w", 0, n, k)
+    p, l = _dev(packed), _dev(lut)
+    a = clef.lut6_gemm(x, p, l)                                  # canonical bytes in
+    b = clef.lut6_gemm(x, clef.lut6_tile(p, k), l, tiled=True)   # tiled once, then multiplied
+    clef.sync_status()
+    assert torch.equal(a, b)
+    need = clef.lib().clef_lut6_gemm_canonical_workspace_size(n, k)
+    assert need == n * k * 3 // 4
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    y = torch.empty((m, n), dtype=torch.float16, device="cuda")
+    rc = clef.lib().clef_lut6_gemm_canonical(
+        ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(p.data_ptr()), ctypes.c_void_p(l.data_ptr()),
+        ctypes.c_void_p(y.data_ptr()), 0, m, n, k, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 8                                               # CLEF_E_WORKSPACE

@@ -71,3 +71,23 @@ def test_full_model_l512():
     e = rel_rmse(hid, ref)
     print(f"32-layer L=512: rel-RMSE {e:.2e}, min row cos {min_row_cosine(hid, ref):.6f}")
     assert e < FINAL_TOL
+
+
+@pytest.mark.slow
+def test_reproducible_prefill_is_bit_identical():
+    """With CLEF_MODEL_REPRODUCIBLE the split residual adds of a short prefill are summed in part
+    order, so two runs of the same 32-layer L = 512 request give the same bits; the result stays
+    within fp32 rounding of the default (unordered) path."""
+    seed, L = 0, 512
+    m = synth_model(seed, 32)
+    ids = torch.from_numpy(synth.token_ids(seed, 1, L)).cuda()
+    fast = m.forward(ids).clone()
+    m.set_reproducible(True)
+    try:
+        a = m.forward(ids).clone()
+        b = m.forward(ids).clone()
+        clef.sync_status()
+    finally:
+        m.set_reproducible(False)
+    assert torch.equal(a, b)
+    assert rel_rmse(a.double().cpu().numpy(), fast.double().cpu().numpy()) < 1e-2
