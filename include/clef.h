@@ -301,6 +301,62 @@ CLEF_API clef_status clef_prefill_forward_image(const clef_model* model, const i
                                                 size_t workspace_bytes, clef_stream stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Joint schema head on the hidden states of one request ("clef-flash - Core AI" README,
+ * sections "Readout contract" and "Core AI shape", Head; "Clef-Flash-ANE-LUT6", section "Model
+ * architecture": 4 layers of width 1,024, 16 heads, 2 routing layers; "clef-flash-LiteRT",
+ * section "Host contract" step 7).  What the pages fix: the inputs (the request's final-norm
+ * hidden rows; the span means q_avg [Q, T] and o_avg [O, T] with 1 / len over each span; g_avg
+ * [T] picking the last real token; lexical [O, 4096], each option's mean lm_head row; member
+ * [Q, O], which question each option belongs to; question types; validity of keys, questions and
+ * options), one logit per option out, and each question's probabilities a float32 softmax over
+ * its options.  The layers between are this library's reading (the pages do not give them),
+ * with width 1,024 and 16 heads of 64:
+ *   slots (Q questions, O options, 1 global row) = span means . W_in^T (4096 -> 1024), plus the
+ *     question-type embedding, plus (options) lexical . W_lex^T and an option embedding, plus
+ *     (global) a global embedding; memory = hidden . W_mem^T (4096 -> 1024);
+ *   4 decoder layers: s += Attention(rmsnorm(s) -> q; memory -> k, v; valid keys only) . W_o^T,
+ *     then s += SwiGLU(rmsnorm(s)) (1024 -> 4096 -> 1024);
+ *   2 routing layers: the same with the slots attending to the valid slots;
+ *   f = rmsnorm(s); logit_o = (f_o W_opt^T) . (f_q(o) W_qst^T) / 32, q(o) the question of o;
+ *   RMSNorm eps 1e-6; attention scale 1/8; invalid options get logit 0 and probability 0.
+ * Weights: fp16, [out, in] row-major, device, 16-byte aligned, caller owned.
+ * hidden [T, 4096] fp16 (the prefill's output for one request); key_valid [T], member [Q][O],
+ * q_valid [Q], o_valid [O] uint8 (0 / 1); type_ids [Q] int32 in 0..2 (others clamp); q_avg, o_avg, g_avg,
+ * lexical fp32; out logits [O], probs [O] fp32.  All device, caller owned.  1 <= T <=
+ * CLEF_MAX_LEN, 1 <= Q <= 16, 1 <= O <= 128 (the pages' head pads to 16 questions and 128
+ * options); CLEF_E_SHAPE otherwise.  Workspace: clef_joint_head_workspace_size(T, Q, O) bytes.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  const uint16_t* norm1;             /* [1024] */
+  const uint16_t *wq, *wk, *wv, *wo; /* [1024, 1024] */
+  const uint16_t* norm2;             /* [1024] */
+  const uint16_t *wg, *wu;           /* [4096, 1024] */
+  const uint16_t* wd;                /* [1024, 4096] */
+} clef_head_layer;
+
+typedef struct {
+  const uint16_t *w_mem, *w_in, *w_lex; /* [1024, 4096] */
+  const uint16_t* e_qtype;              /* [3, 1024]: noul, choice, score */
+  const uint16_t *e_opt, *e_glob;       /* [1024] */
+  clef_head_layer dec[4];               /* decoder layers (slots attend to the tokens) */
+  clef_head_layer route[2];             /* routing layers (slots attend to each other) */
+  const uint16_t* norm_f;               /* [1024] */
+  const uint16_t *w_opt, *w_qst;        /* [1024, 1024] */
+} clef_head;
+
+#define CLEF_HEAD_MAX_Q 16
+#define CLEF_HEAD_MAX_O 128
+
+CLEF_API size_t clef_joint_head_workspace_size(int64_t T, int64_t Q, int64_t O);
+CLEF_API clef_status clef_joint_head(const clef_head* head, const uint16_t* hidden,
+                                     const uint8_t* key_valid, int64_t T, const float* q_avg,
+                                     const float* o_avg, const float* g_avg, const float* lexical,
+                                     const uint8_t* member, const int32_t* type_ids,
+                                     const uint8_t* q_valid, const uint8_t* o_valid, int64_t Q,
+                                     int64_t O, float* logits, float* probs, void* workspace,
+                                     size_t workspace_bytes, clef_stream stream);
+
+/* ------------------------------------------------------------------------------------------
  * Chunked prefill with carried state ("clef-flash - Core AI" README, section "Core AI shape": a
  * request is prefilled as successive calls of 64 positions from zeroed states, each carrying the
  * key and value caches of the attention layers and the conv and recurrent states of the Gated

@@ -9,7 +9,7 @@ The oracle is plain C++17 with OpenMP (``oracle/csrc``, built into ``oracle/libo
 step follows the pages' description in the pages' order with no blocking, fusion or reordering
 beyond the definitions: the gated delta rule as the per-token recurrence, attention as one
 explicit softmax per query row, each GEMM output one dot product.  The Python modules
-``lut6``, ``layers``, ``model`` and ``quantize`` only marshal numpy arrays into its C ABI
+``lut6``, ``layers``, ``model``, ``quantize`` and ``head`` only marshal numpy arrays into its C ABI
 (``oracle/csrc/oracle.h``).
 
 ``oracle/twin`` is a second, independent writing of the same definitions in numpy; it is used
@@ -27,4 +27,4 @@ Sources (cited by page title and section in each function):
 Functions whose result no page or closed form fixes are marked "parity unpinned" (the
 end-to-end activations: no page prints any).
 """
-from . import layers, lut6, model, quantize  # noqa: F401
+from . import head, layers, lut6, model, quantize  # noqa: F401

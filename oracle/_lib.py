@@ -68,6 +68,8 @@ _SIGS = {
     "orc_quant_kmeans_round": (None, [vp, c_i64, vp, c_i64]),
     "orc_quant_group": (None, [vp, c_i64, c_i32, vp, vp]),
     "orc_lut6_quantize": (ctypes.c_int, [vp, c_i64, c_i64, c_i32, vp, vp]),
+    "orc_joint_head": (ctypes.c_int, [vp, vp, c_i64, vp, vp, vp, vp, vp, vp, vp, vp, c_i64, c_i64, vp,
+                                      vp, vp]),
 }
 
 

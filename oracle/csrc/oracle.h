@@ -151,6 +151,43 @@ void orc_quant_group(const double* values, int64_t n, int32_t rounds, uint16_t* 
 int orc_lut6_quantize(const uint16_t* w, int64_t n, int64_t k, int32_t rounds, uint8_t* packed,
                       uint16_t* lut);
 
+/* ------------------------------------------------------------------ the joint schema head
+ * "clef-flash - Core AI" README, Readout contract and Core AI shape (Head): the head reads the
+ * final-norm hidden rows of one request; q_avg [Q, T] and o_avg [O, T] average them over each
+ * question's and option's span (1 / len on the span), g_avg [T] picks the last real token,
+ * lexical [O, 4096] is each option's mean lm_head row, member [Q, O] says which question an
+ * option belongs to; the output is one logit per option, and each question's probabilities are
+ * a softmax over its options.  "Clef-Flash-ANE-LUT6", Model architecture: 4 layers, width 1,024,
+ * 16 heads, 2 routing layers ("clef-flash-LiteRT", Host contract step 7: 2 routing layers and 4
+ * decoder layers over the request's tokens).  The layers themselves are not on the pages; their
+ * form here is a reading (orc_joint_head in head.cpp states it). */
+typedef struct {
+  const uint16_t* norm1;             /* [1024] */
+  const uint16_t *wq, *wk, *wv, *wo; /* [1024, 1024] */
+  const uint16_t* norm2;             /* [1024] */
+  const uint16_t *wg, *wu;           /* [4096, 1024] */
+  const uint16_t* wd;                /* [1024, 4096] */
+} orc_head_layer;
+
+typedef struct {
+  const uint16_t *w_mem, *w_in, *w_lex; /* [1024, 4096] */
+  const uint16_t* e_qtype;              /* [3, 1024] question types noul / choice / score */
+  const uint16_t *e_opt, *e_glob;       /* [1024] */
+  orc_head_layer dec[4];                /* decoder layers: slots attend to the request's tokens */
+  orc_head_layer route[2];              /* routing layers: slots attend to each other */
+  const uint16_t* norm_f;               /* [1024] */
+  const uint16_t *w_opt, *w_qst;        /* [1024, 1024] */
+} orc_head;
+
+/* hidden [T, 4096]; key_valid [T]; q_avg [Q, T]; o_avg [O, T]; g_avg [T]; lexical [O, 4096];
+ * member [Q, O] (0 / 1); type_ids [Q] in 0..2; q_valid [Q]; o_valid [O]; out: logits [O] and
+ * probs [O] (0 for an option of no valid question, or an invalid option). */
+int orc_joint_head(const double* hidden, const uint8_t* key_valid, int64_t T, const double* q_avg,
+                   const double* o_avg, const double* g_avg, const double* lexical,
+                   const uint8_t* member, const int32_t* type_ids, const uint8_t* q_valid,
+                   const uint8_t* o_valid, int64_t Q, int64_t O, const orc_head* w,
+                   double* logits, double* probs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -190,3 +190,78 @@ def embedding_rows(seed, ids):
 def token_ids(seed, batch, length, name="ids"):
     """Uniform token ids over the 248,320-token vocabulary, int32 [batch, length]."""
     return uniform_int(seed, name, -1, (batch, length), VOCAB)
+
+
+# ----------------------------------------------------------------------------------------------
+# Joint schema head (synthetic weights; width 1,024, 16 heads, 4 decoder + 2 routing layers).
+# Projections N(0, 1/fan_in), norm weights 1 + N(0, 0.02), embeddings N(0, 0.5), all fp16.
+# ----------------------------------------------------------------------------------------------
+HEAD_D = 1024
+HEAD_FF = 4096
+
+
+def head_layer_weights(seed, name, layer):
+    d, ff = HEAD_D, HEAD_FF
+    w = {"norm1": norm_weight(seed, f"{name}.norm1", layer, d),
+         "norm2": norm_weight(seed, f"{name}.norm2", layer, d)}
+    for p in ("wq", "wk", "wv", "wo"):
+        w[p] = normal_f16(seed, f"{name}.{p}", layer, (d, d), 0.0, d ** -0.5)
+    w["wg"] = normal_f16(seed, f"{name}.wg", layer, (ff, d), 0.0, d ** -0.5)
+    w["wu"] = normal_f16(seed, f"{name}.wu", layer, (ff, d), 0.0, d ** -0.5)
+    w["wd"] = normal_f16(seed, f"{name}.wd", layer, (d, ff), 0.0, ff ** -0.5)
+    return w
+
+
+def head_weights(seed):
+    """All parameters of the joint schema head (names are the recipe)."""
+    d = HEAD_D
+    w = {"w_mem": normal_f16(seed, "head.w_mem", -1, (d, HIDDEN), 0.0, HIDDEN ** -0.5),
+         "w_in": normal_f16(seed, "head.w_in", -1, (d, HIDDEN), 0.0, HIDDEN ** -0.5),
+         "w_lex": normal_f16(seed, "head.w_lex", -1, (d, HIDDEN), 0.0, HIDDEN ** -0.5),
+         "e_qtype": normal_f16(seed, "head.e_qtype", -1, (3, d), 0.0, 0.5),
+         "e_opt": normal_f16(seed, "head.e_opt", -1, (d,), 0.0, 0.5),
+         "e_glob": normal_f16(seed, "head.e_glob", -1, (d,), 0.0, 0.5),
+         "norm_f": norm_weight(seed, "head.norm_f", -1, d),
+         "w_opt": normal_f16(seed, "head.w_opt", -1, (d, d), 0.0, d ** -0.5),
+         "w_qst": normal_f16(seed, "head.w_qst", -1, (d, d), 0.0, d ** -0.5)}
+    w["dec"] = [head_layer_weights(seed, "head.dec", l) for l in range(4)]
+    w["route"] = [head_layer_weights(seed, "head.route", l) for l in range(2)]
+    return w
+
+
+def head_request(seed, T, questions):
+    """A synthetic decision request's head inputs for T hidden rows: `questions` is a list of
+    option counts.  Spans are drawn as disjoint runs of positions (questions' spans, then each
+    option's), the global row is the last position; lexical rows N(0, 0.02) (the size of an
+    lm_head row mean).  Returns a dict of numpy arrays (q_avg, o_avg, g_avg, lexical, member,
+    type_ids, q_valid, o_valid, key_valid, q_span, o_span)."""
+    Q, O = len(questions), int(sum(questions))
+    lens = uniform_int(seed, "head.span_len", -1, (Q + O,), 7) + 2      # spans of 2..8 positions
+    starts = uniform_int(seed, "head.span_gap", -1, (Q + O,), 3)
+    q_avg = np.zeros((Q, T))
+    o_avg = np.zeros((O, T))
+    pos, spans = 1, []
+    for i in range(Q + O):
+        pos += int(starts[i])
+        spans.append((pos, pos + int(lens[i])))
+        pos += int(lens[i])
+    assert pos < T, "T too short for the spans"
+    for q in range(Q):
+        a, b = spans[q]
+        q_avg[q, a:b] = 1.0 / (b - a)
+    member = np.zeros((Q, O), dtype=np.uint8)
+    o = 0
+    for q, n in enumerate(questions):
+        for _ in range(n):
+            a, b = spans[Q + o]
+            o_avg[o, a:b] = 1.0 / (b - a)
+            member[q, o] = 1
+            o += 1
+    g_avg = np.zeros(T)
+    g_avg[T - 1] = 1.0
+    return {"q_avg": q_avg, "o_avg": o_avg, "g_avg": g_avg,
+            "lexical": normal_f64(seed, "head.lexical", -1, (O, HIDDEN), 0.0, 0.02),
+            "member": member, "type_ids": (uniform_int(seed, "head.type", -1, (Q,), 3)),
+            "q_valid": np.ones(Q, dtype=np.uint8), "o_valid": np.ones(O, dtype=np.uint8),
+            "key_valid": np.ones(T, dtype=np.uint8),
+            "q_span": spans[:Q], "o_span": spans[Q:]}
