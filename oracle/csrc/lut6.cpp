@@ -61,27 +61,31 @@ static void dot_2x2(const double* x0, const double* x1, const double* w0, const 
 
 void dense_linear(const double* x, int64_t m, int64_t k, const double* W, int64_t n, double* y) {
   // Every y[i][j] is one dot product of x row i and W row j over all k, summed as orc::dot sums.
-  // Outputs are taken 32 rows x 32 columns at a time (and 2 x 2 within that) so that the rows
-  // they read stay in cache; that changes which outputs are computed together, never how any
-  // one is computed.
-  const int64_t RB = 32, CB = 32;
-  const int64_t rblocks = (m + RB - 1) / RB, cblocks = (n + CB - 1) / CB;
+  // Outputs are taken in bands of 512 weight rows (kept in the shared cache while every x row
+  // passes under them), within a band 32 rows x 32 columns at a time and 2 x 2 within that.
+  // That changes which outputs are computed together, never how any one is computed.
+  const int64_t RB = 32, CB = 32, BAND = 512;
+  const int64_t rblocks = (m + RB - 1) / RB;
+  for (int64_t b0 = 0; b0 < n; b0 += BAND) {
+    const int64_t b1 = std::min(n, b0 + BAND);
+    const int64_t cblocks = (b1 - b0 + CB - 1) / CB;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
-  for (int64_t rb = 0; rb < rblocks; ++rb)
-    for (int64_t cb = 0; cb < cblocks; ++cb) {
-      const int64_t i1 = std::min(m, (rb + 1) * RB), j1 = std::min(n, (cb + 1) * CB);
-      for (int64_t i = rb * RB; i < i1; i += 2)
-        for (int64_t j = cb * CB; j < j1; j += 2) {
-          // a ragged last row or column pairs with itself; its duplicate result is dropped
-          const int64_t i2 = std::min(i + 1, i1 - 1), j2 = std::min(j + 1, j1 - 1);
-          double r00, r01, r10, r11;
-          dot_2x2(x + i * k, x + i2 * k, W + j * k, W + j2 * k, k, &r00, &r01, &r10, &r11);
-          y[i * n + j] = r00;
-          if (j2 != j) y[i * n + j2] = r01;
-          if (i2 != i) y[i2 * n + j] = r10;
-          if (i2 != i && j2 != j) y[i2 * n + j2] = r11;
-        }
-    }
+    for (int64_t rb = 0; rb < rblocks; ++rb)
+      for (int64_t cb = 0; cb < cblocks; ++cb) {
+        const int64_t i1 = std::min(m, (rb + 1) * RB), j1 = std::min(b1, b0 + (cb + 1) * CB);
+        for (int64_t i = rb * RB; i < i1; i += 2)
+          for (int64_t j = b0 + cb * CB; j < j1; j += 2) {
+            // a ragged last row or column pairs with itself; its duplicate result is dropped
+            const int64_t i2 = std::min(i + 1, i1 - 1), j2 = std::min(j + 1, j1 - 1);
+            double r00, r01, r10, r11;
+            dot_2x2(x + i * k, x + i2 * k, W + j * k, W + j2 * k, k, &r00, &r01, &r10, &r11);
+            y[i * n + j] = r00;
+            if (j2 != j) y[i * n + j2] = r01;
+            if (i2 != i) y[i2 * n + j] = r10;
+            if (i2 != i && j2 != j) y[i2 * n + j2] = r11;
+          }
+      }
+  }
 }
 
 }  // namespace orc
