@@ -112,9 +112,9 @@ def test_canonical_entry_against_tiled_entry():
         b = clef.lut6_gemm(x, clef.lut6_tile(p, k), l, out_fp32=fp32, tiled=True)  # tiled, whole tiles
         clef.sync_status()
         assert torch.equal(a, a2)
-        # both paths accumulate in fp32 in different orders: ~sqrt(k) 2^-24 apart (6.6e-6 at
-        # k = 12288); in fp16 out, one output rounding (2^-11)
-        assert rel_rmse(a.double().cpu().numpy(), b.double().cpu().numpy()) < (1e-5 if fp32 else 1e-3)
+        # each path is within its own bound of the exact product (2e-5 fp32 out, 1e-3 fp16 out;
+        # test_gemm_matches_oracle), so the two are within the sum of the bounds
+        assert rel_rmse(a.double().cpu().numpy(), b.double().cpu().numpy()) < (4e-5 if fp32 else 2e-3)
     need = clef.lib().clef_lut6_gemm_canonical_workspace_size(n, k)
     assert need >= n * k * 3 // 4
     ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
