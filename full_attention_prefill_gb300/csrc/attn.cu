@@ -110,16 +110,14 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
 //   warp 3   MMA: O += P_j V_j (M=128, N=256, K=64; P_j read from the first 32 columns of its S
 //            buffer, V an MN-major shared operand).  The two MMA chains have a thread each: a
 //            thread's mbarrier waits complete only after the MMAs it has committed.
-//   warps 4-19 first copy Q (rows of 256 dims, after rotary) from global memory into tensor
-//            memory; then softmax, four threads per row (warps w, w+4, w+8, w+12 share TMEM
-//            lanes 32 (w % 4)..; warps 4-7 take keys 0..15 of a tile, 8-11 keys 16..31, 12-15
-//            keys 32..47, 16-19 keys 48..63): read S, mask (diagonal tiles only), online max/sum
-//            in base 2 with the four parts' maxima combined through shared memory (one barrier
-//            per tile: the exchange slots alternate with the tile's parity), write P (fp16) over
-//            the first 32 columns of its S buffer.  O is rescaled (in TMEM, each quarter of its
-//            columns by one of the four threads) only when a row's max grows by more than 2^8,
-//            so P stays below 256; the final O is divided by the row sum, multiplied by
-//            sigmoid(gate) and stored.
+//   warps 4-11 first copy Q (rows of 256 dims, after rotary) from global memory into tensor
+//            memory; then softmax, two threads per row (warps w and w+4 share TMEM lanes
+//            32 (w % 4)..; warps 4-7 take keys 0..31 of a tile, warps 8-11 keys 32..63): read S,
+//            mask (diagonal tiles only), online max/sum in base 2 with the two halves' maxima
+//            combined through shared memory, write P (fp16) over the first 32 columns of its S
+//            buffer.  O is rescaled (in TMEM, each half of its columns by one of the two
+//            threads) only when a row's max grows by more than 2^8, so P stays below 256; the
+//            final O is divided by the row sum, multiplied by sigmoid(gate) and stored.
 // Tensor memory (512 columns): O [0,256), S/P buffers [256,320) and [320,384), Q [384,512).
 // ------------------------------------------------------------------------------------------
 constexpr int TBN = 64;                   // keys per tile
@@ -131,11 +129,10 @@ constexpr int OFF_V = OFF_K + KST * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
 constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int NPART = 4;                     // softmax threads per row (key parts of a tile)
-constexpr int OFF_XCH = OFF_SLOT + 16;       // [2 parities][NPART][128 rows] fp32: max / sum
-constexpr int FLASH_SMEM = OFF_XCH + 2 * NPART * BM * 4 + 1024;
+constexpr int OFF_XCH = OFF_SLOT + 16;       // [2 halves][128 rows] fp32: row max / row sum
+constexpr int FLASH_SMEM = OFF_XCH + 2 * BM * 4 + 1024;
 static_assert(FLASH_SMEM <= 232448, "shared memory per CTA");
-constexpr int FLASH_THREADS = 128 + NPART * 128;
+constexpr int FLASH_THREADS = 384;
 constexpr uint32_t S_COL = 256;           // S/P buffers at TMEM columns 256 and 320
 constexpr uint32_t Q_COL = 384;           // Q (the S MMAs' A operand): 128 columns of fp16 pairs
 constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 units)
@@ -170,7 +167,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, NPART * 4);  // the warps that write Q into tensor memory
+    mbar_init(bar_q, 8);  // the 8 warps that write Q into tensor memory
     for (int i = 0; i < KST; ++i) {
       mbar_init(bar_kf + 8 * i, 1);
       mbar_init(bar_ke + 8 * i, 1);
@@ -181,7 +178,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, NPART * 4);
+      mbar_init(bar_p + 8 * i, 8);
       mbar_init(bar_pf + 8 * i, 1);
     }
     mbar_init(bar_fin, 1);
@@ -277,30 +274,33 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     }
   } else if (warp >= 4) {
     const int quarter = warp & 3;
-    const int part = (warp - 4) >> 2;                  // keys 16 part .. 16 part + 15 of a tile
+    const int half = (warp - 4) >> 2;                  // 0: keys 0..31 of a tile, 1: keys 32..63
     const int r = quarter * 32 + lane;                 // row of this thread
     const int pos = p0 + (r >> 2);
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [parity][part][row]
+    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [half][row]
     const float sl2 = 0.0625f * 1.4426950408889634f;  // 1/sqrt(256) in base 2
-    // the four warps of a lane quarter meet on named barrier 1 + quarter (128 threads)
-    auto row_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + quarter) : "memory"); };
+    // the two warps of a lane quarter meet on named barrier 1 + quarter (64 threads)
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
     {
       // Q into tensor memory: row r, column Q_COL + c holds dims 2c, 2c+1 (the A-operand layout
-      // of kind::f16); this thread writes its row's dims 64 part .. 64 part + 63
+      // of kind::f16); this thread writes its row's dims 128 half .. 128 half + 127
       const bool valid = pos < L;
-      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + part * 64;
-      uint32_t qv[32];
+      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + half * 128;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t qv[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 d = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i)
-                              : make_uint4(0u, 0u, 0u, 0u);
-        qv[4 * i] = d.x;
-        qv[4 * i + 1] = d.y;
-        qv[4 * i + 2] = d.z;
-        qv[4 * i + 3] = d.w;
+        for (int i = 0; i < 8; ++i) {
+          const uint4 d = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 2 * c0) + i)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * i] = d.x;
+          qv[4 * i + 1] = d.y;
+          qv[4 * i + 2] = d.z;
+          qv[4 * i + 3] = d.w;
+        }
+        tmem_st_32x32b_x32(tl + Q_COL + half * 64 + c0, qv);
       }
-      tmem_st_32x32b_x32(tl + Q_COL + part * 32, qv);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -311,43 +311,41 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const int qpos = pos0 + pos;                        // this row's position in the request
     float m_ref = -INFINITY;   // reference max of the raw scores (P = 2^((s - m_ref) sl2))
     float lsum = 0.f;
-    // The four threads of a row pass the same named barrier once every iteration, whatever
-    // happens: a failed (timed-out) wait only turns the rest of the work off (ok is
-    // warp-uniform).  The exchange slots of tile j are reused by tile j + 2, which every thread
-    // writes only after the barrier of tile j + 1, i.e. after all reads of tile j.
+    // Both threads of a row pass the same named barriers every iteration, whatever happens: a
+    // failed (timed-out) wait only turns the rest of the work off (ok is warp-uniform).
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
       ok = ok && mbar_wait(bar_s + 8 * s, (uint32_t)(j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
       ok = __all_sync(0xffffffffu, ok);
-      uint32_t sv[16];
+      uint32_t sv[32];
       float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
-        tmem_ld_32x32b_x16(tl + S_COL + s * TBN + part * 16, sv);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + half * 32, sv);
         tc_wait_ld();
-        const int key0 = j * TBN + part * 16;
+        const int key0 = j * TBN + half * 32;
         if (j * TBN + TBN - 1 <= p_first) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) mt = fmaxf(mt, __uint_as_float(sv[c]));
+          for (int c = 0; c < 32; ++c) mt = fmaxf(mt, __uint_as_float(sv[c]));
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
+          for (int c = 0; c < 32; ++c) {
             const float v = (key0 + c <= qpos) ? __uint_as_float(sv[c]) : -INFINITY;
             sv[c] = __float_as_uint(v);
             mt = fmaxf(mt, v);
           }
         }
       }
-      // row max over the four parts
-      float* xb = xch + (j & 1) * (NPART * BM);
-      xb[part * BM + r] = mt;
-      row_sync();
-#pragma unroll
-      for (int o = 0; o < NPART; ++o) mt = fmaxf(mt, xb[o * BM + r]);
+      // row max over both halves (the previous exchange's reads are fenced off by that
+      // exchange's second barrier)
+      xch[half * BM + r] = mt;
+      pair_sync();
+      mt = fmaxf(mt, xch[(half ^ 1) * BM + r]);
+      pair_sync();
       if (!ok) continue;
       const float m_new = fmaxf(m_ref, mt);
-      const bool need = (m_new - m_ref) * sl2 > kRescale;   // the same in all threads of a row
+      const bool need = (m_new - m_ref) * sl2 > kRescale;   // the same in both threads of a row
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O may only be rescaled once P_{j-1} V_{j-1} has landed in it (P_{j+1} V_{j+1} cannot
         // be done yet, so the parity test is unambiguous)
@@ -356,10 +354,10 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
                                                status, DEV_TIMEOUT_EPILOGUE));
         if (!ok) continue;
         tc_fence_after();
-        // rescale this warp's quarter (64 columns) of its O rows
+        // rescale this warp's half (128 columns) of its O rows
         const float f = need ? exp2f((m_ref - m_new) * sl2) : 1.f;
 #pragma unroll 1
-        for (int c0 = part * (D / NPART); c0 < (part + 1) * (D / NPART); c0 += 32) {
+        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
           uint32_t ov[32];
           tmem_ld_32x32b_x32(tl + c0, ov);
           tc_wait_ld();
@@ -373,39 +371,34 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       if (need) m_ref = m_new;
       // P = 2^(s sl2 - m_ref sl2): one FFMA and one exp2 per score
       const float moff = -m_ref * sl2;
-      uint32_t pk[8];
+      uint32_t pk[16];
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 16; ++c) {
         const float e0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sl2, moff));
         const float e1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, moff));
         rs += e0 + e1;
         pk[c] = pack_half2(e0, e1);
       }
-      lsum += rs;  // this part's share of the row sum
-      tmem_st_32x32b_x8(tl + S_COL + s * TBN + part * 8, pk);
+      lsum += rs;  // this half's share of the row sum
+      tmem_st_32x32b_x16(tl + S_COL + s * TBN + half * 16, pk);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p + 8 * s);
     }
     // epilogue: wait for the last P V, then O / l * sigmoid(gate), each thread of a row taking
-    // a quarter of its columns (the row sum's exchange uses the slots of parity nt)
-    {
-      float* xb = xch + (nt & 1) * (NPART * BM);
-      xb[part * BM + r] = lsum;
-      row_sync();
-      lsum = 0.f;
-#pragma unroll
-      for (int o = 0; o < NPART; ++o) lsum += xb[o * BM + r];
-    }
+    // half of its columns
+    xch[half * BM + r] = lsum;
+    pair_sync();
+    lsum += xch[(half ^ 1) * BM + r];
     if (ok && mbar_wait(bar_fin, 0, status, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const int hq = 4 * g + (r & 3);
       const int64_t row = (int64_t)tb + pos;
 #pragma unroll 1
-      for (int c0 = part * (D / NPART); c0 < (part + 1) * (D / NPART); c0 += 32) {
+      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(tl + c0, ov);
         tc_wait_ld();

@@ -314,14 +314,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       : "memory");
 }
 
-// 32 lanes x 8 consecutive 32-bit columns written from registers.
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-}
-
 // Shared-memory matrix descriptor (tcgen05 form): K-major operand, 128-byte swizzle, rows of
 // 128 bytes grouped by 8 (1024-byte atoms).  Fields: start>>4 [0,14), LBO>>4 [16,30),
 // SBO>>4 [32,46), version 1 [46,48), base offset 0 [49,52), layout SWIZZLE_128B = 2 [61,64).

@@ -142,12 +142,13 @@ __global__ void check_finite_kernel(const __half* __restrict__ x, int64_t rows, 
   }
 }
 
-// ab = xn . W_ab^T: 64 tokens x 64 outputs per CTA, k streamed in blocks of 64 (cp.async double
-// buffer), warp w owns tokens 16w..16w+15.
-constexpr int AB_T = 64, AB_K = 64, AB_LD = AB_K + 8;
+// ab = xn . W_ab^T: 64 tokens x 64 outputs per CTA, k streamed in blocks of 64 through a ring of
+// AB_ST cp.async stages (three blocks in flight while one is multiplied), warp w owns tokens
+// 16w..16w+15.
+constexpr int AB_T = 64, AB_K = 64, AB_LD = AB_K + 8, AB_ST = 4;
 struct AbSmem {
-  __half X[2][AB_T][AB_LD];
-  __half W[2][64][AB_LD];
+  __half X[AB_ST][AB_T][AB_LD];
+  __half W[AB_ST][64][AB_LD];
 };
 
 // Gates from the summed projections: g = -exp(A_log) softplus(a + dt_bias) (>= -30), beta = sigmoid(b).
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
                                                       float* __restrict__ g,
                                                       float* __restrict__ beta,
                                                       float* __restrict__ part, int64_t M) {
-  __shared__ __align__(16) AbSmem s;
+  extern __shared__ __align__(16) uint8_t ab_smem[];
+  AbSmem& s = *reinterpret_cast<AbSmem*>(ab_smem);
   const int64_t t0 = (int64_t)blockIdx.x * AB_T;
   const int nkb_all = H / AB_K;
   const int kb0 = blockIdx.y * nkb_all / gridDim.y;
@@ -189,12 +191,15 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
   float acc[8][4];
 #pragma unroll
   for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  load(0, kb0);
+  for (int i = 0; i < AB_ST - 1; ++i) {
+    if (kb0 + i < kb1) load(i, kb0 + i); else cp_async_commit();
+  }
   for (int kb = kb0; kb < kb1; ++kb) {
-    const int buf = (kb - kb0) & 1;
-    if (kb + 1 < kb1) load(buf ^ 1, kb + 1); else cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
+    const int buf = (kb - kb0) % AB_ST;
+    cp_async_wait<AB_ST - 2>();   // block kb has landed
+    __syncthreads();              // ... for every thread, and the slot of kb - 1 is free again
+    const int nxt = kb + AB_ST - 1;
+    if (nxt < kb1) load((nxt - kb0) % AB_ST, nxt); else cp_async_commit();
     const uint32_t sX = smem_u32(&s.X[buf][0][0]), sW = smem_u32(&s.W[buf][0][0]);
 #pragma unroll
     for (int ks = 0; ks < AB_K / 16; ++ks) {
@@ -208,7 +213,6 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
         mma16816(acc[n + 1], a, bq[2], bq[3]);
       }
     }
-    __syncthreads();
   }
   cp_async_wait<0>();
   const int gq = lane >> 2, tq = lane & 3;
@@ -296,7 +300,9 @@ clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A
   int slices = 1;
   while (slices < kAbMaxSlices && ctas * slices * 2 <= num_sms()) slices *= 2;
   TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
-  glue::ab_proj_kernel<<<dim3((unsigned)ctas, (unsigned)slices), 128, 0, stream>>>(
+  static std::atomic<uint64_t> attr{0};
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)glue::ab_proj_kernel, sizeof(glue::AbSmem), &attr));
+  glue::ab_proj_kernel<<<dim3((unsigned)ctas, (unsigned)slices), 128, sizeof(glue::AbSmem), stream>>>(
       xn, w_ab, A_log, dt_bias, g, beta, part, M);
   CLEF_LAUNCH_CHECK();
   if (slices > 1) {

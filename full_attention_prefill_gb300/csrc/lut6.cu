@@ -175,10 +175,14 @@ struct Seg {
   int sk_tile;     // stream-K tile index (tile - dp)
 };
 
+// 32-bit arithmetic throughout: the shared steps S are fewer than 2 SMs x num_kb (num_kb <=
+// 2^14), so c * S stays far below 2^31.
 struct Sched {
   int G, num_tiles, num_kb, dp, sk;
-  __host__ __device__ int64_t sk_steps() const { return (int64_t)(num_tiles - dp) * num_kb; }
-  __host__ __device__ int64_t share_begin(int c) const { return (int64_t)c * sk_steps() / sk; }
+  __host__ __device__ int sk_steps() const { return (num_tiles - dp) * num_kb; }
+  __host__ __device__ int share_begin(int c) const {
+    return (int)((unsigned)c * (unsigned)sk_steps() / (unsigned)sk);
+  }
   // segment j of CTA c; false when there is none
   __host__ __device__ bool seg(int c, int j, Seg& g) const {
     const int n_dp = c < dp ? (dp - 1 - c) / G + 1 : 0;
@@ -192,32 +196,134 @@ struct Sched {
     }
     if (c >= sk || sk_steps() == 0) return false;
     const int i = j - n_dp;
-    const int64_t a = share_begin(c), b = share_begin(c + 1);
-    const int64_t t = a / num_kb + i;
-    const int64_t s0 = t * num_kb > a ? t * num_kb : a;
-    const int64_t s1 = (t + 1) * num_kb < b ? (t + 1) * num_kb : b;
+    const int a = share_begin(c), b = share_begin(c + 1);
+    const int t = a / num_kb + i;
+    const int s0 = t * num_kb > a ? t * num_kb : a;
+    const int s1 = (t + 1) * num_kb < b ? (t + 1) * num_kb : b;
     if (s0 >= s1) return false;
-    g.tile = dp + (int)t;
-    g.kb0 = (int)(s0 - t * num_kb);
-    g.kb1 = (int)(s1 - t * num_kb);
+    g.tile = dp + t;
+    g.kb0 = s0 - t * num_kb;
+    g.kb1 = s1 - t * num_kb;
     g.slot = 3 * c + i;
-    g.sk_tile = (int)t;
+    g.sk_tile = t;
     return true;
+  }
+  // the CTA whose share holds shared step s
+  __host__ __device__ int owner(int s) const {
+    int c = (int)((unsigned)s * (unsigned)sk / (unsigned)sk_steps());
+    while (c > 0 && share_begin(c) > s) --c;
+    while (share_begin(c + 1) <= s) ++c;
+    return c;
   }
   // the CTAs whose shares hold steps of stream-K tile t: c_lo .. c_hi
   __host__ __device__ void pieces(int t, int& c_lo, int& c_hi) const {
-    const int64_t s0 = (int64_t)t * num_kb, s1 = s0 + num_kb - 1;
-    const int64_t S = sk_steps();
-    int c = (int)(s0 * sk / S);
-    while (c > 0 && share_begin(c) > s0) --c;
-    while (share_begin(c + 1) <= s0) ++c;
-    c_lo = c;
-    c = (int)(s1 * sk / S);
-    while (c > 0 && share_begin(c) > s1) --c;
-    while (share_begin(c + 1) <= s1) ++c;
-    c_hi = c;
+    c_lo = owner(t * num_kb);
+    c_hi = owner(t * num_kb + num_kb - 1);
   }
 };
+
+// What one epilogue warp needs to write its 32 channels x 64 tokens of a tile.
+struct EpiCtx {
+  void* y;
+  int64_t ldy;
+  int M, N, mode;
+  int ecol, ch, quarter, lane;
+};
+
+// Write Y for the warp's 32 channels x 64 tokens of the tile at (n0e, m0e) from r0 (tokens
+// ecol .. ecol + 31) and r1 (tokens ecol + 32 .. ecol + 63).
+__device__ __forceinline__ void store_tile(const EpiCtx& x, int n0e, int m0e,
+                                           const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+  const int tok0 = m0e + x.ecol;
+  const int col = n0e + x.ch;
+  if (x.mode == EPI_SWIGLU_F16) {
+    // lanes 0..15: gate rows, lanes 16..31: the up rows of the same channels; the gate lane
+    // writes tokens 0..31 of the warp's 64, the up lane tokens 32..63
+    const bool up = x.lane >= 16;
+    const int oc = n0e / 2 + x.quarter * 16 + (x.lane & 15);
+    __half* out = reinterpret_cast<__half*>(x.y);
+    const bool oc_ok = oc < x.N / 2;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t send = up ? r0[i] : r1[i];
+      const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+      const float gate = up ? other : __uint_as_float(r0[i]);
+      const float upv = up ? __uint_as_float(r1[i]) : other;
+      const int tok = tok0 + (up ? 32 : 0) + i;
+      if (oc_ok && tok < x.M) out[(int64_t)tok * x.ldy + oc] = __float2half_rn(silu_f(gate) * upv);
+    }
+  } else if (col < x.N) {
+    if (x.mode == EPI_F16) {
+      __half* out = reinterpret_cast<__half*>(x.y) + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (tok0 + i < x.M) out[(int64_t)(tok0 + i) * x.ldy] = __float2half_rn(__uint_as_float(r0[i]));
+        if (tok0 + 32 + i < x.M)
+          out[(int64_t)(tok0 + 32 + i) * x.ldy] = __float2half_rn(__uint_as_float(r1[i]));
+      }
+    } else if (x.mode == EPI_F32) {
+      float* out = reinterpret_cast<float*>(x.y) + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (tok0 + i < x.M) out[(int64_t)(tok0 + i) * x.ldy] = __uint_as_float(r0[i]);
+        if (tok0 + 32 + i < x.M) out[(int64_t)(tok0 + 32 + i) * x.ldy] = __uint_as_float(r1[i]);
+      }
+    } else {
+      // residual add, done by L2: each element receives exactly one add per launch (the same
+      // as load + add + store), so launches repeat bit for bit
+      float* out = reinterpret_cast<float*>(x.y) + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (tok0 + i < x.M) red_add_f32(out + (int64_t)(tok0 + i) * x.ldy, __uint_as_float(r0[i]));
+        if (tok0 + 32 + i < x.M)
+          red_add_f32(out + (int64_t)(tok0 + 32 + i) * x.ldy, __uint_as_float(r1[i]));
+      }
+    }
+  }
+}
+
+// The end of a stream-K piece, once every epilogue warp has stored its partial sums (and fenced
+// them) and arrived on bar_pc: one thread counts the piece for the tile; the CTA that brings the
+// count to the tile's number of pieces adds all pieces (its own included, read back from L2) in
+// CTA order and writes the tile.
+__device__ __forceinline__ bool sk_finish(const EpiCtx& x, const Sched& sc, int tile, int sk_tile,
+                                       int n0e, int m0e, const float* part,
+                                       unsigned* tile_count, uint32_t bar_pc, uint32_t bar_pd,
+                                       volatile int* sk_last, int parity, bool leader,
+                                       unsigned* status) {
+  int c_lo, c_hi;
+  sc.pieces(sk_tile, c_lo, c_hi);
+  if (leader) {
+    int last = 0;
+    if (mbar_wait(bar_pc, (uint32_t)parity, status, DEV_TIMEOUT_EPILOGUE)) {
+      const unsigned before = atomicAdd(tile_count + sk_tile, 1u);
+      last = before == (unsigned)(c_hi - c_lo) ? 1 : 0;
+      if (last) tile_count[sk_tile] = 0u;   // ready for the next launch
+      __threadfence();
+    }
+    *sk_last = last;
+    mbar_arrive(bar_pd);
+  }
+  if (!mbar_wait(bar_pd, (uint32_t)parity, status, DEV_TIMEOUT_EPILOGUE)) return false;
+  if (*sk_last) {
+    uint32_t r0[32], r1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = __float_as_uint(0.f);
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const int slot = 3 * c + (sk_tile - sc.share_begin(c) / sc.num_kb);
+      const float* piece = part + (int64_t)slot * (BT * BN);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __ldcg(piece + (x.ecol + i) * BN + x.ch));
+        r1[i] = __float_as_uint(__uint_as_float(r1[i]) +
+                                __ldcg(piece + (x.ecol + 32 + i) * BN + x.ch));
+      }
+    }
+    store_tile(x, n0e, m0e, r0, r1);
+  }
+  (void)tile;
+  return true;
+}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -401,60 +507,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ch = quarter * 32 + lane;                // this lane's channel in the tile
     int sk_done = 0;                                   // stream-K epilogues so far (parities)
 
-    // Write Y for this warp's 32 channels x 64 tokens of the tile at (n0e, m0e) from r0, r1.
-    auto store = [&](int n0e, int m0e, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
-      const int tok0 = m0e + ecol;
-      const int col = n0e + ch;
-      if (mode == EPI_SWIGLU_F16) {
-        // lanes 0..15: gate rows, lanes 16..31: the up rows of the same channels; the gate lane
-        // writes tokens 0..31 of the warp's 64, the up lane tokens 32..63
-        const bool up = lane >= 16;
-        const int oc = n0e / 2 + quarter * 16 + (lane & 15);
-        __half* out = reinterpret_cast<__half*>(y);
-        const bool oc_ok = oc < N / 2;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t send = up ? r0[i] : r1[i];
-          const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
-          const float gate = up ? other : __uint_as_float(r0[i]);
-          const float upv = up ? __uint_as_float(r1[i]) : other;
-          const int tok = tok0 + (up ? 32 : 0) + i;
-          if (oc_ok && tok < M) out[(int64_t)tok * ldy + oc] = __float2half_rn(silu_f(gate) * upv);
-        }
-      } else if (col < N) {
-        if (mode == EPI_F16) {
-          __half* out = reinterpret_cast<__half*>(y) + col;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (tok0 + i < M) out[(int64_t)(tok0 + i) * ldy] = __float2half_rn(__uint_as_float(r0[i]));
-            if (tok0 + 32 + i < M)
-              out[(int64_t)(tok0 + 32 + i) * ldy] = __float2half_rn(__uint_as_float(r1[i]));
-          }
-        } else if (mode == EPI_F32) {
-          float* out = reinterpret_cast<float*>(y) + col;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (tok0 + i < M) out[(int64_t)(tok0 + i) * ldy] = __uint_as_float(r0[i]);
-            if (tok0 + 32 + i < M) out[(int64_t)(tok0 + 32 + i) * ldy] = __uint_as_float(r1[i]);
-          }
-        } else {
-          // residual add, done by L2: each element receives exactly one add per launch (the
-          // same as load + add + store), so launches repeat bit for bit
-          float* out = reinterpret_cast<float*>(y) + col;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (tok0 + i < M) red_add_f32(out + (int64_t)(tok0 + i) * ldy, __uint_as_float(r0[i]));
-            if (tok0 + 32 + i < M)
-              red_add_f32(out + (int64_t)(tok0 + 32 + i) * ldy, __uint_as_float(r1[i]));
-          }
-        }
-      }
-    };
+    const EpiCtx ex{y, ldy, M, N, mode, ecol, ch, quarter, lane};
 
-    // Drain this warp's 32 lanes x 64 columns of the accumulator of segment `e` (its ite-th),
-    // release it, then write Y, or (a stream-K piece) store the partial sums, and if this CTA is
-    // the last to finish the tile, add the tile's pieces in CTA order and write Y.
-    auto epilogue = [&](const Seg& e, int ite) -> bool {
+    // Drain this warp's 32 lanes x 64 columns of the accumulator of this CTA's segment `ite`,
+    // release it, then write Y, or (a stream-K piece) store the partial sums and finish the
+    // piece (sk_finish).  The segment is looked up again here, so that the dequantisation loop
+    // keeps only its index.
+    auto epilogue = [&](int ite) -> bool {
+      Seg e;
+      sc.seg(cta, ite, e);
       int n0e, m0e;
       tile_coord(e.tile, n_tiles, m_tiles, n0e, m0e);
       if (!mbar_wait(bar_accf, (uint32_t)ite & 1, status, DEV_TIMEOUT_EPILOGUE)) return false;
@@ -467,10 +528,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acce);
       if (e.slot < 0) {
-        store(n0e, m0e, r0, r1);
+        store_tile(ex, n0e, m0e, r0, r1);
         return true;
       }
-      // a stream-K piece: partial sums [token][channel] in its slot
+      // a stream-K piece: partial sums [token][channel] in its slot, fenced before the count
       float* mine = part + (int64_t)e.slot * (BT * BN);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -480,62 +541,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __threadfence();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pc);
-      int c_lo, c_hi;
-      sc.pieces(e.sk_tile, c_lo, c_hi);
-      if (dq == 0 && lane == 0) {
-        // every warp's partial is stored (and fenced): count this piece for the tile
-        int last = 0;
-        if (mbar_wait(bar_pc, (uint32_t)sk_done & 1, status, DEV_TIMEOUT_EPILOGUE)) {
-          const unsigned before = atomicAdd(tile_count + e.sk_tile, 1u);
-          last = before == (unsigned)(c_hi - c_lo) ? 1 : 0;
-          if (last) tile_count[e.sk_tile] = 0u;   // ready for the next launch
-          __threadfence();
-        }
-        *sk_last = last;
-        mbar_arrive(bar_pd);
-      }
-      const bool got = mbar_wait(bar_pd, (uint32_t)sk_done & 1, status, DEV_TIMEOUT_EPILOGUE);
+      const bool done = sk_finish(ex, sc, e.tile, e.sk_tile, n0e, m0e, part, tile_count, bar_pc,
+                                  bar_pd, sk_last, sk_done & 1, dq == 0 && lane == 0, status);
       ++sk_done;
-      if (!got) return false;
-      if (*sk_last) {
-        // the whole tile: its pieces in CTA order (this CTA's own from registers)
-        uint32_t s0[32], s1[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s0[i] = s1[i] = __float_as_uint(0.f);
-        for (int c = c_lo; c <= c_hi; ++c) {
-          const int64_t a = sc.share_begin(c);
-          const int slot = 3 * c + (int)((int64_t)e.sk_tile - a / sc.num_kb);
-          if (slot == e.slot) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              s0[i] = __float_as_uint(__uint_as_float(s0[i]) + __uint_as_float(r0[i]));
-              s1[i] = __float_as_uint(__uint_as_float(s1[i]) + __uint_as_float(r1[i]));
-            }
-          } else {
-            const float* other = part + (int64_t)slot * (BT * BN);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              s0[i] = __float_as_uint(__uint_as_float(s0[i]) + __ldcg(other + (ecol + i) * BN + ch));
-              s1[i] = __float_as_uint(__uint_as_float(s1[i]) +
-                                      __ldcg(other + (ecol + 32 + i) * BN + ch));
-            }
-          }
-        }
-        store(n0e, m0e, s0, s1);
-      }
-      return true;
+      return done;
     };
 
     int64_t g = 0;
     bool ok = true;
-    bool pending = false;   // a segment whose epilogue is due
-    Seg pe{};               // that segment
-    int pit = 0;            // and its index
+    int pending = -1;       // the segment whose epilogue is due
     Seg sg;
     int it = 0;
     for (; ok && sc.seg(cta, it, sg); ++it) {
-      int n0, m0;
-      tile_coord(sg.tile, n_tiles, m_tiles, n0, m0);
       const int ts = it & 1;
       if (!mbar_wait(bar_tfull + 8 * ts, (uint32_t)(it >> 1) & 1, status, DEV_TIMEOUT_DEQUANT)) {
         ok = false;
@@ -544,11 +561,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tb = sb + OFF_T + ts * TBL_BYTES + grp * 128;
       // the accumulator of the previous segment is drained after the first `lead` steps of this
       // one have been dequantised, so its MMAs start as soon as the accumulator is free
-      const int lead = min(AS - 1, sg.kb1 - sg.kb0 - 1);
-      for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++g) {
-        if (kb - sg.kb0 == lead && pending) {
-          ok = epilogue(pe, pit);
-          pending = false;
+      const int nsteps = sg.kb1 - sg.kb0;
+      const int lead = min(AS - 1, nsteps - 1);
+      for (int step = 0; step < nsteps; ++step, ++g) {
+        if (step == lead && pending >= 0) {
+          ok = epilogue(pending);
+          pending = -1;
           if (!ok) break;
         }
         if ((int)(g & 1) != par) continue;
@@ -585,11 +603,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty + 8 * ts);  // done with this segment's tables
-      pending = true;
-      pe = sg;
-      pit = it;
+      pending = it;
     }
-    if (ok && pending) epilogue(pe, pit);
+    if (ok && pending >= 0) epilogue(pending);
   }
   tc_fence_before();
   __syncthreads();
@@ -656,7 +672,7 @@ static lut::Sched plan_schedule(int64_t M, int64_t N, int64_t K, int sms, bool c
   const int64_t cost_dp = (int64_t)((tiles + sms - 1) / sms) * (nkb + 4);
   const int waves = tiles / sms;
   const int dp = waves >= 1 ? (waves - 1) * sms : 0;
-  const int64_t S = (int64_t)(tiles - dp) * nkb;
+  const int64_t S = (int64_t)(tiles - dp) * nkb;   // < 2 sms num_kb: fits the 32-bit schedule
   const int sk = (int)std::max<int64_t>(1, std::min<int64_t>(sms, S / 8));
   const int64_t cost_sk = (int64_t)(dp / sms) * (nkb + 4) + (S + sk - 1) / sk + 14;
   if (cost_sk + 8 >= cost_dp) return dp_only;
