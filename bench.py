@@ -457,10 +457,14 @@ def run_micro(args):
         x = torch.from_numpy(synth.normal_f16(0, "micro.x", 0, (M, K))).to(dev)
         packed, lut = synth.lut6_weight(0, "micro.w", 0, N, K)
         p, l = torch.from_numpy(packed).to(dev), torch.from_numpy(lut).to(dev)
-        p = clef.lut6_tile(p, K)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
-        fn = lambda: clef.lut6_gemm(x, p, l, out=y, tiled=True)  # noqa: E731
-        flops, desc = 2.0 * M * N * K, f"lut6_gemm M={M} N={N} K={K}"
+        if args.canonical:
+            # the card's packing through clef_lut6_gemm_canonical (stream-K where it pays)
+            fn = lambda: clef.lut6_gemm(x, p, l, out=y)  # noqa: E731
+        else:
+            p = clef.lut6_tile(p, K)
+            fn = lambda: clef.lut6_gemm(x, p, l, out=y, tiled=True)  # noqa: E731
+        flops, desc = 2.0 * M * N * K, f"lut6_gemm M={M} N={N} K={K}" + (" canonical" if args.canonical else "")
     elif args.micro == "attn":
         L = args.L
         q = torch.from_numpy(synth.normal_f16(0, "q", 0, (1, L, 16, 256))).to(dev)
@@ -567,6 +571,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--micro", choices=["gemm", "attn", "gdn", "layer", "chunk", "quantize", "image"], default=None)
     ap.add_argument("--chunk", type=int, default=64)
+    ap.add_argument("--canonical", action="store_true",
+                    help="--micro gemm: pass the card's packing (clef_lut6_gemm_canonical)")
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--m", type=int, default=4096)
     ap.add_argument("--n", type=int, default=24576)

@@ -62,7 +62,11 @@ class Model(ctypes.Structure):
         ("embed", ctypes.c_void_p),
         ("vocab", ctypes.c_int64),
         ("final_norm", ctypes.c_void_p),
+        ("flags", ctypes.c_int32),
     ]
+
+
+MODEL_REPRODUCIBLE = 1
 
 
 class State(ctypes.Structure):
@@ -86,8 +90,6 @@ _SIGS = {
     "clef_debug_gdn_workspace_layout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                                        ctypes.c_void_p, ctypes.c_void_p]),
     "clef_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
-    "clef_debug_lut6_schedule": (ctypes.c_int, [ctypes.c_int64] * 3 + [ctypes.c_int32] + [ctypes.c_void_p] * 2 +
-                                 [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
     "clef_check_finite": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                          ctypes.c_void_p]),
     "clef_lut6_pack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),

@@ -392,15 +392,9 @@ clef_status clef_lut6_tile(const uint8_t* packed, int64_t n, int64_t k, uint8_t*
   return lut6_tile_launch(packed, n, k, tiled, static_cast<cudaStream_t>(stream));
 }
 
-static size_t canon_tiled_bytes(int64_t n, int64_t k) {
-  return ((size_t)n * (size_t)(k / 4 * 3) + 255) & ~size_t(255);
-}
-
 size_t clef_lut6_gemm_canonical_workspace_size(int64_t n, int64_t k) {
   if (n <= 0 || k <= 0 || n % 16 || k % 64) return 0;
-  // the tiled weight, then the stream-K partial sums and piece counters
-  return canon_tiled_bytes(n, k) + (size_t)lut6_split_part_bytes() +
-         (size_t)lut6_split_count_bytes();
+  return (size_t)n * (size_t)(k / 4 * 3);
 }
 
 clef_status clef_lut6_gemm_canonical(const uint16_t* x, const uint8_t* packed, const uint16_t* lut,
@@ -429,30 +423,10 @@ clef_status clef_lut6_gemm_canonical(const uint16_t* x, const uint8_t* packed, c
     set_error("clef_lut6_gemm_canonical: workspace must be 16-byte aligned");
     return CLEF_E_ALIGN;
   }
-  if (!x || !lut || !y) {
-    set_error("clef_lut6_gemm_canonical: NULL pointer");
-    return CLEF_E_INVALID;
-  }
-  if (misaligned(x) || misaligned(lut) || misaligned(y)) {
-    set_error("clef_lut6_gemm_canonical: device pointers must be 16-byte aligned");
-    return CLEF_E_ALIGN;
-  }
-  if (m > (int64_t)INT32_MAX / 2 || n > (1 << 24) || k > (1 << 20)) {
-    set_error("clef_lut6_gemm_canonical: size out of the supported range");
-    return CLEF_E_SHAPE;
-  }
-  if (debug_should_fail()) return CLEF_E_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* tiled = static_cast<uint8_t*>(workspace);
-  float* part = reinterpret_cast<float*>(tiled + canon_tiled_bytes(n, k));
-  unsigned* counts = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(part) +
-                                                 lut6_split_part_bytes());
-  const clef_status st = lut6_tile_launch(packed, n, k, tiled, s);
+  const clef_status st = clef_lut6_tile(packed, n, k, static_cast<uint8_t*>(workspace), stream);
   if (st != CLEF_OK) return st;
-  CLEF_CUDA_CHECK(cudaMemsetAsync(counts, 0, (size_t)lut6_split_count_bytes(), s));
-  return lut6_gemm_launch(reinterpret_cast<const __half*>(x), tiled,
-                          reinterpret_cast<const __half*>(lut), y, n, m, n, k,
-                          y_is_fp32 ? EPI_F32 : EPI_F16, s, part, counts);
+  return clef_lut6_gemm(x, static_cast<const uint8_t*>(workspace), lut, y, y_is_fp32, m, n, k,
+                        stream);
 }
 
 clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* packed, const uint16_t* lut, void* y,

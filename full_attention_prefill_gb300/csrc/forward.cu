@@ -41,8 +41,7 @@ struct FwdWs {
   __half* mix;
   __half* h;
   void* scan;
-  float* part;       // stream-K partial sums of the LUT-6 GEMMs
-  unsigned* counts;  // stream-K piece counters (zeroed at the start of every call)
+  float* part;     // k-part partial sums of the split residual adds (ordered reduction)
 };
 
 static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
@@ -67,8 +66,12 @@ static size_t fwd_layout(int64_t B, int64_t L, void* base, FwdWs* w) {
   t.mix = static_cast<__half*>(take(M * H * 2));
   t.h = static_cast<__half*>(take(M * I * 2));
   t.scan = take(gdn_scan_workspace_bytes(B, L, true));
-  t.part = static_cast<float*>(take((size_t)lut6_split_part_bytes()));
-  t.counts = static_cast<unsigned*>(take((size_t)lut6_split_count_bytes()));
+  {
+    // the residual adds (out-proj K = 4096, down K = 12288, N = 4096) split over k-parts only
+    // when there are few tiles; reproducible prefills keep each part's sums here
+    const int64_t parts = std::max(lut6_add_split(M, H, H), lut6_add_split(M, H, I));
+    t.part = parts > 1 ? static_cast<float*>(take((size_t)parts * M * H * 4)) : nullptr;
+  }
   if (w) *w = t;
   return off;
 }
@@ -92,16 +95,16 @@ struct LayerState {
 };
 
 static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, int64_t L,
-                             cudaStream_t s, const LayerState& st = LayerState()) {
+                             cudaStream_t s, const LayerState& st = LayerState(),
+                             bool reproducible = false) {
   const int64_t M = B * L;
-  float* part = w.part;
-  unsigned* cnt = w.counts;
+  float* part = reproducible ? w.part : nullptr;
   const __half* attn_norm = reinterpret_cast<const __half*>(ly.attn_norm);
   CLEF_TRY(rmsnorm_launch(w.x, attn_norm, w.xn, M, s));
   const __half* in_lut = reinterpret_cast<const __half*>(ly.in_proj.lut);
   if (ly.kind == CLEF_LAYER_GDN) {
     CLEF_TRY(lut6_gemm_launch(w.xn, ly.in_proj.packed, in_lut, w.proj, GDN_PROJ, M, GDN_PROJ, H,
-                              EPI_F16, s, part, cnt));
+                              EPI_F16, s));
     CLEF_TRY(ab_proj_launch(w.xn, reinterpret_cast<const __half*>(ly.ab_w),
                             reinterpret_cast<const __half*>(ly.A_log),
                             reinterpret_cast<const __half*>(ly.dt_bias), w.g, w.beta, w.abpart, M,
@@ -115,7 +118,7 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
                              w.mix, H, B, L, w.scan, s));
   } else {
     CLEF_TRY(lut6_gemm_launch(w.xn, ly.in_proj.packed, in_lut, w.proj, ATT_PROJ, M, ATT_PROJ, H,
-                              EPI_F16, s, part, cnt));
+                              EPI_F16, s));
     __half* qp = w.proj;
     __half* gp = w.proj + 4096;
     __half* kp = w.proj + 8192;
@@ -138,13 +141,13 @@ static clef_status run_layer(const clef_layer& ly, const FwdWs& w, int64_t B, in
   }
   CLEF_TRY(lut6_gemm_launch(w.mix, ly.out_proj.packed,
                             reinterpret_cast<const __half*>(ly.out_proj.lut), w.x, H, M, H, H,
-                            EPI_ADD_F32, s, part, cnt));
+                            EPI_ADD_F32, s, part));
   // MLP
   CLEF_TRY(rmsnorm_launch(w.x, reinterpret_cast<const __half*>(ly.mlp_norm), w.xn, M, s));
   CLEF_TRY(lut6_gemm_launch(w.xn, ly.gate_up.packed, reinterpret_cast<const __half*>(ly.gate_up.lut),
-                            w.h, I, M, 2 * I, H, EPI_SWIGLU_F16, s, part, cnt));
+                            w.h, I, M, 2 * I, H, EPI_SWIGLU_F16, s));
   CLEF_TRY(lut6_gemm_launch(w.h, ly.down.packed, reinterpret_cast<const __half*>(ly.down.lut), w.x,
-                            H, M, H, I, EPI_ADD_F32, s, part, cnt));
+                            H, M, H, I, EPI_ADD_F32, s, part));
   return CLEF_OK;
 }
 
@@ -209,14 +212,14 @@ static clef_status prefill_impl(const char* who, const clef_model* model, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   FwdWs w;
   fwd_layout(B, L, workspace, &w);
-  // the stream-K piece counters start at zero (every GEMM launch leaves them zero again)
-  CLEF_CUDA_CHECK(cudaMemsetAsync(w.counts, 0, (size_t)lut6_split_count_bytes(), s));
   const int64_t M = B * L;
   CLEF_TRY(embed_launch(ids, reinterpret_cast<const __half*>(model->embed), model->vocab, w.x, M, s));
   if (image_rows) CLEF_TRY(image_rows_launch(image_rows, w.x, B, L, mr.start, mr.h * mr.w, s));
   LayerState ls;
   ls.mr = mr;
-  for (int i = 0; i < model->n_layers; ++i) CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+  const bool repro = (model->flags & CLEF_MODEL_REPRODUCIBLE) != 0;
+  for (int i = 0; i < model->n_layers; ++i)
+    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls, repro));
   return rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
                         reinterpret_cast<__half*>(hidden), M, s, /*check_finite=*/true);
 }
@@ -325,9 +328,6 @@ clef_status clef_decoder_layer(const clef_layer* layer, float* x, int64_t B, int
   if (debug_should_fail()) return CLEF_E_CUDA;
   FwdWs w;
   fwd_layout(B, L, workspace, &w);
-  // the stream-K piece counters start at zero (every GEMM launch leaves them zero again)
-  CLEF_CUDA_CHECK(cudaMemsetAsync(w.counts, 0, (size_t)lut6_split_count_bytes(),
-                                  static_cast<cudaStream_t>(stream)));
   w.x = x;  // the layer works on the caller's residual stream in place
   return run_layer(*layer, w, B, L, static_cast<cudaStream_t>(stream));
 }
@@ -445,8 +445,6 @@ clef_status clef_prefill_forward_chunk(const clef_model* model, const int32_t* i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   FwdWs w;
   fwd_layout(B, L, workspace, &w);
-  // the stream-K piece counters start at zero (every GEMM launch leaves them zero again)
-  CLEF_CUDA_CHECK(cudaMemsetAsync(w.counts, 0, (size_t)lut6_split_count_bytes(), s));
   const int64_t M = B * L;
   CLEF_TRY(embed_launch(ids, reinterpret_cast<const __half*>(model->embed), model->vocab, w.x, M, s));
   int gi = 0, ai = 0;
@@ -464,7 +462,8 @@ clef_status clef_prefill_forward_chunk(const clef_model* model, const int32_t* i
       ls.vc = reinterpret_cast<__half*>(state->vcache) + (size_t)ai * per_layer;
       ++ai;
     }
-    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls));
+    CLEF_TRY(run_layer(model->layers[i], w, B, L, s, ls,
+                       (model->flags & CLEF_MODEL_REPRODUCIBLE) != 0));
   }
   CLEF_TRY(rmsnorm_launch(w.x, reinterpret_cast<const __half*>(model->final_norm),
                           reinterpret_cast<__half*>(hidden), M, s, /*check_finite=*/true));

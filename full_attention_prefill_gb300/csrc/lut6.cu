@@ -63,10 +63,9 @@ constexpr int OFF_X = 0;
 constexpr int OFF_P = OFF_X + XS * X_BYTES;
 constexpr int OFF_T = OFF_P + AS * P_BYTES;
 constexpr int OFF_BAR = OFF_T + 2 * TBL_BYTES;
-constexpr int NUM_BARS = 3 * AS + 4 + 3 + 2;
+constexpr int NUM_BARS = 3 * AS + 4 + 3;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_FLAG = OFF_SLOT + 16;       // stream-K: "this CTA finishes the tile"
-constexpr int SMEM_USED = OFF_FLAG + 16;
+constexpr int SMEM_USED = OFF_SLOT + 16;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(A_COL + AS * 32 <= TMEM_COLS, "tensor memory budget");
@@ -162,184 +161,28 @@ __device__ __forceinline__ void tile_coord(int t, int n_tiles, int m_tiles, int&
   n0 = (local / gm) * BN;
 }
 
-// ---- schedule ------------------------------------------------------------------------------
-// Tiles [0, dp) go whole to the CTAs in turn (CTA c: tiles c, c + G, ...).  The k-steps of the
-// remaining tiles are shared evenly by the first `sk` CTAs (stream-K): CTA c takes steps
-// [c S / sk, (c + 1) S / sk) of the S = (tiles - dp) * num_kb steps (tile-major), cut into one
-// segment per tile it touches (at most 3: the tiles left over are fewer than 2 G, so a share is
-// under 2 num_kb steps).  A stream-K segment writes its partial sums to partial slot 3 c + i;
-// the last CTA to finish a tile adds the tile's pieces in CTA order and writes the output.
-struct Seg {
-  int tile, kb0, kb1;
-  int slot;        // -1: a whole tile of the data-parallel part
-  int sk_tile;     // stream-K tile index (tile - dp)
-};
-
-// 32-bit arithmetic throughout: the shared steps S are fewer than 2 SMs x num_kb (num_kb <=
-// 2^14), so c * S stays far below 2^31.
-struct Sched {
-  int G, num_tiles, num_kb, dp, sk;
-  __host__ __device__ int sk_steps() const { return (num_tiles - dp) * num_kb; }
-  __host__ __device__ int share_begin(int c) const {
-    return (int)((unsigned)c * (unsigned)sk_steps() / (unsigned)sk);
-  }
-  // segment j of CTA c; false when there is none
-  __host__ __device__ bool seg(int c, int j, Seg& g) const {
-    const int n_dp = c < dp ? (dp - 1 - c) / G + 1 : 0;
-    if (j < n_dp) {
-      g.tile = c + j * G;
-      g.kb0 = 0;
-      g.kb1 = num_kb;
-      g.slot = -1;
-      g.sk_tile = -1;
-      return true;
-    }
-    if (c >= sk || sk_steps() == 0) return false;
-    const int i = j - n_dp;
-    const int a = share_begin(c), b = share_begin(c + 1);
-    const int t = a / num_kb + i;
-    const int s0 = t * num_kb > a ? t * num_kb : a;
-    const int s1 = (t + 1) * num_kb < b ? (t + 1) * num_kb : b;
-    if (s0 >= s1) return false;
-    g.tile = dp + t;
-    g.kb0 = s0 - t * num_kb;
-    g.kb1 = s1 - t * num_kb;
-    g.slot = 3 * c + i;
-    g.sk_tile = t;
-    return true;
-  }
-  // the CTA whose share holds shared step s
-  __host__ __device__ int owner(int s) const {
-    int c = (int)((unsigned)s * (unsigned)sk / (unsigned)sk_steps());
-    while (c > 0 && share_begin(c) > s) --c;
-    while (share_begin(c + 1) <= s) ++c;
-    return c;
-  }
-  // the CTAs whose shares hold steps of stream-K tile t: c_lo .. c_hi
-  __host__ __device__ void pieces(int t, int& c_lo, int& c_hi) const {
-    c_lo = owner(t * num_kb);
-    c_hi = owner(t * num_kb + num_kb - 1);
-  }
-};
-
-// What one epilogue warp needs to write its 32 channels x 64 tokens of a tile.
-struct EpiCtx {
-  void* y;
-  int64_t ldy;
-  int M, N, mode;
-  int ecol, ch, quarter, lane;
-};
-
-// Write Y for the warp's 32 channels x 64 tokens of the tile at (n0e, m0e) from r0 (tokens
-// ecol .. ecol + 31) and r1 (tokens ecol + 32 .. ecol + 63).
-__device__ __forceinline__ void store_tile(const EpiCtx& x, int n0e, int m0e,
-                                           const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
-  const int tok0 = m0e + x.ecol;
-  const int col = n0e + x.ch;
-  if (x.mode == EPI_SWIGLU_F16) {
-    // lanes 0..15: gate rows, lanes 16..31: the up rows of the same channels; the gate lane
-    // writes tokens 0..31 of the warp's 64, the up lane tokens 32..63
-    const bool up = x.lane >= 16;
-    const int oc = n0e / 2 + x.quarter * 16 + (x.lane & 15);
-    __half* out = reinterpret_cast<__half*>(x.y);
-    const bool oc_ok = oc < x.N / 2;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t send = up ? r0[i] : r1[i];
-      const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
-      const float gate = up ? other : __uint_as_float(r0[i]);
-      const float upv = up ? __uint_as_float(r1[i]) : other;
-      const int tok = tok0 + (up ? 32 : 0) + i;
-      if (oc_ok && tok < x.M) out[(int64_t)tok * x.ldy + oc] = __float2half_rn(silu_f(gate) * upv);
-    }
-  } else if (col < x.N) {
-    if (x.mode == EPI_F16) {
-      __half* out = reinterpret_cast<__half*>(x.y) + col;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (tok0 + i < x.M) out[(int64_t)(tok0 + i) * x.ldy] = __float2half_rn(__uint_as_float(r0[i]));
-        if (tok0 + 32 + i < x.M)
-          out[(int64_t)(tok0 + 32 + i) * x.ldy] = __float2half_rn(__uint_as_float(r1[i]));
-      }
-    } else if (x.mode == EPI_F32) {
-      float* out = reinterpret_cast<float*>(x.y) + col;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (tok0 + i < x.M) out[(int64_t)(tok0 + i) * x.ldy] = __uint_as_float(r0[i]);
-        if (tok0 + 32 + i < x.M) out[(int64_t)(tok0 + 32 + i) * x.ldy] = __uint_as_float(r1[i]);
-      }
-    } else {
-      // residual add, done by L2: each element receives exactly one add per launch (the same
-      // as load + add + store), so launches repeat bit for bit
-      float* out = reinterpret_cast<float*>(x.y) + col;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (tok0 + i < x.M) red_add_f32(out + (int64_t)(tok0 + i) * x.ldy, __uint_as_float(r0[i]));
-        if (tok0 + 32 + i < x.M)
-          red_add_f32(out + (int64_t)(tok0 + 32 + i) * x.ldy, __uint_as_float(r1[i]));
-      }
-    }
-  }
-}
-
-// The end of a stream-K piece, once every epilogue warp has stored its partial sums (and fenced
-// them) and arrived on bar_pc: one thread counts the piece for the tile; the CTA that brings the
-// count to the tile's number of pieces adds all pieces (its own included, read back from L2) in
-// CTA order and writes the tile.
-__device__ __forceinline__ bool sk_finish(const EpiCtx& x, const Sched& sc, int tile, int sk_tile,
-                                       int n0e, int m0e, const float* part,
-                                       unsigned* tile_count, uint32_t bar_pc, uint32_t bar_pd,
-                                       volatile int* sk_last, int parity, bool leader,
-                                       unsigned* status) {
-  int c_lo, c_hi;
-  sc.pieces(sk_tile, c_lo, c_hi);
-  if (leader) {
-    int last = 0;
-    if (mbar_wait(bar_pc, (uint32_t)parity, status, DEV_TIMEOUT_EPILOGUE)) {
-      const unsigned before = atomicAdd(tile_count + sk_tile, 1u);
-      last = before == (unsigned)(c_hi - c_lo) ? 1 : 0;
-      if (last) tile_count[sk_tile] = 0u;   // ready for the next launch
-      __threadfence();
-    }
-    *sk_last = last;
-    mbar_arrive(bar_pd);
-  }
-  if (!mbar_wait(bar_pd, (uint32_t)parity, status, DEV_TIMEOUT_EPILOGUE)) return false;
-  if (*sk_last) {
-    uint32_t r0[32], r1[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r0[i] = r1[i] = __float_as_uint(0.f);
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int slot = 3 * c + (sk_tile - sc.share_begin(c) / sc.num_kb);
-      const float* piece = part + (int64_t)slot * (BT * BN);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __ldcg(piece + (x.ecol + i) * BN + x.ch));
-        r1[i] = __float_as_uint(__uint_as_float(r1[i]) +
-                                __ldcg(piece + (x.ecol + 32 + i) * BN + x.ch));
-      }
-    }
-    store_tile(x, n0e, m0e, r0, r1);
-  }
-  (void)tile;
-  return true;
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
-                     void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode, Sched sc,
-                     float* __restrict__ part, unsigned* __restrict__ tile_count,
-                     unsigned* status) {
+                     void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
+                     int ksplit, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int num_kb = K / BK;
   const int n_tiles = (N + BN - 1) / BN;
   const int m_tiles = (M + BT - 1) / BT;
-  const int cta = blockIdx.x;
+  const int num_tiles = n_tiles * m_tiles;
+  // work units: (tile, k part); with ksplit > 1 (residual-add mode only) each unit covers
+  // num_kb / ksplit steps and adds its partial sum into Y
+  const int nkb = num_kb / ksplit;
+  const int num_units = num_tiles * ksplit;
+  // the accumulator of tile i is drained after the first `lead` steps of tile i+1 have been
+  // dequantised, so the MMAs of tile i+1 start as soon as it is free
+  const int lead = min(AS - 1, nkb - 1);
 
   // One "ready" and one "empty" barrier per step (ring of AS): step g may run its MMAs once its
   // X tile has landed and its A stage is written (ready[g % AS]: the X bytes plus one arrival
@@ -354,10 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar_accf = bar_tempty + 16;           // accumulator complete
   const uint32_t bar_acce = bar_accf + 8;              // accumulator drained
   const uint32_t bar_fin = bar_acce + 8;               // the MMA thread's last MMAs completed
-  const uint32_t bar_pc = bar_fin + 8;                 // stream-K: every warp's partial stored
-  const uint32_t bar_pd = bar_pc + 8;                  // stream-K: the tile counter was read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
-  volatile int* sk_last = reinterpret_cast<volatile int*>(smem + OFF_FLAG);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < AS; ++s) {
@@ -372,8 +212,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_accf, 1);
     mbar_init(bar_acce, NUM_DQ_WARPS);
     mbar_init(bar_fin, 1);
-    mbar_init(bar_pc, NUM_DQ_WARPS);
-    mbar_init(bar_pd, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_x);
     tma_prefetch_desc(&tmap_p);
@@ -390,17 +228,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int first = blockIdx.x;
+  const int stride = gridDim.x;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- X loads
     if (lane == 0) {
       int64_t g = 0;
       bool ok = true;
-      Seg sg;
-      for (int j = 0; ok && sc.seg(cta, j, sg); ++j) {
+      for (int u = first; u < num_units && ok; u += stride) {
         int n0, m0;
-        tile_coord(sg.tile, n_tiles, m_tiles, n0, m0);
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++g) {
+        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        const int kb0 = (u / num_tiles) * nkb;
+        for (int kb = kb0; kb < kb0 + nkb; ++kb, ++g) {
           // X slot g % XS was last read by step g - XS
           const int64_t f = g - XS;
           if (f >= 0 && !mbar_wait(bar_empty + 8 * (int)(f % AS), (uint32_t)(f / AS) & 1, status,
@@ -424,10 +264,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int64_t g = 0;
       int it = 0;
       bool ok = true;
-      Seg sg;
-      for (; ok && sc.seg(cta, it, sg); ++it) {
+      for (int u = first; u < num_units && ok; u += stride, ++it) {
         int n0, m0;
-        tile_coord(sg.tile, n_tiles, m_tiles, n0, m0);
+        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        const int kb0 = (u / num_tiles) * nkb;
         const int ts = it & 1;
         if (it >= 2 && !mbar_wait(bar_tempty + 8 * ts, ((uint32_t)(it >> 1) & 1) ^ 1, status,
                                   DEV_TIMEOUT_TMA)) {
@@ -438,7 +278,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(bar_tfull + 8 * ts, groups * 128);
         bulk_load(sb + OFF_T + ts * TBL_BYTES, lut + (size_t)(n0 / 16) * 64, groups * 128,
                   bar_tfull + 8 * ts);
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++g) {
+        for (int kb = kb0; kb < kb0 + nkb; ++kb, ++g) {
           // slot s (indices and A stage) was last used by step g - AS
           const int s = (int)(g % AS);
           const uint32_t ph = (uint32_t)(g / AS) & 1;
@@ -451,7 +291,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_3d(sb + OFF_P + s * P_BYTES, &tmap_p, bar_pfull + 8 * s, 0, 3 * kb, n0 / 16);
         }
       }
-      // `it` segments had their tables requested (the loop stops on the first missing one)
       for (int64_t h = g > AS ? g - AS : 0; h < g; ++h)
         mbar_wait(bar_pfull + 8 * (int)(h % AS), (uint32_t)(h / AS) & 1, status, DEV_TIMEOUT_TMA);
       for (int u = it > 2 ? it - 2 : 0; u < it; ++u)
@@ -463,14 +302,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BN, BT);
       int sx = 0, sa = 0;      // X slot and ready/empty slot of the current step
       uint32_t ph = 0;         // phase parity of ready[sa]
+      int it = 0;
       bool ok = true;
-      Seg sg;
-      for (int it = 0; ok && sc.seg(cta, it, sg); ++it) {
+      for (int u = first; u < num_units && ok; u += stride, ++it) {
         if (it >= 1 && !mbar_wait(bar_acce, (uint32_t)(it - 1) & 1, status, DEV_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(bar_ready + 8 * sa, ph, status, DEV_TIMEOUT_MMA)) {
             ok = false;
             break;
@@ -478,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a = tmem + A_COL + sa * 32;
           const uint32_t b = sb + OFF_X + sx * X_BYTES;
-          tc_mma_f16_ts(tmem, a, sdesc_k_sw128(b), idesc, kb != sg.kb0);
+          tc_mma_f16_ts(tmem, a, sdesc_k_sw128(b), idesc, kb != 0);
           tc_mma_f16_ts(tmem, a + 8, sdesc_k_sw128(b + 32), idesc, 1);
           tc_mma_f16_ts(tmem, a + 16, sdesc_k_sw128(b + 64), idesc, 1);
           tc_mma_f16_ts(tmem, a + 24, sdesc_k_sw128(b + 96), idesc, 1);
@@ -504,20 +343,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ecol = (dq >> 2) * 64;                   // epilogue: token columns ecol .. +63
     const uint32_t tl = tmem + ((uint32_t)(grp * 16) << 16) + A_COL;
     const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + ecol;
-    const int ch = quarter * 32 + lane;                // this lane's channel in the tile
-    int sk_done = 0;                                   // stream-K epilogues so far (parities)
 
-    const EpiCtx ex{y, ldy, M, N, mode, ecol, ch, quarter, lane};
-
-    // Drain this warp's 32 lanes x 64 columns of the accumulator of this CTA's segment `ite`,
-    // release it, then write Y, or (a stream-K piece) store the partial sums and finish the
-    // piece (sk_finish).  The segment is looked up again here, so that the dequantisation loop
-    // keeps only its index.
-    auto epilogue = [&](int ite) -> bool {
-      Seg e;
-      sc.seg(cta, ite, e);
-      int n0e, m0e;
-      tile_coord(e.tile, n_tiles, m_tiles, n0e, m0e);
+    // Drain this warp's 32 lanes x 64 columns of the accumulator of the tile at (n0e, m0e),
+    // release it, then write Y from registers.
+    auto epilogue = [&](int n0e, int m0e, int ite, int kpart) -> bool {
+      const int tok0 = m0e + ecol;
+      const int col = n0e + quarter * 32 + lane;
       if (!mbar_wait(bar_accf, (uint32_t)ite & 1, status, DEV_TIMEOUT_EPILOGUE)) return false;
       tc_fence_after();
       uint32_t r0[32], r1[32];
@@ -527,46 +358,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acce);
-      if (e.slot < 0) {
-        store_tile(ex, n0e, m0e, r0, r1);
-        return true;
-      }
-      // a stream-K piece: partial sums [token][channel] in its slot, fenced before the count
-      float* mine = part + (int64_t)e.slot * (BT * BN);
+      if (mode == EPI_SWIGLU_F16) {
+        // lanes 0..15: gate rows, lanes 16..31: the up rows of the same channels; the gate lane
+        // writes tokens 0..31 of the warp's 64, the up lane tokens 32..63
+        const bool up = lane >= 16;
+        const int oc = n0e / 2 + quarter * 16 + (lane & 15);
+        __half* out = reinterpret_cast<__half*>(y);
+        const bool oc_ok = oc < N / 2;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        mine[(ecol + i) * BN + ch] = __uint_as_float(r0[i]);
-        mine[(ecol + 32 + i) * BN + ch] = __uint_as_float(r1[i]);
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t send = up ? r0[i] : r1[i];
+          const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+          const float gate = up ? other : __uint_as_float(r0[i]);
+          const float upv = up ? __uint_as_float(r1[i]) : other;
+          const int tok = tok0 + (up ? 32 : 0) + i;
+          if (oc_ok && tok < M) out[(int64_t)tok * ldy + oc] = __float2half_rn(silu_f(gate) * upv);
+        }
+      } else if (col < N) {
+        if (mode == EPI_F16) {
+          __half* out = reinterpret_cast<__half*>(y) + col;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (tok0 + i < M) out[(int64_t)(tok0 + i) * ldy] = __float2half_rn(__uint_as_float(r0[i]));
+            if (tok0 + 32 + i < M)
+              out[(int64_t)(tok0 + 32 + i) * ldy] = __float2half_rn(__uint_as_float(r1[i]));
+          }
+        } else if (mode == EPI_F32 || mode == EPI_PART_F32) {
+          // a k-part of a split residual add goes to its own slice [kpart][M][ldy]
+          float* out = reinterpret_cast<float*>(y) + col +
+                       (mode == EPI_PART_F32 ? (int64_t)kpart * M * ldy : 0);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (tok0 + i < M) out[(int64_t)(tok0 + i) * ldy] = __uint_as_float(r0[i]);
+            if (tok0 + 32 + i < M) out[(int64_t)(tok0 + 32 + i) * ldy] = __uint_as_float(r1[i]);
+          }
+        } else {
+          // residual add, done by L2; no load latency on this path.  Without a K split each
+          // element receives exactly one add per launch (the same as load + add + store); with
+          // one, the parts' adds land in any order, so such launches repeat only to fp32
+          // rounding
+          float* out = reinterpret_cast<float*>(y) + col;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (tok0 + i < M) red_add_f32(out + (int64_t)(tok0 + i) * ldy, __uint_as_float(r0[i]));
+            if (tok0 + 32 + i < M)
+              red_add_f32(out + (int64_t)(tok0 + 32 + i) * ldy, __uint_as_float(r1[i]));
+          }
+        }
       }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pc);
-      const bool done = sk_finish(ex, sc, e.tile, e.sk_tile, n0e, m0e, part, tile_count, bar_pc,
-                                  bar_pd, sk_last, sk_done & 1, dq == 0 && lane == 0, status);
-      ++sk_done;
-      return done;
+      return true;
     };
 
     int64_t g = 0;
-    bool ok = true;
-    int pending = -1;       // the segment whose epilogue is due
-    Seg sg;
     int it = 0;
-    for (; ok && sc.seg(cta, it, sg); ++it) {
+    bool ok = true;
+    int pn0 = -1, pm0 = 0, pkp = 0;  // tile (and k-part) whose epilogue is pending
+    for (int u = first; u < num_units && ok; u += stride, ++it) {
+      int n0, m0;
+      tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
       const int ts = it & 1;
       if (!mbar_wait(bar_tfull + 8 * ts, (uint32_t)(it >> 1) & 1, status, DEV_TIMEOUT_DEQUANT)) {
         ok = false;
         break;
       }
       const uint32_t tb = sb + OFF_T + ts * TBL_BYTES + grp * 128;
-      // the accumulator of the previous segment is drained after the first `lead` steps of this
-      // one have been dequantised, so its MMAs start as soon as the accumulator is free
-      const int nsteps = sg.kb1 - sg.kb0;
-      const int lead = min(AS - 1, nsteps - 1);
-      for (int step = 0; step < nsteps; ++step, ++g) {
-        if (step == lead && pending >= 0) {
-          ok = epilogue(pending);
-          pending = -1;
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        if (kb == lead && pn0 >= 0) {
+          ok = epilogue(pn0, pm0, it - 1, pkp);
+          pn0 = -1;
           if (!ok) break;
         }
         if ((int)(g & 1) != par) continue;
@@ -602,16 +461,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * ts);  // done with this segment's tables
-      pending = it;
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * ts);  // done with this tile's tables
+      pn0 = n0;
+      pm0 = m0;
+      pkp = u / num_tiles;
     }
-    if (ok && pending >= 0) epilogue(pending);
+    if (ok && pn0 >= 0) epilogue(pn0, pm0, it - 1, pkp);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// y[t][c] += part[0][t][c] + part[1][t][c] + ... added one part at a time in part order (the
+// same sequence of fp32 additions on every run); part is [parts][M][N].  Four columns per thread.
+__global__ void split_reduce_kernel(float* __restrict__ y, int64_t ldy, const float* __restrict__ part,
+                                    int parts, int64_t M, int64_t N) {
+  const int64_t quads = M * (N / 4);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < quads;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / (N / 4), c = 4 * (i % (N / 4));
+    float4 acc = *reinterpret_cast<const float4*>(y + t * ldy + c);
+    for (int p = 0; p < parts; ++p) {
+      const float4 v = *reinterpret_cast<const float4*>(part + ((int64_t)p * M + t) * N + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(y + t * ldy + c) = acc;
   }
 }
 
@@ -656,32 +537,30 @@ __global__ void lut6_tile_kernel(const uint8_t* __restrict__ packed, int64_t n, 
 
 }  // namespace lut
 
-int64_t lut6_split_part_bytes() { return (int64_t)num_sms() * 3 * lut::BT * lut::BN * 4; }
-int64_t lut6_split_count_bytes() { return (int64_t)num_sms() * 2 * 4; }
-
-// The schedule of one launch: every tile data-parallel, or (given the partial-sum workspace)
-// the full waves data-parallel and the rest stream-K, whichever leaves the busiest CTA fewer
-// k-steps (an epilogue counted as about 4 steps; a stream-K share adds two partial epilogues
-// and the final sum, about 14), by a margin of 8 steps.
-static lut::Sched plan_schedule(int64_t M, int64_t N, int64_t K, int sms, bool can_split) {
+int lut6_add_split(int64_t M, int64_t N, int64_t K) {
+  // When there are too few tiles to fill the GPU, pick the split that minimises the longest
+  // CTA's work, counted in k-steps plus about four steps per unit for its epilogue.
   using namespace lut;
-  const int tiles = (int)(((N + BN - 1) / BN) * ((M + BT - 1) / BT));
-  const int nkb = (int)(K / BK);
-  Sched dp_only{tiles < sms ? tiles : sms, tiles, nkb, tiles, 0};
-  if (!can_split || tiles % sms == 0) return dp_only;
-  const int64_t cost_dp = (int64_t)((tiles + sms - 1) / sms) * (nkb + 4);
-  const int waves = tiles / sms;
-  const int dp = waves >= 1 ? (waves - 1) * sms : 0;
-  const int64_t S = (int64_t)(tiles - dp) * nkb;   // < 2 sms num_kb: fits the 32-bit schedule
-  const int sk = (int)std::max<int64_t>(1, std::min<int64_t>(sms, S / 8));
-  const int64_t cost_sk = (int64_t)(dp / sms) * (nkb + 4) + (S + sk - 1) / sk + 14;
-  if (cost_sk + 8 >= cost_dp) return dp_only;
-  return Sched{sms, tiles, nkb, dp, sk};
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);
+  const int64_t sms = num_sms();
+  const int64_t nkb = K / BK;
+  int ksplit = 1;
+  int64_t best = -1;
+  for (int s = 1; s <= 8; ++s) {
+    if (nkb % s != 0 || nkb / s < 4) continue;
+    const int64_t rounds = (tiles * s + sms - 1) / sms;
+    const int64_t cost = rounds * (nkb / s + 4);
+    if (best < 0 || cost < best) {
+      best = cost;
+      ksplit = s;
+    }
+  }
+  return ksplit;
 }
 
 clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
-                             cudaStream_t stream, float* part, unsigned* counts) {
+                             cudaStream_t stream, float* part_ws) {
   using namespace lut;
   if (M == 0) return CLEF_OK;
   CUtensorMap tx, tp;
@@ -701,62 +580,38 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   CLEF_CUDA_CHECK(smem_opt_in((const void*)lut6_gemm_kernel, SMEM_BYTES, &attr));
   // the tables are fetched with 16-byte bulk copies
   if ((reinterpret_cast<uintptr_t>(lut) & 15) != 0) return CLEF_E_ALIGN;
+  const int64_t tiles = ((N + BN - 1) / BN) * ((M + BT - 1) / BT);
   const int sms = num_sms();
-  const bool can_split = part != nullptr && counts != nullptr &&
-                         (reinterpret_cast<uintptr_t>(part) & 15) == 0;
-  const Sched sc = plan_schedule(M, N, K, sms, can_split);
+  // Residual-add mode may split K across CTAs (each part adds its partial sum, or with part_ws
+  // writes it to its own slice for the ordered reduction below)
+  const int ksplit = mode == EPI_ADD_F32 ? lut6_add_split(M, N, K) : 1;
+  const bool ordered = ksplit > 1 && part_ws != nullptr;
+  if (ordered && (N % 4 != 0 || ldy % 4 != 0 || (reinterpret_cast<uintptr_t>(part_ws) & 15) != 0))
+    return CLEF_E_ALIGN;
+  const int64_t units = tiles * ksplit;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
   const double out_bytes = mode == EPI_F16 ? 2.0 * M * N
                            : mode == EPI_F32 ? 4.0 * M * N
                            : mode == EPI_ADD_F32 ? 8.0 * M * N
                                                  : 1.0 * M * N;  // SwiGLU: fp16 [M, N/2]
-  TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
-                0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
-  lut6_gemm_kernel<<<(unsigned)sc.G, NUM_THREADS, SMEM_BYTES, stream>>>(
-      tx, tp, lut, y, ldy, (int)M, (int)N, (int)K, mode, sc, part, counts, status_word_ptr());
-  CLEF_LAUNCH_CHECK();
-  return CLEF_OK;
-}
-
-}  // namespace clef
-
-// Host only: the schedule a LUT-6 GEMM launch of this shape would use on `sms` SMs with the
-// stream-K workspace (for tests of its index arithmetic without a GPU).  plan[4] = grid,
-// data-parallel tiles, stream-K CTAs, tiles; segs[5 * i ..] = (cta, tile, kb0, kb1, slot) of
-// every CTA's segments in order; pieces[2 * t ..] = (first, last) CTA of stream-K tile t.
-extern "C" clef_status clef_debug_lut6_schedule(int64_t M, int64_t N, int64_t K, int32_t sms,
-                                                int32_t* plan, int32_t* segs, int32_t max_segs,
-                                                int32_t* n_segs, int32_t* pieces,
-                                                int32_t max_pieces) {
-  using namespace clef;
-  using namespace clef::lut;
-  if (!plan || !segs || !n_segs || !pieces || M < 1 || N < 16 || K < 64 || sms < 1)
-    return CLEF_E_INVALID;
-  const Sched sc = plan_schedule(M, N, K, sms, true);
-  plan[0] = sc.G;
-  plan[1] = sc.dp;
-  plan[2] = sc.sk;
-  plan[3] = sc.num_tiles;
-  int n = 0;
-  for (int c = 0; c < sc.G; ++c) {
-    Seg g;
-    for (int j = 0; sc.seg(c, j, g); ++j) {
-      if (n == max_segs) return CLEF_E_SHAPE;
-      int32_t* r = segs + 5 * n++;
-      r[0] = c;
-      r[1] = g.tile;
-      r[2] = g.kb0;
-      r[3] = g.kb1;
-      r[4] = g.slot;
-    }
+  {
+    TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
+                  0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
+    lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+        tx, tp, lut, ordered ? static_cast<void*>(part_ws) : y, ordered ? N : ldy, (int)M, (int)N,
+        (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, status_word_ptr());
+    CLEF_LAUNCH_CHECK();
   }
-  *n_segs = n;
-  const int sk_tiles = sc.num_tiles - sc.dp;
-  if (sk_tiles > max_pieces) return CLEF_E_SHAPE;
-  for (int t = 0; t < sk_tiles && sc.sk > 0; ++t) sc.pieces(t, pieces[2 * t], pieces[2 * t + 1]);
+  if (ordered) {
+    TraceScope ts(stream, "split_reduce", 0.0, 4.0 * M * N * (2 + ksplit));
+    const int64_t quads = M * (N / 4);
+    const int64_t blocks = std::min<int64_t>((quads + 255) / 256, (int64_t)sms * 8);
+    split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(y), ldy, part_ws,
+                                                              ksplit, M, N);
+    CLEF_LAUNCH_CHECK();
+  }
   return CLEF_OK;
 }
-
-namespace clef {
 
 clef_status lut6_tile_launch(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,
                              cudaStream_t stream) {

@@ -9,25 +9,22 @@ enum Epilogue : int {
   EPI_F32 = 1,        // y fp32 = acc
   EPI_ADD_F32 = 2,    // y fp32 += acc (residual add, in place)
   EPI_SWIGLU_F16 = 3, // y fp16 [m, n/2] = SiLU(gate) * up, gate/up rows interleaved by 16
+  EPI_PART_F32 = 4,   // (internal) k-part p of a split residual add: part[p][m][n] fp32 = acc
 };
 
-// Workspace of the stream-K part of a launch (see lut6_gemm_launch), on the current device:
-// partial sums (fp32, 3 tiles per SM) and the per-tile piece counters (zeroed before first use;
-// every launch leaves them zero again).
-int64_t lut6_split_part_bytes();
-int64_t lut6_split_count_bytes();
+// The number of k-parts a residual-add launch of this shape is split into (1: no split).
+int lut6_add_split(int64_t M, int64_t N, int64_t K);
 
 // y[m, n] (row stride ldy elements) = x[m, k] . W^T with W in the tiled layout
 // (clef_lut6_tile).  Requires n % 16 == 0, k % 64 == 0 (n % 32 == 0 for EPI_SWIGLU_F16), x packed
 // [m, k], lut 16-byte aligned.
-// With part and counts given (lut6_split_part_bytes / lut6_split_count_bytes, counters zero), a
-// launch whose tiles leave the last wave of SMs partly idle runs its full waves data-parallel
-// and shares the k-steps of the remaining tiles evenly among all SMs (stream-K): each share
-// stores its partial sums and the SM that finishes a tile last adds the tile's pieces in a fixed
-// order, so every run gives the same bits.  Without them every tile runs whole on one SM.
+// In EPI_ADD_F32 mode with part_ws set and a split launch, the k-parts write their partial
+// sums to part_ws ([parts][M][N] fp32, lut6_add_split parts) and one more kernel adds them to y in
+// part order: the result is then the same bits on every run (without part_ws the parts add
+// straight into y in whatever order they finish).
 clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half* lut, void* y,
                              int64_t ldy, int64_t M, int64_t N, int64_t K, int mode,
-                             cudaStream_t stream, float* part = nullptr, unsigned* counts = nullptr);
+                             cudaStream_t stream, float* part_ws = nullptr);
 
 // canonical packed [n, k*3/4] -> tiled layout of the GEMM (same size)
 clef_status lut6_tile_launch(const uint8_t* packed, int64_t n, int64_t k, uint8_t* tiled,

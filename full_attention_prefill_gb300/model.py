@@ -100,8 +100,14 @@ class DeviceModel:
         m.embed = _ptr(self.embed)
         m.vocab = self.embed.shape[0]
         m.final_norm = _ptr(self.final_norm)
+        m.flags = 0
         self.struct = m
         self._ws = None
+
+    def set_reproducible(self, on: bool = True):
+        """Ordered reduction of split residual adds (clef.h CLEF_MODEL_REPRODUCIBLE): every run of
+        the same prefill then gives the same bits."""
+        self.struct.flags = 1 if on else 0
 
     @staticmethod
     def kind_of(layer_index: int) -> int:

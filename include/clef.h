@@ -142,14 +142,10 @@ CLEF_API clef_status clef_lut6_gemm(const uint16_t* x, const uint8_t* tiled, con
    the row-major bit stream of clef_lut6_pack).  The GEMM's tensor-memory dequantisation reads a
    lane's 32 indices of one k-block as 24 contiguous bytes, which the card's row-major stream
    does not give, so this call first writes the tiled permutation (clef_lut6_tile) into the
-   caller's workspace, then multiplies: one extra pass over the packed bytes per call.  The rest
-   of the workspace lets a launch whose tiles leave the last wave of SMs partly idle share that
-   wave's k-blocks among all SMs (stream-K, as the prefill does); its pieces are added in a
-   fixed order, so the result is the same on every run (it may differ from clef_lut6_gemm's in
-   the last bits of fp32 rounding).  A caller that multiplies by the same weight many times
-   should tile it once and call clef_lut6_gemm.  workspace: device, >=
-   clef_lut6_gemm_canonical_workspace_size(n, k) bytes, 16-byte aligned (CLEF_E_WORKSPACE if
-   smaller).  Other requirements as clef_lut6_gemm. */
+   caller's workspace, then runs clef_lut6_gemm on it: one extra pass over the packed bytes per
+   call.  A caller that multiplies by the same weight many times should tile it once and call
+   clef_lut6_gemm.  workspace: device, >= clef_lut6_gemm_canonical_workspace_size(n, k) bytes,
+   16-byte aligned (CLEF_E_WORKSPACE if smaller).  Other requirements as clef_lut6_gemm. */
 CLEF_API size_t clef_lut6_gemm_canonical_workspace_size(int64_t n, int64_t k);
 CLEF_API clef_status clef_lut6_gemm_canonical(const uint16_t* x, const uint8_t* packed,
                                               const uint16_t* lut, void* y, int32_t y_is_fp32,
@@ -249,7 +245,16 @@ typedef struct {
   const uint16_t* embed;     /* [vocab, 4096] fp16 token embeddings */
   int64_t vocab;             /* 248320 for clef-flash */
   const uint16_t* final_norm;/* [4096] fp16 */
+  int32_t flags;             /* 0, or CLEF_MODEL_REPRODUCIBLE */
 } clef_model;
+
+/* clef_model.flags: make every run of the same prefill give the same bits.  Short prefills
+   split the residual-add projections (out-proj, MLP down) over k-parts to fill the GPU; by
+   default each part adds its partial sum into the fp32 residual as it finishes, so the order of
+   those fp32 additions (and the last bits of the result) can change from run to run.  With this
+   flag each part writes its sums to the workspace and one more kernel adds them in part order.
+   Long prefills (no split) are reproducible either way. */
+#define CLEF_MODEL_REPRODUCIBLE 1
 
 /* Bytes of workspace clef_prefill_forward / clef_decoder_layer need for B requests of L
    positions. */
@@ -438,16 +443,6 @@ CLEF_API void clef_debug_fail_next(int32_t n_calls);
    carried state (only when the scan runs in pieces), o (only with_norm); -1 for a region not
    used.  offsets: 8 int64, caller owned; *total = the workspace bytes the scan needs.  For tests
    of the carving against the size query.  CLEF_E_INVALID for NULL outputs or B, L < 1. */
-/* Host only, no device call: the work schedule of a LUT-6 GEMM launch of shape M x N x K on `sms`
-   SMs when the stream-K workspace is given (as in the prefill): plan[4] = (CTAs, tiles run
-   whole, CTAs sharing the rest, tiles); segs[5 * i ..] = (CTA, tile, first k-block, end
-   k-block, partial slot or -1) for every segment, CTA by CTA in order (*n_segs of them, at most
-   max_segs); pieces[2 * t ..] = the first and last CTA holding k-blocks of shared tile t.  For
-   tests of the index arithmetic.  CLEF_E_SHAPE if the arrays are too small. */
-CLEF_API clef_status clef_debug_lut6_schedule(int64_t M, int64_t N, int64_t K, int32_t sms,
-                                              int32_t* plan, int32_t* segs, int32_t max_segs,
-                                              int32_t* n_segs, int32_t* pieces, int32_t max_pieces);
-
 CLEF_API clef_status clef_debug_gdn_workspace_layout(int64_t B, int64_t L, int32_t with_norm,
                                                      int64_t* offsets, int64_t* total);
 

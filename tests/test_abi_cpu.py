@@ -137,44 +137,3 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT,
                        timeout=300)
     assert "raised:" in r.stdout and "no fallback" in r.stdout, r.stdout + r.stderr
-
-
-@pytest.mark.parametrize("sms", [152, 148, 132, 7])
-def test_lut6_schedule_covers_every_step_once(lib, sms):
-    """The LUT-6 GEMM's work schedule (host arithmetic, no GPU): every (tile, k-block) of every
-    prefill shape is done exactly once; whole tiles go to CTAs in turn; the shared (stream-K)
-    tiles' segments write distinct partial slots below 3 x CTAs, at most 3 per CTA; the CTAs that
-    hold a shared tile's k-blocks are exactly the recorded piece range; shared tiles fit the
-    2 x SMs counters."""
-    shapes = [(M, N, K) for M in (1, 63, 130, 512, 1000, 4096, 16384)
-              for N, K in ((12288, 4096), (10240, 4096), (4096, 4096), (24576, 4096), (4096, 12288))]
-    shapes += [(77, 784, 320), (2600, 2048, 192)]
-    for M, N, K in shapes:
-        plan = (ctypes.c_int32 * 4)()
-        segs = (ctypes.c_int32 * (5 * 20000))()
-        pieces = (ctypes.c_int32 * (2 * 4 * sms))()
-        n = ctypes.c_int32(0)
-        rc = lib.clef_debug_lut6_schedule(M, N, K, sms, plan, segs, 20000, ctypes.byref(n), pieces, 4 * sms)
-        assert rc == 0
-        G, dp, sk, tiles = plan
-        nkb = K // 64
-        assert tiles == -(-N // 128) * -(-M // 256) and G <= sms and 0 <= dp <= tiles
-        assert (tiles - dp) < 2 * sms
-        cover = np.zeros((tiles, nkb), dtype=np.int32)
-        slots, per_cta, holders = set(), {}, {}
-        for i in range(n.value):
-            c, t, k0, k1, slot = segs[5 * i:5 * i + 5]
-            assert 0 <= c < G and 0 <= t < tiles and 0 <= k0 < k1 <= nkb
-            cover[t, k0:k1] += 1
-            if slot < 0:
-                assert t < dp and (k0, k1) == (0, nkb) and t % G == c
-            else:
-                assert t >= dp and c < sk and 3 * c <= slot < 3 * c + 3 and slot < 3 * G
-                assert slot not in slots
-                slots.add(slot)
-                per_cta[c] = per_cta.get(c, 0) + 1
-                holders.setdefault(t - dp, []).append(c)
-        assert np.all(cover == 1), (M, N, K)
-        assert all(v <= 3 for v in per_cta.values())
-        for t, cs in holders.items():
-            assert cs == list(range(pieces[2 * t], pieces[2 * t + 1] + 1)), (M, N, K, t)

@@ -74,16 +74,20 @@ def test_full_model_l512():
 
 
 @pytest.mark.slow
-def test_prefill_is_bit_identical_run_to_run():
-    """Every prefill is the same bits on every run: the LUT-6 GEMMs' schedule is fixed per shape
-    and the stream-K pieces of a tile (short prefills and last waves) are added in a fixed order,
-    and no other kernel adds in a run-dependent order.  Checked at L = 512 (GEMMs stream-K) and on
-    32 requests of 512 (a long prefill: data-parallel waves plus a stream-K last wave)."""
-    seed = 0
+def test_reproducible_prefill_is_bit_identical():
+    """With CLEF_MODEL_REPRODUCIBLE the split residual adds of a short prefill are summed in part
+    order, so two runs of the same 32-layer L = 512 request give the same bits; the result stays
+    within fp32 rounding of the default (unordered) path."""
+    seed, L = 0, 512
     m = synth_model(seed, 32)
-    for B, L in ((1, 512), (32, 512)):
-        ids = torch.from_numpy(synth.token_ids(seed, B, L)).cuda()
+    ids = torch.from_numpy(synth.token_ids(seed, 1, L)).cuda()
+    fast = m.forward(ids).clone()
+    m.set_reproducible(True)
+    try:
         a = m.forward(ids).clone()
         b = m.forward(ids).clone()
         clef.sync_status()
-        assert torch.equal(a, b), f"B={B} L={L}: runs differ"
+    finally:
+        m.set_reproducible(False)
+    assert torch.equal(a, b)
+    assert rel_rmse(a.double().cpu().numpy(), fast.double().cpu().numpy()) < 1e-2
