@@ -207,8 +207,10 @@ struct WySmem {
     } t;
   } u;
   __half K[C][LDH];
-  __half V[C][LDH];
-  float Tf[C][C + 4];                            // T in fp32
+  union {
+    float Tf[C][C + 4];                          // T in fp32, until its scaled fp16 copies exist
+    __half V[C][LDH];                            // then V (loaded behind the W product)
+  } tv;
   float gc[C];
   float bt[C];
   float eb[C];                                   // beta_r exp(g_r)
@@ -232,14 +234,14 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
-  // Q, K (key head h/2) and V (head h) rows, zero past the request's end
+  // Q and K (key head h/2) rows, zero past the request's end; V (head h) comes later, into the
+  // space of the fp32 T once that is consumed
   for (int i = tid; i < C * (D / 8); i += 128) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < nvalid;
     const int64_t rr = ok ? t0 + r : t0;
     cp_async16(smem_u32(&s.u.Q[r][c8]), qq + rr * (HK * D) + (h >> 1) * D + c8, ok);
     cp_async16(smem_u32(&s.K[r][c8]), kk + rr * (HK * D) + (h >> 1) * D + c8, ok);
-    cp_async16(smem_u32(&s.V[r][c8]), vv + rr * (HV * D) + h * D + c8, ok);
   }
   cp_async_commit();
   if (warp == 0) {
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
       if (r > lane) t[r] = -(a0 + a1);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) s.Tf[base + r][base + lane] = t[r];
+    for (int r = 0; r < 16; ++r) s.tv.Tf[base + r][base + lane] = t[r];
   }
   __syncthreads();
   // T, off-diagonal blocks at distance d: block (i, j = i - d); thread (block, column cc, row
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
       for (int kq = 4 * j; kq < 4 * i; ++kq) {   // 4 columns of A_i. (rows of T_.j) per step
         float tv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tv[e] = s.Tf[4 * kq + e][colg];
+        for (int e = 0; e < 4; ++e) tv[e] = s.tv.Tf[4 * kq + e][colg];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           const float4 av = *reinterpret_cast<const float4*>(&s.u.A[i0 + r][4 * kq]);
@@ -400,10 +402,10 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
         float acc = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; m += 4) {
-          const float4 tvv = *reinterpret_cast<const float4*>(&s.Tf[i0 + r][i0 + m]);
+          const float4 tvv = *reinterpret_cast<const float4*>(&s.tv.Tf[i0 + r][i0 + m]);
           acc += tvv.x * x[m] + tvv.y * x[m + 1] + tvv.z * x[m + 2] + tvv.w * x[m + 3];
         }
-        s.Tf[i0 + r][colg] = -acc;
+        s.tv.Tf[i0 + r][colg] = -acc;
       }
     }
     __syncthreads();
@@ -411,16 +413,28 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
   // A is dead: T diag(beta e^g) and T diag(beta) in fp16 (blocks above the diagonal are zero)
   for (int i = tid; i < C * C; i += 128) {
     const int r = i / C, sc = i % C;
-    const float tv = (sc >> 4) > (r >> 4) ? 0.f : s.Tf[r][sc];
+    const float tv = (sc >> 4) > (r >> 4) ? 0.f : s.tv.Tf[r][sc];
     s.u.t.Tw[r][sc] = __float2half_rn(tv * s.eb[sc]);
     s.u.t.Tu[r][sc] = __float2half_rn(tv * s.bt[sc]);
   }
   __syncthreads();
+  // the fp32 T is dead: V's rows into its space, landing while W = T diag(beta e^g) K runs
+  for (int i = tid; i < C * (D / 8); i += 128) {
+    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
+    const bool ok = r < nvalid;
+    const int64_t rr = ok ? t0 + r : t0;
+    cp_async16(smem_u32(&s.tv.V[r][c8]), vv + rr * (HV * D) + h * D + c8, ok);
+  }
+  cp_async_commit();
   // W = T diag(beta e^g) K and U' = T diag(beta) V  (rows 16w.., all 128 columns)
 #pragma unroll 1
   for (int which = 0; which < 2; ++which) {
+    if (which == 1) {
+      cp_async_wait<0>();
+      __syncthreads();   // V has landed for every thread
+    }
     const uint32_t sT = smem_u32(which == 0 ? &s.u.t.Tw[0][0] : &s.u.t.Tu[0][0]);
-    const uint32_t sB = smem_u32(which == 0 ? &s.K[0][0] : &s.V[0][0]);
+    const uint32_t sB = smem_u32(which == 0 ? &s.K[0][0] : &s.tv.V[0][0]);
     float acc[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
