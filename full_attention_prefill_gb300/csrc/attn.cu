@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
                                                    __half* __restrict__ kout, int64_t ldko, int L,
                                                    int pos0, int64_t kctx, int mstart, int mh,
                                                    int mw) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float cs[32], sn[32];
   const int64_t tok = blockIdx.x;
   const int64_t t = tok % L;
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const __half* __restrict__ q, int64_t ldq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __half* __restrict__ gate, int64_t ldg,
     __half* __restrict__ out, int64_t ldo, int L, int pos0, unsigned* status) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // the barriers and tensor memory are set up; now the inputs
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
@@ -435,6 +439,8 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
 // (request * L + t), `cols` fp16 per row (a multiple of 8), 16 bytes per thread.
 __global__ void kv_store_kernel(const __half* __restrict__ src, int64_t lds, __half* __restrict__ dst,
                                 int64_t ldd, int64_t M, int L, int pos0, int64_t dctx, int cols) {
+  pdl_trigger();
+  pdl_wait();
   const int per_row = cols / 8;
   const int64_t n = M * per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -455,10 +461,10 @@ clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t l
                         const MRope& mr) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
-  attn::rope_kernel<<<(unsigned)M, 128, 0, stream>>>(qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
-                                                     (int)L, (int)pos0, kctx, (int)mr.start,
-                                                     (int)mr.h, (int)mr.w);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(attn::rope_kernel, dim3((unsigned)M), dim3(128), 0, stream,
+       qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
+       (int)L, (int)pos0, kctx, (int)mr.start,
+       (int)mr.h, (int)mr.w));
   return CLEF_OK;
 }
 
@@ -492,9 +498,8 @@ clef_status flash_launch(const __half* q, int64_t ldq, const __half* k, int64_t 
   TraceScope ts(stream, "flash_attn",
                 4.0 * attn::D * attn::HQ * (double)B * ((double)L * pos0 + (double)L * (L + 1) / 2.0),
                 (double)B * L * (16 + 16 + 16) * attn::D * 2.0 + (double)B * (pos0 + L) * 8 * attn::D * 2.0);
-  attn::flash_tc_kernel<<<grid, attn::FLASH_THREADS, attn::FLASH_SMEM, stream>>>(
-      q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, (int)pos0, status_word_ptr());
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(attn::flash_tc_kernel, dim3(grid), dim3(attn::FLASH_THREADS), attn::FLASH_SMEM, stream,
+       q, ldq, mk, mv, gate, ldg, out, ldo, (int)L, (int)pos0, status_word_ptr()));
   return CLEF_OK;
 }
 
@@ -504,8 +509,8 @@ clef_status kv_store_launch(const __half* src, int64_t lds, __half* dst, int64_t
   TraceScope ts(stream, "kv_store", 0.0, (double)M * cols * 4.0);
   const int64_t n = M * (cols / 8);
   const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 4096);
-  attn::kv_store_kernel<<<grid, 256, 0, stream>>>(src, lds, dst, ldd, M, (int)L, (int)pos0, dctx, cols);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(attn::kv_store_kernel, dim3(grid), dim3(256), 0, stream,
+       src, lds, dst, ldd, M, (int)L, (int)pos0, dctx, cols));
   return CLEF_OK;
 }
 

@@ -66,6 +66,22 @@ struct TraceScope {
   }
 };
 
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 #define CLEF_CUDA_CHECK(expr)                                                      \
   do {                                                                             \
     cudaError_t _e = (expr);                                                       \
@@ -96,6 +112,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ---- programmatic dependent launch ----
+// A kernel launched with launch_pdl may start while the kernel before it on its stream finishes:
+// it lets its own successor launch at once (pdl_trigger) and waits for its predecessor to
+// complete, with its memory visible, before the first read of anything the predecessor wrote
+// (pdl_wait; a no-op when there is no such predecessor).  What runs before pdl_wait touches only
+// kernel parameters, shared memory and tensor memory.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void report(unsigned* status, unsigned code) {
   if (status) atomicCAS(status, 0u, code);

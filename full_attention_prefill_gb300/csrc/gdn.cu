@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
     const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
     const __half* __restrict__ conv_in, __half* __restrict__ q, __half* __restrict__ k,
     __half* __restrict__ v, int64_t M, int L) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t prep_smem[];
   __half* tile = reinterpret_cast<__half*>(prep_smem);   // [PREP_T + 3][PREP_CH], row i = token tok0 - 3 + i
   const int tid = threadIdx.x;
@@ -160,6 +162,8 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
 // thread reads the old rows it needs before writing.
 __global__ void conv_state_kernel(const __half* __restrict__ proj, int64_t ldp, __half* state,
                                   int64_t B, int L) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n = B * (8192 / 8);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -179,6 +183,8 @@ __global__ void conv_state_kernel(const __half* __restrict__ proj, int64_t ldp, 
 
 // g = log(alpha), clamped, for callers that pass alpha itself.
 __global__ void log_alpha_kernel(const float* __restrict__ alpha, float* __restrict__ g, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float a = alpha[i];
@@ -222,6 +228,8 @@ __global__ void __launch_bounds__(128) gdn_chunk_wy_kernel(
     const float* __restrict__ g, const float* __restrict__ beta, float* __restrict__ ef,
     __half* __restrict__ Wout, float* __restrict__ Uout, __half* __restrict__ Kdout,
     __half* __restrict__ AqkT, int L, int nch, int c0, int ncl) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t smraw[];
   WySmem& s = *reinterpret_cast<WySmem*>(smraw);
   // this launch covers chunks c0 .. c0 + ncl - 1 of every request
@@ -476,6 +484,8 @@ __global__ void __launch_bounds__(256) gdn_gated_norm_kernel(const __half* __res
                                                              int64_t ldz,
                                                              const __half* __restrict__ w,
                                                              __half* __restrict__ y, int64_t ldy) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t tok = blockIdx.x;
   const int c0 = threadIdx.x * 16;            // 16 consecutive values of head c0 / 128
   float ov[16], zv[16];
@@ -591,9 +601,9 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
   static std::atomic<uint64_t> attr{0};
   CLEF_CUDA_CHECK(smem_opt_in((const void*)gdn::gdn_prep_kernel, gdn::PREP_SMEM, &attr));
   dim3 grid(8192 / gdn::PREP_CH, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
-  gdn::gdn_prep_kernel<<<grid, 256, gdn::PREP_SMEM, stream>>>(proj, ldp, conv_w, conv_in, q, k, v,
-                                                               M, (int)L);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_prep_kernel, dim3(grid), dim3(256), gdn::PREP_SMEM, stream,
+       proj, ldp, conv_w, conv_in, q, k, v,
+       M, (int)L));
   return CLEF_OK;
 }
 
@@ -602,9 +612,8 @@ clef_status conv_state_launch(const __half* proj, int64_t ldp, __half* state, in
   if (B == 0) return CLEF_OK;
   TraceScope ts(stream, "conv_state", 0.0, (double)B * 3 * 8192 * 2 * 2);
   const int64_t n = B * (8192 / 8);
-  gdn::conv_state_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
-      proj, ldp, state, B, (int)L);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(gdn::conv_state_kernel, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256), 0, stream,
+       proj, ldp, state, B, (int)L));
   return CLEF_OK;
 }
 
@@ -652,9 +661,8 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
   const int nch = (int)((L + gdn::C - 1) / gdn::C);
   if (!g) {
     const int64_t n = M * gdn::HV;
-    gdn::log_alpha_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
-        alpha, w.g, n);
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(gdn::log_alpha_kernel, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256), 0, stream,
+         alpha, w.g, n));
     g = w.g;
   }
   __half* o = z ? w.o : out;
@@ -663,9 +671,8 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
     const double C = gdn::C, D = gdn::D, HVd = gdn::HV, nchunks = (double)B * ncl;
     TraceScope ts(s, "gdn_chunk_wy", nchunks * HVd * 8.0 * C * C * D,
                   nchunks * C * HVd * D * (2 + 2 + 2 + 2 + 4) + nchunks * HVd * C * C * 2);
-    gdn::gdn_chunk_wy_kernel<<<dim3((unsigned)(B * ncl), gdn::HV), 128, sizeof(gdn::WySmem), s>>>(
-        q, k, v, g, beta, w.ef, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch, (int)c0, (int)ncl);
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_chunk_wy_kernel, dim3(dim3((unsigned)(B * ncl), gdn::HV)), dim3(128), sizeof(gdn::WySmem), s,
+         q, k, v, g, beta, w.ef, w.W, w.U1, w.Kt, w.Aqk, (int)L, nch, (int)c0, (int)ncl));
     return CLEF_OK;
   };
   const int pieces = gdn_pieces(B, L);
@@ -701,9 +708,8 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
           for (int64_t b = 0; b < B; ++b) {
             const int64_t r0 = b * L + t0;
             TraceScope ts(ss->hi, "gdn_gated_norm", 0.0, (double)(t1 - t0) * 4096 * 2 * 3);
-            gdn::gdn_gated_norm_kernel<<<(unsigned)(t1 - t0), 256, 0, ss->hi>>>(
-                o + r0 * ldo_pass, z + r0 * ldz, ldz, o_norm, out + r0 * ldo, ldo);
-            CLEF_LAUNCH_CHECK();
+            CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_gated_norm_kernel, dim3((unsigned)(t1 - t0)), dim3(256), 0, ss->hi,
+                 o + r0 * ldo_pass, z + r0 * ldz, ldz, o_norm, out + r0 * ldo, ldo));
           }
         }
       }
@@ -720,8 +726,8 @@ clef_status gdn_scan_launch(const __half* q, const __half* k, const __half* v, c
   }
   if (z && pieces <= 1) {
     TraceScope ts(stream, "gdn_gated_norm", 0.0, (double)M * 4096 * 2 * 3);
-    gdn::gdn_gated_norm_kernel<<<(unsigned)M, 256, 0, stream>>>(o, z, ldz, o_norm, out, ldo);
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_gated_norm_kernel, dim3((unsigned)M), dim3(256), 0, stream,
+         o, z, ldz, o_norm, out, ldo));
   }
   return CLEF_OK;
 }

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
     const __grid_constant__ CUtensorMap tKd, const __grid_constant__ CUtensorMap tA,
     const __grid_constant__ CUtensorMap tO, const float* __restrict__ U1, const float* __restrict__ ef, const float* __restrict__ s0, float* __restrict__ s_out, int L,
     int nch, int c0, int ncl, unsigned* status) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // the barriers and tensor memory are set up; now the inputs
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -465,10 +467,9 @@ clef_status gdn_state_launch(const __half* q, const __half* Kd, const __half* W,
                 // per (chunk, value head): W, Kd, U', out rows (2 + 2 + 4 + 2 bytes x D), its
                 // share of the q rows (a key head serves two value heads), Aqk^T
                 chunks * Cd * (Dd * (2 + 2 + 4 + 2) + Dd * 2.0 * HK / HV + Cd * 2));
-  gdn_state_tc_kernel<<<(unsigned)(B * HV), ST_THREADS, ST_SMEM, stream>>>(
-      tW, tQ, tKd, tA, tO, U1, ef, s0, s_out, (int)L, (int)nch, (int)c0, (int)ncl,
-      status_word_ptr());
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(gdn_state_tc_kernel, dim3((unsigned)(B * HV)), dim3(ST_THREADS), ST_SMEM, stream,
+       tW, tQ, tKd, tA, tO, U1, ef, s0, s_out, (int)L, (int)nch, (int)c0, (int)ncl,
+       status_word_ptr()));
   return CLEF_OK;
 }
 

@@ -18,6 +18,8 @@ constexpr int H = 4096;
 __global__ void __launch_bounds__(256) image_rows_kernel(const __half* __restrict__ rows,
                                                          float* __restrict__ x, int64_t L,
                                                          int64_t start, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t r = blockIdx.x, b = r / n, k = r % n;
   const int c0 = threadIdx.x * 16;
   const uint4* src = reinterpret_cast<const uint4*>(rows + r * H + c0);
@@ -37,6 +39,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
                                                     const __half* __restrict__ table,
                                                     int64_t vocab, float* __restrict__ x,
                                                     unsigned* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t tok = blockIdx.x;
   const int32_t id = ids[tok];
   const bool ok = id >= 0 && (int64_t)id < vocab;
@@ -67,6 +71,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const __half* __restrict__ w,
                                                       __half* __restrict__ y, unsigned* status,
                                                       unsigned long long* bad_row) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[8];
   const int64_t tok = blockIdx.x;
   const int c0 = threadIdx.x * 16;
@@ -172,6 +178,8 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
                                                       float* __restrict__ g,
                                                       float* __restrict__ beta,
                                                       float* __restrict__ part, int64_t M) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t ab_smem[];
   AbSmem& s = *reinterpret_cast<AbSmem*>(ab_smem);
   const int64_t t0 = (int64_t)blockIdx.x * AB_T;
@@ -239,6 +247,8 @@ __global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__
 __global__ void ab_gates_kernel(const float* __restrict__ part, int slices,
                                 const __half* __restrict__ A_log, const __half* __restrict__ dt_bias,
                                 float* __restrict__ g, float* __restrict__ beta, int64_t M) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= M * 64) return;
   float v = 0.f;
@@ -252,8 +262,8 @@ clef_status embed_launch(const int32_t* ids, const __half* table, int64_t vocab,
                          int64_t M, cudaStream_t stream) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "embed", 0.0, M * (4096.0 * 2 + 4096.0 * 4));
-  glue::embed_kernel<<<(unsigned)M, 256, 0, stream>>>(ids, table, vocab, x, status_word_ptr());
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(glue::embed_kernel, dim3((unsigned)M), dim3(256), 0, stream,
+       ids, table, vocab, x, status_word_ptr()));
   return CLEF_OK;
 }
 
@@ -261,8 +271,8 @@ clef_status image_rows_launch(const __half* rows, float* x, int64_t B, int64_t L
                               int64_t n, cudaStream_t stream) {
   if (B == 0 || n == 0) return CLEF_OK;
   TraceScope ts(stream, "image_rows", 0.0, B * n * (4096.0 * 2 + 4096.0 * 4));
-  glue::image_rows_kernel<<<(unsigned)(B * n), 256, 0, stream>>>(rows, x, L, start, n);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(glue::image_rows_kernel, dim3((unsigned)(B * n)), dim3(256), 0, stream,
+       rows, x, L, start, n));
   return CLEF_OK;
 }
 
@@ -270,10 +280,9 @@ clef_status rmsnorm_launch(const float* x, const __half* w, __half* y, int64_t M
                            cudaStream_t stream, bool check_finite) {
   if (M == 0) return CLEF_OK;
   TraceScope ts(stream, "rmsnorm", 0.0, M * (4096.0 * 4 + 4096.0 * 2));
-  glue::rmsnorm_kernel<<<(unsigned)M, 256, 0, stream>>>(
-      x, w, y, check_finite ? status_word_ptr() : nullptr,
-      check_finite ? bad_row_word_ptr() : nullptr);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(glue::rmsnorm_kernel, dim3((unsigned)M), dim3(256), 0, stream,
+       x, w, y, check_finite ? status_word_ptr() : nullptr,
+       check_finite ? bad_row_word_ptr() : nullptr));
   return CLEF_OK;
 }
 
@@ -302,13 +311,12 @@ clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A
   TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
   static std::atomic<uint64_t> attr{0};
   CLEF_CUDA_CHECK(smem_opt_in((const void*)glue::ab_proj_kernel, sizeof(glue::AbSmem), &attr));
-  glue::ab_proj_kernel<<<dim3((unsigned)ctas, (unsigned)slices), 128, sizeof(glue::AbSmem), stream>>>(
-      xn, w_ab, A_log, dt_bias, g, beta, part, M);
-  CLEF_LAUNCH_CHECK();
+  CLEF_CUDA_CHECK(launch_pdl(glue::ab_proj_kernel, dim3(dim3((unsigned)ctas, (unsigned)slices)), dim3(128), sizeof(glue::AbSmem), stream,
+       xn, w_ab, A_log, dt_bias, g, beta, part, M));
   if (slices > 1) {
-    glue::ab_gates_kernel<<<(unsigned)((M * 64 + 255) / 256), 256, 0, stream>>>(part, slices, A_log,
-                                                                              dt_bias, g, beta, M);
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(glue::ab_gates_kernel, dim3((unsigned)((M * 64 + 255) / 256)), dim3(256), 0, stream,
+         part, slices, A_log,
+         dt_bias, g, beta, M));
   }
   return CLEF_OK;
 }

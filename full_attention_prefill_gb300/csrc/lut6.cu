@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
                      void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
                      int ksplit, unsigned* status) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // the barriers and tensor memory are set up; now the inputs
   const int first = blockIdx.x;
   const int stride = gridDim.x;
 
@@ -480,6 +482,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // same sequence of fp32 additions on every run); part is [parts][M][N].  Four columns per thread.
 __global__ void split_reduce_kernel(float* __restrict__ y, int64_t ldy, const float* __restrict__ part,
                                     int parts, int64_t M, int64_t N) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t quads = M * (N / 4);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < quads;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -597,18 +601,17 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
   {
     TraceScope ts(stream, "lut6_gemm", 2.0 * M * N * K,
                   0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
-    lut6_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-        tx, tp, lut, ordered ? static_cast<void*>(part_ws) : y, ordered ? N : ldy, (int)M, (int)N,
-        (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, status_word_ptr());
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(lut6_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream,
+         tx, tp, lut, ordered ? static_cast<void*>(part_ws) : y, ordered ? N : ldy, (int)M, (int)N,
+         (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, status_word_ptr()));
   }
   if (ordered) {
     TraceScope ts(stream, "split_reduce", 0.0, 4.0 * M * N * (2 + ksplit));
     const int64_t quads = M * (N / 4);
     const int64_t blocks = std::min<int64_t>((quads + 255) / 256, (int64_t)sms * 8);
-    split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(y), ldy, part_ws,
-                                                              ksplit, M, N);
-    CLEF_LAUNCH_CHECK();
+    CLEF_CUDA_CHECK(launch_pdl(split_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+         static_cast<float*>(y), ldy, part_ws,
+         ksplit, M, N));
   }
   return CLEF_OK;
 }
