@@ -459,7 +459,7 @@ def run_micro(args):
         p, l = torch.from_numpy(packed).to(dev), torch.from_numpy(lut).to(dev)
         y = torch.empty((M, N), dtype=torch.float16, device=dev)
         if args.canonical:
-            # the card's packing through clef_lut6_gemm_canonical (stream-K where it pays)
+            # the card's packing through clef_lut6_gemm_canonical (tiled into a workspace first)
             fn = lambda: clef.lut6_gemm(x, p, l, out=y)  # noqa: E731
         else:
             p = clef.lut6_tile(p, K)

@@ -49,7 +49,6 @@ constexpr int BT = 256;                       // tokens per tile: MMA N (B opera
 constexpr int BK = 64;                        // one step
 constexpr int XS = 5;                         // X ring stages
 constexpr int AS = 8;                         // packed-index ring = tensor-memory A ring stages
-constexpr int GROUP_M = 8;                    // token tiles walked together (L2 reuse)
 constexpr int X_BYTES = BT * BK * 2;          // 32 KB
 constexpr int P_BLOCK = 768;                  // packed bytes of one 16-row group per step
 constexpr int P_BYTES = (BN / 16) * P_BLOCK;  // 6 KB
@@ -149,13 +148,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // Tile t of the persistent walk -> (first output channel n0, first token m0).  Tiles go in
-// groups of GROUP_M token tiles: inside a group the token tile varies fastest, so the CTAs
-// running at one time share a few weight tiles and a few X tiles, which stay in L2.
-__device__ __forceinline__ void tile_coord(int t, int n_tiles, int m_tiles, int& n0, int& m0) {
-  const int per_group = GROUP_M * n_tiles;
+// groups of group_m token tiles: inside a group the token tile varies fastest, so the CTAs
+// running at one time share a few weight tiles and a few X tiles, which stay in L2.  The X rows
+// of a group stay in L2 while all channel tiles pass over them; the packed weights are read
+// again from DRAM for every group.
+__device__ __forceinline__ void tile_coord(int t, int n_tiles, int m_tiles, int group_m, int& n0,
+                                           int& m0) {
+  const int per_group = group_m * n_tiles;
   const int grp = t / per_group;
-  const int first_m = grp * GROUP_M;
-  const int gm = min(GROUP_M, m_tiles - first_m);
+  const int first_m = grp * group_m;
+  const int gm = min(group_m, m_tiles - first_m);
   const int local = t - grp * per_group;
   m0 = (first_m + local % gm) * BT;
   n0 = (local / gm) * BN;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     lut6_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_p, const __half* __restrict__ lut,
                      void* __restrict__ y, int64_t ldy, int M, int N, int K, int mode,
-                     int ksplit, unsigned* status) {
+                     int ksplit, int group_m, unsigned* status) {
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int u = first; u < num_units && ok; u += stride) {
         int n0, m0;
-        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        tile_coord(u % num_tiles, n_tiles, m_tiles, group_m, n0, m0);
         const int kb0 = (u / num_tiles) * nkb;
         for (int kb = kb0; kb < kb0 + nkb; ++kb, ++g) {
           // X slot g % XS was last read by step g - XS
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int u = first; u < num_units && ok; u += stride, ++it) {
         int n0, m0;
-        tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+        tile_coord(u % num_tiles, n_tiles, m_tiles, group_m, n0, m0);
         const int kb0 = (u / num_tiles) * nkb;
         const int ts = it & 1;
         if (it >= 2 && !mbar_wait(bar_tempty + 8 * ts, ((uint32_t)(it >> 1) & 1) ^ 1, status,
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int pn0 = -1, pm0 = 0, pkp = 0;  // tile (and k-part) whose epilogue is pending
     for (int u = first; u < num_units && ok; u += stride, ++it) {
       int n0, m0;
-      tile_coord(u % num_tiles, n_tiles, m_tiles, n0, m0);
+      tile_coord(u % num_tiles, n_tiles, m_tiles, group_m, n0, m0);
       const int ts = it & 1;
       if (!mbar_wait(bar_tfull + 8 * ts, (uint32_t)(it >> 1) & 1, status, DEV_TIMEOUT_DEQUANT)) {
         ok = false;
@@ -541,6 +543,21 @@ __global__ void lut6_tile_kernel(const uint8_t* __restrict__ packed, int64_t n, 
 
 }  // namespace lut
 
+int lut6_group_m(int64_t K, int mode) {
+  // As many token tiles per group as keep the group's X rows (256 tokens x K fp16 each) within
+  // a share of L2 that leaves room for the weight tiles and the output in flight: fewer groups
+  // mean fewer passes of the packed weights through DRAM.  Measured at 16,384 tokens: 16 tiles
+  // (32 MB of X) at K = 4096 cut a SwiGLU launch's DRAM reads from 736 to 474 MB, 32 tiles
+  // made X itself miss (2.3 GB); residual adds, whose fp32 read-modify-write of Y also passes
+  // through L2, keep 8 (16 read 17% more and ran 2% slower).
+  using namespace lut;
+  if (mode == EPI_ADD_F32 || mode == EPI_PART_F32) return 8;
+  constexpr int64_t kXBudget = 48ll << 20;
+  int g = 4;
+  while (g < 64 && 2 * g * BT * K * 2 <= kXBudget) g *= 2;
+  return g;
+}
+
 int lut6_add_split(int64_t M, int64_t N, int64_t K) {
   // When there are too few tiles to fill the GPU, pick the split that minimises the longest
   // CTA's work, counted in k-steps plus about four steps per unit for its epilogue.
@@ -603,7 +620,7 @@ clef_status lut6_gemm_launch(const __half* x, const uint8_t* tiled, const __half
                   0.75 * N * K + 8.0 * N + 2.0 * M * K + out_bytes);
     CLEF_CUDA_CHECK(launch_pdl(lut6_gemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream,
          tx, tp, lut, ordered ? static_cast<void*>(part_ws) : y, ordered ? N : ldy, (int)M, (int)N,
-         (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, status_word_ptr()));
+         (int)K, ordered ? (int)EPI_PART_F32 : mode, ksplit, lut6_group_m(K, mode), status_word_ptr()));
   }
   if (ordered) {
     TraceScope ts(stream, "split_reduce", 0.0, 4.0 * M * N * (2 + ksplit));
