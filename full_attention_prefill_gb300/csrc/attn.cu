@@ -239,12 +239,13 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
           ok = mbar_wait(bar_pf + 8 * s, (uint32_t)((j - 2) >> 1) & 1, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
+        // one descriptor per tile, the 16 slices by constant offsets of its start-address field
+        // (building each from the address costs the issuing thread more than an N = 64 MMA runs)
+        const uint64_t kd = sdesc_k_sw128(sb + OFF_K + sk * KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_k_sw128(sb + OFF_K + sk * KV_BYTES + (kk >> 2) * KV_BLOCK + (kk & 3) * 32);
-          tc_mma_f16_ts(tmem + S_COL + s * TBN, tmem + Q_COL + kk * 8, bd, idesc_s, kk != 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_f16_ts(tmem + S_COL + s * TBN, tmem + Q_COL + kk * 8,
+                        kd + (uint64_t)(((kk >> 2) * KV_BLOCK + (kk & 3) * 32) >> 4), idesc_s, kk != 0);
         tc_commit(bar_s + 8 * s);
         tc_commit(bar_ke + 8 * sk);
       }
@@ -263,11 +264,11 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
              mbar_wait(bar_vf + 8 * sv, (uint32_t)(j / VST) & 1, status, DEV_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
+        const uint64_t vd = sdesc_mn_sw128(sb + OFF_V + sv * KV_BYTES, KV_BLOCK, 1024);
 #pragma unroll
-        for (int kk = 0; kk < TBN / 16; ++kk) {
-          const uint64_t bd = sdesc_mn_sw128(sb + OFF_V + sv * KV_BYTES + kk * 16 * 128, KV_BLOCK, 1024);
-          tc_mma_f16_ts(tmem, tmem + S_COL + s * TBN + kk * 8, bd, idesc_o, (j | kk) != 0);
-        }
+        for (int kk = 0; kk < TBN / 16; ++kk)
+          tc_mma_f16_ts(tmem, tmem + S_COL + s * TBN + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4),
+                        idesc_o, (j | kk) != 0);
         tc_commit(bar_pf + 8 * s);
         tc_commit(bar_ve + 8 * sv);
       }
@@ -329,17 +330,16 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
         tmem_ld_32x32b_x32(tl + S_COL + s * TBN + half * 32, sv);
         tc_wait_ld();
         const int key0 = j * TBN + half * 32;
-        if (j * TBN + TBN - 1 <= p_first) {
+        if (j * TBN + TBN - 1 > p_first) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mt = fmaxf(mt, __uint_as_float(sv[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float v = (key0 + c <= qpos) ? __uint_as_float(sv[c]) : -INFINITY;
-            sv[c] = __float_as_uint(v);
-            mt = fmaxf(mt, v);
-          }
+          for (int c = 0; c < 32; ++c)
+            if (key0 + c > qpos) sv[c] = __float_as_uint(-INFINITY);
         }
+        // four independent max chains
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
+        mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       // row max over both halves (the previous exchange's reads are fenced off by that
       // exchange's second barrier)
@@ -376,15 +376,15 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
       // P = 2^(s sl2 - m_ref sl2): one FFMA and one exp2 per score
       const float moff = -m_ref * sl2;
       uint32_t pk[16];
-      float rs = 0.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sum chains
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float e0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sl2, moff));
         const float e1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, moff));
-        rs += e0 + e1;
+        rs[c & 3] += e0 + e1;
         pk[c] = pack_half2(e0, e1);
       }
-      lsum += rs;  // this half's share of the row sum
+      lsum += (rs[0] + rs[1]) + (rs[2] + rs[3]);  // this half's share of the row sum
       tmem_st_32x32b_x16(tl + S_COL + s * TBN + half * 16, pk);
       tc_wait_st();
       tc_fence_before();

@@ -181,8 +181,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
       for (int i = 0; i < ncl; ++i) {
         const int st = i & 1;
         const uint32_t ph = (uint32_t)i & 1;
-        const uint32_t pa = sb + OFF_A + st * A_BYTES;
-        const uint32_t pb = sb + OFF_B + st * B_BYTES;
+        // one descriptor per operand and chunk; the K slices are constant offsets of its
+        // address field, formed before the waits so that the MMAs issue as soon as they pass
+        const uint64_t ad = sdesc_k_sw128(sb + OFF_A + st * A_BYTES + A_WQ);
+        const uint64_t bd = sdesc_mn_sw128(sb + OFF_B + st * B_BYTES, BLK, 1024);
         // [U^T | O1^T] = S0h . [W ; Q]^T, once the previous chunk's O has been drained
         if (!mbar_wait(bar_fa + 8 * st, (i >> 1) & 1, status, DEV_TIMEOUT_MMA) ||
             !mbar_wait(bar_s0, ph, status, DEV_TIMEOUT_MMA) ||
@@ -192,8 +194,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           tc_mma_f16_ts(tmem + COL_UACC, tmem + COL_S0H + kk * 8,
-                        sdesc_k_sw128(pa + A_WQ + (kk >> 2) * 2 * BLK + (kk & 3) * 32), id_1,
-                        kk != 0);
+                        ad + (uint64_t)(((kk >> 2) * 2 * BLK + (kk & 3) * 32) >> 4), id_1, kk != 0);
         tc_commit(bar_u);
         tc_commit(bar_ea + 8 * st);   // W, Q no longer read (the row threads add theirs for U')
         any = true;
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1) gdn_state_tc_kernel(
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          tc_mma_f16_ts(tmem + COL_S, tmem + COL_UH + kk * 8,
-                        sdesc_mn_sw128(pb + kk * 16 * 128, BLK, 1024), id_2, 1);
+          tc_mma_f16_ts(tmem + COL_S, tmem + COL_UH + kk * 8, bd + (uint64_t)((kk * 16 * 128) >> 4),
+                        id_2, 1);
         tc_commit(bar_s);
         tc_commit(bar_eb + 8 * st);
       }

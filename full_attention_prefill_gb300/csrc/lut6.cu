@@ -314,17 +314,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         for (int kb = 0; kb < nkb; ++kb) {
+          // operands of this step, formed before the wait so that the MMAs issue as soon as it
+          // passes (the four K slices are constant offsets of the descriptor's address field)
+          const uint32_t a = tmem + A_COL + sa * 32;
+          const uint64_t bd = sdesc_k_sw128(sb + OFF_X + sx * X_BYTES);
           if (!mbar_wait(bar_ready + 8 * sa, ph, status, DEV_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = tmem + A_COL + sa * 32;
-          const uint32_t b = sb + OFF_X + sx * X_BYTES;
-          tc_mma_f16_ts(tmem, a, sdesc_k_sw128(b), idesc, kb != 0);
-          tc_mma_f16_ts(tmem, a + 8, sdesc_k_sw128(b + 32), idesc, 1);
-          tc_mma_f16_ts(tmem, a + 16, sdesc_k_sw128(b + 64), idesc, 1);
-          tc_mma_f16_ts(tmem, a + 24, sdesc_k_sw128(b + 96), idesc, 1);
+          tc_mma_f16_ts(tmem, a, bd, idesc, kb != 0);
+          tc_mma_f16_ts(tmem, a + 8, bd + 2, idesc, 1);
+          tc_mma_f16_ts(tmem, a + 16, bd + 4, idesc, 1);
+          tc_mma_f16_ts(tmem, a + 24, bd + 6, idesc, 1);
           tc_commit(bar_empty + 8 * sa);
           sx = sx + 1 == XS ? 0 : sx + 1;
           if (++sa == AS) {
