@@ -113,13 +113,18 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
 //            buffer, V an MN-major shared operand).  The two MMA chains have a thread each: a
 //            thread's mbarrier waits complete only after the MMAs it has committed.
 //   warps 4-11 first copy Q (rows of 256 dims, after rotary) from global memory into tensor
-//            memory; then softmax, two threads per row (warps w and w+4 share TMEM lanes
-//            32 (w % 4)..; warps 4-7 take keys 0..31 of a tile, warps 8-11 keys 32..63): read S,
-//            mask (diagonal tiles only), online max/sum in base 2 with the two halves' maxima
-//            combined through shared memory, write P (fp16) over the first 32 columns of its S
-//            buffer.  O is rescaled (in TMEM, each half of its columns by one of the two
-//            threads) only when a row's max grows by more than 2^8, so P stays below 256; the
-//            final O is divided by the row sum, multiplied by sigmoid(gate) and stored.
+//            memory; then softmax in two groups that take alternate tiles: warps 4-7 the even
+//            tiles (S buffer 0), warps 8-11 the odd ones (buffer 1), one thread per row and all
+//            64 keys of its tile (warps w and w+4 share TMEM lanes 32 (w % 4)..).  A thread reads
+//            S, masks (diagonal tiles only), takes the tile's max and then, in base 2, the
+//            online softmax step against a reference max that passes from group to group once
+//            per tile (shared memory and a named arrive / sync barrier, before either group's
+//            exponentials, so two tiles' exponentials run at once), and writes P (fp16) over
+//            the first 32 columns of its S buffer.  The reference, and with it O (in TMEM, by
+//            the row's thread), moves only when a row's max grows by more than 2^8, so P stays
+//            below 256; each group keeps its share of the row sum relative to the reference it
+//            last used.  The final O is divided by the combined row sum, multiplied by
+//            sigmoid(gate) and stored, each thread of a row taking half of its columns.
 // Tensor memory (512 columns): O [0,256), S/P buffers [256,320) and [320,384), Q [384,512).
 // ------------------------------------------------------------------------------------------
 constexpr int TBN = 64;                   // keys per tile
@@ -131,13 +136,22 @@ constexpr int OFF_V = OFF_K + KST * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
 constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_XCH = OFF_SLOT + 16;       // [2 halves][128 rows] fp32: row max / row sum
-constexpr int FLASH_SMEM = OFF_XCH + 2 * BM * 4 + 1024;
+constexpr int OFF_XCH = OFF_SLOT + 16;       // 6 x [128 rows] fp32: reference maxima, row sums
+constexpr int FLASH_SMEM = OFF_XCH + 6 * BM * 4 + 1024;
 static_assert(FLASH_SMEM <= 232448, "shared memory per CTA");
 constexpr int FLASH_THREADS = 384;
 constexpr uint32_t S_COL = 256;           // S/P buffers at TMEM columns 256 and 320
 constexpr uint32_t Q_COL = 384;           // Q (the S MMAs' A operand): 128 columns of fp16 pairs
 constexpr float kRescale = 8.0f;          // lazy rescale threshold (base-2 units)
+
+// 2^x by the hardware's approximate exp2 (PTX ex2.approx.ftz.f32, subnormal results flushed
+// to zero): P is rounded to fp16 right after, a far larger error than the approximation's.
+// 2^-inf = 0 for masked scores.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const __half* __restrict__ q, int64_t ldq, const __grid_constant__ CUtensorMap tk,
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s + 8 * i, 1);
-      mbar_init(bar_p + 8 * i, 8);
+      mbar_init(bar_p + 8 * i, 4);   // the 4 warps of the group that owns buffer i
       mbar_init(bar_pf + 8 * i, 1);
     }
     mbar_init(bar_fin, 1);
@@ -279,19 +293,26 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     }
   } else if (warp >= 4) {
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;                  // 0: keys 0..31 of a tile, 1: keys 32..63
+    const int grp = (warp - 4) >> 2;                   // 0: even tiles (S buffer 0), 1: odd tiles
     const int r = quarter * 32 + lane;                 // row of this thread
     const int pos = p0 + (r >> 2);
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem + OFF_XCH);  // [half][row]
+    float* xm = reinterpret_cast<float*>(smem + OFF_XCH);   // [row] reference max handed over
+    float* xl = xm + BM;                                     // [group][row] row sums
+    float* xr = xl + 2 * BM;                                 // [group][row] their references
+    float* xf = xr + 2 * BM;                                 // [row] reference after the last tile
     const float sl2 = 0.0625f * 1.4426950408889634f;  // 1/sqrt(256) in base 2
-    // the two warps of a lane quarter meet on named barrier 1 + quarter (64 threads)
+    // named barriers of the two warps on lane quarter q (64 threads): 1 + q both ways at the
+    // end; 5 + q carries the reference max from the even-tile group to the odd-tile group,
+    // 9 + q back
+    const int bar_send = (grp == 0 ? 5 : 9) + quarter;
+    const int bar_recv = (grp == 0 ? 9 : 5) + quarter;
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
     {
       // Q into tensor memory: row r, column Q_COL + c holds dims 2c, 2c+1 (the A-operand layout
-      // of kind::f16); this thread writes its row's dims 128 half .. 128 half + 127
+      // of kind::f16); this thread writes its row's dims 128 grp .. 128 grp + 127
       const bool valid = pos < L;
-      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + half * 128;
+      const __half* qrow = q + ((int64_t)tb + (valid ? pos : 0)) * ldq + (4 * g + (r & 3)) * D + grp * 128;
 #pragma unroll 1
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t qv[32];
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
           qv[4 * i + 2] = d.z;
           qv[4 * i + 3] = d.w;
         }
-        tmem_st_32x32b_x32(tl + Q_COL + half * 64 + c0, qv);
+        tmem_st_32x32b_x32(tl + Q_COL + grp * 64 + c0, qv);
       }
       tc_wait_st();
       tc_fence_before();
@@ -315,53 +336,66 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
     const int p_first = pos0 + p0;
     const int qpos = pos0 + pos;                        // this row's position in the request
     float m_ref = -INFINITY;   // reference max of the raw scores (P = 2^((s - m_ref) sl2))
+    float m_l = -INFINITY;     // the reference this group's row sum is relative to
     float lsum = 0.f;
-    // Both threads of a row pass the same named barriers every iteration, whatever happens: a
-    // failed (timed-out) wait only turns the rest of the work off (ok is warp-uniform).
+    // Both warps of a lane quarter pass the same named barriers whatever happens: a failed
+    // (timed-out) wait only turns the rest of the work off (ok is warp-uniform).
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
+    for (int j = grp; j < nt; j += 2) {
+      const int s = grp;                                // tile j's S/P buffer
       ok = ok && mbar_wait(bar_s + 8 * s, (uint32_t)(j >> 1) & 1, status, DEV_TIMEOUT_EPILOGUE);
       ok = __all_sync(0xffffffffu, ok);
-      uint32_t sv[32];
+      uint32_t sv0[32], sv1[32];                        // keys 0..31 and 32..63 of the tile
       float mt = -INFINITY;
       if (ok) {
         tc_fence_after();
-        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + half * 32, sv);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN, sv0);
+        tmem_ld_32x32b_x32(tl + S_COL + s * TBN + 32, sv1);
         tc_wait_ld();
-        const int key0 = j * TBN + half * 32;
-        if (j * TBN + TBN - 1 > p_first) {
+        const int key0 = j * TBN;
+        if (key0 + TBN - 1 > p_first) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (key0 + c > qpos) sv[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 32; ++c) {
+            if (key0 + c > qpos) sv0[c] = __float_as_uint(-INFINITY);
+            if (key0 + 32 + c > qpos) sv1[c] = __float_as_uint(-INFINITY);
+          }
         }
         // four independent max chains
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sv[c]));
+        for (int c = 0; c < 32; c += 2) {
+          m4[(c >> 1) & 1] = fmaxf(m4[(c >> 1) & 1], fmaxf(__uint_as_float(sv0[c]), __uint_as_float(sv0[c + 1])));
+          m4[2 + ((c >> 1) & 1)] = fmaxf(m4[2 + ((c >> 1) & 1)],
+                                        fmaxf(__uint_as_float(sv1[c]), __uint_as_float(sv1[c + 1])));
+        }
         mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
-      // row max over both halves (the previous exchange's reads are fenced off by that
-      // exchange's second barrier)
-      xch[half * BM + r] = mt;
-      pair_sync();
-      mt = fmaxf(mt, xch[(half ^ 1) * BM + r]);
-      pair_sync();
+      // the reference after tile j - 1, from the other group
+      if (j >= 1) {
+        asm volatile("bar.sync %0, 64;" ::"r"(bar_recv) : "memory");
+        m_ref = xm[r];
+      }
+      const float m_prev = m_ref;                       // the reference O is relative to
+      const float m_new = fmaxf(m_prev, mt);
+      const bool need = ok && (m_new - m_prev) * sl2 > kRescale;
+      if (need) m_ref = m_new;
+      // the other group's next tile may start its exponentials now
+      if (j + 1 < nt) {
+        xm[r] = m_ref;
+        asm volatile("bar.arrive %0, 64;" ::"r"(bar_send) : "memory");
+      }
       if (!ok) continue;
-      const float m_new = fmaxf(m_ref, mt);
-      const bool need = (m_new - m_ref) * sl2 > kRescale;   // the same in both threads of a row
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O may only be rescaled once P_{j-1} V_{j-1} has landed in it (P_{j+1} V_{j+1} cannot
-        // be done yet, so the parity test is unambiguous)
+        // O may only be rescaled once P_{j-1} V_{j-1} has landed in it (P_j V_j cannot have
+        // been issued yet, so the parity test is unambiguous)
         const int jp = j - 1;
         ok = __all_sync(0xffffffffu, mbar_wait(bar_pf + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1,
                                                status, DEV_TIMEOUT_EPILOGUE));
         if (!ok) continue;
         tc_fence_after();
-        // rescale this warp's half (128 columns) of its O rows
-        const float f = need ? exp2f((m_ref - m_new) * sl2) : 1.f;
+        const float f = need ? exp2f((m_prev - m_new) * sl2) : 1.f;
 #pragma unroll 1
-        for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ov[32];
           tmem_ld_32x32b_x32(tl + c0, ov);
           tc_wait_ld();
@@ -370,39 +404,54 @@ __global__ void __launch_bounds__(FLASH_THREADS, 1) flash_tc_kernel(
           tmem_st_32x32b_x32(tl + c0, ov);
         }
         tc_wait_st();
-        lsum *= f;
       }
-      if (need) m_ref = m_new;
+      // this group's row sum follows the reference
+      if (m_ref != m_l) {
+        if (lsum > 0.f) lsum *= exp2f((m_l - m_ref) * sl2);
+        m_l = m_ref;
+      }
       // P = 2^(s sl2 - m_ref sl2): one FFMA and one exp2 per score
       const float moff = -m_ref * sl2;
-      uint32_t pk[16];
+      uint32_t pk[32];
       float rs[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sum chains
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float e0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sl2, moff));
-        const float e1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, moff));
-        rs[c & 3] += e0 + e1;
+        const float e0 = ex2_fast(fmaf(__uint_as_float(sv0[2 * c]), sl2, moff));
+        const float e1 = ex2_fast(fmaf(__uint_as_float(sv0[2 * c + 1]), sl2, moff));
+        const float e2 = ex2_fast(fmaf(__uint_as_float(sv1[2 * c]), sl2, moff));
+        const float e3 = ex2_fast(fmaf(__uint_as_float(sv1[2 * c + 1]), sl2, moff));
+        rs[c & 1] += e0 + e1;
+        rs[2 + (c & 1)] += e2 + e3;
         pk[c] = pack_half2(e0, e1);
+        pk[16 + c] = pack_half2(e2, e3);
       }
-      lsum += (rs[0] + rs[1]) + (rs[2] + rs[3]);  // this half's share of the row sum
-      tmem_st_32x32b_x16(tl + S_COL + s * TBN + half * 16, pk);
+      lsum += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      tmem_st_32x32b_x32(tl + S_COL + s * TBN, pk);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p + 8 * s);
     }
-    // epilogue: wait for the last P V, then O / l * sigmoid(gate), each thread of a row taking
-    // half of its columns
-    xch[half * BM + r] = lsum;
+    // the two groups' row sums, each brought to the reference of the last tile (the one O is
+    // relative to); then O / l * sigmoid(gate), each thread of a row taking half of its columns
+    if (grp == ((nt - 1) & 1)) xf[r] = m_ref;
+    xl[grp * BM + r] = lsum;
+    xr[grp * BM + r] = m_l;
     pair_sync();
-    lsum += xch[(half ^ 1) * BM + r];
+    const float m_fin = xf[r];
+    float l = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float lh = xl[h * BM + r];
+      if (lh > 0.f) l += lh * exp2f((xr[h * BM + r] - m_fin) * sl2);
+    }
     if (ok && mbar_wait(bar_fin, 0, status, DEV_TIMEOUT_EPILOGUE)) {
       tc_fence_after();
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
       const int hq = 4 * g + (r & 3);
       const int64_t row = (int64_t)tb + pos;
 #pragma unroll 1
-      for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
+      for (int c0 = grp * (D / 2); c0 < (grp + 1) * (D / 2); c0 += 32) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(tl + c0, ov);
         tc_wait_ld();
