@@ -39,7 +39,7 @@ METRIC = "prefill tokens/s, 32-layer hybrid (L=512, L=16384); % of HBM/tensor ro
 # 16,384-position prefill: ncu dram__bytes_read.sum + dram__bytes_write.sum of each of the eight
 # launch shapes, captured in their decoder layers at 16,384 positions; no capture for the other
 # workloads.
-GEMM_DRAM_BYTES_PER_LAUNCH = {"l16384": 1077.6e6}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"l16384": 1016.8e6}
 
 WORKLOADS = {
     "l16384": dict(B=1, L=16384, desc="32-layer hybrid prefill, 1 request x 16384 positions"),

@@ -12,8 +12,12 @@ enum Epilogue : int {
   EPI_PART_F32 = 4,   // (internal) k-part p of a split residual add: part[p][m][n] fp32 = acc
 };
 
-// Token tiles per group of the GEMM's tile walk for a reduction length K and epilogue mode.
-int lut6_group_m(int64_t K, int mode);
+// Token tiles per group of the GEMM's tile walk for a reduction length K, epilogue mode and
+// tile width (256 or 512 tokens).
+int lut6_group_m(int64_t K, int mode, int tile_tokens);
+
+// Whether a launch of M tokens x N channels (no K split) takes the 512-token tiles.
+bool lut6_use_wide(int64_t M, int64_t N);
 
 // The number of k-parts a residual-add launch of this shape is split into (1: no split).
 int lut6_add_split(int64_t M, int64_t N, int64_t K);

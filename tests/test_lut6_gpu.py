@@ -30,7 +30,11 @@ def test_dequant_bit_exact(n, k):
 CASES = [(128, 4096, 4096), (77, 256, 128), (300, 784, 320), (1, 16, 64), (129, 512, 64 * 7),
          (1000, 1024, 1024), (4100, 1296, 128), (2600, 2048, 64 * 3),
          # the prefill's projection shapes at a short and a middle length
-         (512, 12288, 4096), (512, 4096, 12288), (4096, 4096, 4096)]
+         (512, 12288, 4096), (512, 4096, 12288), (4096, 4096, 4096),
+         # 384-token tiles (launches whose wide tiles fill the GPU): ragged m, a partial last
+         # channel tile with a 3-step k (the accumulators drained after 2 steps of the next
+         # tile), a 1-step k, and several tiles per CTA
+         (4100, 4608, 1024), (2600, 4624, 64 * 3), (3000, 6144, 64), (6000, 8192, 512)]
 
 
 @pytest.mark.parametrize("m,n,k", CASES)
@@ -69,9 +73,10 @@ def test_gemm_rejects_bad_shapes():
     assert e.value.code == 2
 
 
-def test_gemm_deterministic():
-    x = _dev(synth.normal_f16(3, "x", 0, (512, 1024)))
-    packed, lut = synth.lut6_weight(3, "w", 0, 1024, 1024)
+@pytest.mark.parametrize("m,n", [(512, 1024), (4096, 8192)])
+def test_gemm_deterministic(m, n):
+    x = _dev(synth.normal_f16(3, "x", 0, (m, 1024)))
+    packed, lut = synth.lut6_weight(3, "w", 0, n, 1024)
     p, l = _dev(packed), _dev(lut)
     a = clef.lut6_gemm(x, p, l)
     b = clef.lut6_gemm(x, p, l)
