@@ -8,7 +8,7 @@
 // query heads of a group, causal additive mask.
 //
 //   rope_kernel   rotates dims 0..63 of every q and k head (rotate-half pairs (j, j+32), angle
-//                 pos * 1e7^(-j/32), computed in fp64), in place or into a copy.  With a picture
+//                 pos * 1e7^(-j/32), formed and reduced to [-pi, pi] in fp64), in place or into a copy.  With a picture
 //                 block (M-RoPE, "Host contract" step 5: three planes, sections 11 / 11 / 10
 //                 interleaved, so pair j reads plane j mod 3), a picture token k at index s + k
 //                 has planes (s, s + k / W, s + k % W) and tokens after the block move back by
@@ -17,6 +17,7 @@
 //                 each K/V tile is read once for the group; tcgen05 MMAs with S and O in tensor
 //                 memory; online softmax over 64-key tiles; epilogue o * sigmoid(gate).
 #include <algorithm>
+#include <cmath>
 
 #include "attn.cuh"
 #include "common.cuh"
@@ -29,12 +30,17 @@ constexpr int HQ = 16, HKV = 4;
 constexpr int BM = 128;            // rows per CTA = 32 positions x 4 heads
 constexpr int POS = BM / 4;        // positions per CTA
 
+// The 32 rotary frequencies 1e7^(-j/32), computed once in fp64 on the host.
+struct RopeFreq {
+  double f[32];
+};
+
 __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qin, int64_t ldqi,
                                                    __half* __restrict__ qout, int64_t ldqo,
                                                    const __half* __restrict__ kin, int64_t ldki,
                                                    __half* __restrict__ kout, int64_t ldko, int L,
                                                    int pos0, int64_t kctx, int mstart, int mh,
-                                                   int mw) {
+                                                   int mw, const __grid_constant__ RopeFreq fr) {
   pdl_trigger();
   pdl_wait();
   __shared__ float cs[32], sn[32];
@@ -60,12 +66,19 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
     }
     const int plane = tid % 3;
     const int pos = plane == 0 ? pt : (plane == 1 ? ph : pw);
-    // angle = pos * theta^(-j/32), reduced and evaluated in fp64 (ln 1e7 = 16.118...)
-    const double inv_freq = exp(-(double)tid * (16.11809565095832 / 32.0));
-    double s, c;
-    sincos((double)pos * inv_freq, &s, &c);
-    cs[tid] = (float)c;
-    sn[tid] = (float)s;
+    // angle = pos * theta^(-j/32) formed in fp64 and reduced to [-pi, pi] there (Cody and
+    // Waite's two-constant reduction, with 2 pi as its nearest double plus the remainder, each
+    // k * constant taken exactly inside an fma), then sin and cos in fp32 of the reduced angle:
+    // a few fp64 operations per angle instead of an fp64 sin/cos (fp64 runs at a small fraction
+    // of the fp32 rate on this part)
+    const double a = (double)pos * fr.f[tid];
+    const double kq = rint(a * 0.15915494309189535);          // 1 / (2 pi)
+    double r = fma(-kq, 6.2831853071795860, a);                // 2 pi rounded to double
+    r = fma(-kq, 2.4492935982947064e-16, r);                   // 2 pi minus that
+    float s, c;
+    sincosf((float)r, &s, &c);
+    cs[tid] = c;
+    sn[tid] = s;
   }
   __syncthreads();
   const bool copy_q = qout != qin, copy_k = kout != kin;
@@ -509,11 +522,16 @@ clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t l
                         int64_t L, int64_t pos0, int64_t kctx, cudaStream_t stream,
                         const MRope& mr) {
   if (M == 0) return CLEF_OK;
+  static const attn::RopeFreq fr = [] {
+    attn::RopeFreq f;
+    for (int j = 0; j < 32; ++j) f.f[j] = std::exp(-(double)j * (std::log(1e7) / 32.0));
+    return f;
+  }();
   TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
   CLEF_CUDA_CHECK(launch_pdl(attn::rope_kernel, dim3((unsigned)M), dim3(128), 0, stream,
        qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
        (int)L, (int)pos0, kctx, (int)mr.start,
-       (int)mr.h, (int)mr.w));
+       (int)mr.h, (int)mr.w, fr));
   return CLEF_OK;
 }
 
