@@ -177,6 +177,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
   }
 }
+// The same bounded wait by polling (mbarrier.test_wait, which never suspends the thread): for a
+// thread whose every microsecond idle shows up as idle tensor cycles (the tensor pipe queues
+// only about two MMAs ahead of it); measured 0.4% faster than mbar_wait for the 384-token GEMM's
+// MMA thread.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, unsigned* status,
+                                               unsigned code) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((i & 255) == 255 && globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, code);
+      return false;
+    }
+  }
+}
 
 // ---- proxy fences ----
 __device__ __forceinline__ void fence_proxy_async_smem() {

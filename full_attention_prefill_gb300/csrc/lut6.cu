@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // passes
           const uint32_t a = tmem + W_A_COL + s * 32;
           const uint64_t xd = sdesc_k_sw128(sb + W_OFF_X + s * W_X_BYTES);
-          if (!mbar_wait(bar_ready + 8 * s, ph, status, DEV_TIMEOUT_MMA)) {
+          if (!mbar_wait_spin(bar_ready + 8 * s, ph, status, DEV_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
