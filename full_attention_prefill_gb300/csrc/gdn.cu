@@ -38,111 +38,145 @@ constexpr float kLogAlphaMin = -30.0f;
 
 // ------------------------------------------------------------------------------------------
 // Prep for the decoder layer: causal depthwise conv (4 taps) + SiLU over the 8192 QKV channels and
-// the per-head L2 norm of q and k.  A CTA (256 threads) takes a tile of PREP_T tokens x 512
-// channels: all PREP_T + 3 rows (the conv's history included) are copied into shared memory at
-// once with cp.async, so three CTAs per SM keep ~200 KB of loads in flight; then thread (token
-// half, 4 channels) walks its PREP_T / 2 tokens with the 3-row history in registers.  A warp
+// the per-head L2 norm of q and k.  Persistent: three CTAs (256 threads) per SM walk tiles of
+// PREP_T tokens x 512 channels (tile t: channel block t mod 16, token block t / 16).  A tile's
+// PREP_T + 3 rows (the conv's history included) are copied into shared memory with cp.async,
+// double-buffered so that the next tile's copies are in flight while this one is computed; then
+// thread (token half, 4 channels) walks its PREP_T / 2 tokens with the 3-row history in
+// registers, fully unrolled when none of them lies within 3 positions of a request start.  A warp
 // covers 128 channels, exactly one q or k head, so the norm is a warp reduction.  The gates
-// come from the a/b projection's epilogue.
+// come from the a/b projection's epilogue.  Token indices are 32-bit (the entry points refuse
+// more than 2^22 tokens).
 // proj [M, ldp] fp16: q 0..2047 | k 2048..4095 | v 4096..8191 (| z 8192..).
 // ------------------------------------------------------------------------------------------
-constexpr int PREP_T = 64;
+constexpr int PREP_T = 32;
 constexpr int PREP_CH = 512;
-constexpr int PREP_SMEM = (PREP_T + 3) * PREP_CH * 2;
-__global__ void __launch_bounds__(256) gdn_prep_kernel(
-    const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
-    const __half* __restrict__ conv_in, __half* __restrict__ q, __half* __restrict__ k,
-    __half* __restrict__ v, int64_t M, int L) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ __align__(16) uint8_t prep_smem[];
-  __half* tile = reinterpret_cast<__half*>(prep_smem);   // [PREP_T + 3][PREP_CH], row i = token tok0 - 3 + i
-  const int tid = threadIdx.x;
-  const int cbase = blockIdx.x * PREP_CH;
-  const int64_t tok0 = (int64_t)blockIdx.y * PREP_T;
-  // rows outside [0, M) are zero-filled
-  for (int i = tid; i < (PREP_T + 3) * (PREP_CH / 8); i += 256) {
-    const int r = i / (PREP_CH / 8), c8 = (i % (PREP_CH / 8)) * 8;
-    const int64_t t = tok0 - 3 + r;
-    const bool ok = t >= 0 && t < M;
-    cp_async16(smem_u32(tile + r * PREP_CH + c8), proj + (ok ? t : 0) * ldp + cbase + c8, ok);
+constexpr int PREP_ROWS = PREP_T + 3;
+constexpr int PREP_BUF = PREP_ROWS * PREP_CH * 2;
+constexpr int PREP_SMEM = 2 * PREP_BUF;
+constexpr int PREP_CTAS_PER_SM = 3;
+// x * sigmoid(x) and 1 / sqrt(x) by the hardware's approximate exp2, reciprocal and reciprocal
+// square root with subnormals flushed (PTX ex2.approx.ftz.f32, rcp.approx.ftz.f32,
+// rsqrt.approx.ftz.f32): one instruction each, where the non-flushing forms add range handling.
+// Large negative x: 2^(-x log2 e) overflows to +inf and the reciprocal to 0, so the result is -0.
+__device__ __forceinline__ float silu_ftz(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return x * r;
+}
+__device__ __forceinline__ float rsqrt_ftz(float x) {
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// The 4 channels of a tile row as floats.
+__device__ __forceinline__ void prep_row(const __half* p, float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+// One output token from its four taps (oldest first): conv, SiLU, and for q and k the head's L2
+// norm (the warp's 32 lanes hold its 128 channels).
+template <bool QK>
+__device__ __forceinline__ void prep_token(const float (&w)[4][4], const float (&x0)[4],
+                                           const float (&x1)[4], const float (&x2)[4],
+                                           const float (&x3)[4], __half* out) {
+  float y[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    y[c] = silu_ftz(w[c][0] * x0[c] + w[c][1] * x1[c] + w[c][2] * x2[c] + w[c][3] * x3[c]);
+  if (QK) {
+    float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float r = rsqrt_ftz(ss + 1e-6f);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[c] *= r;
   }
-  cp_async_commit();
-  const int cl = (tid & 127) * 4;           // this thread's 4 channels within the tile
-  const int ch0 = cbase + cl;
-  const int th = tid >> 7;                  // token half
-  float w[4][4];                            // [channel][tap]
-  {
-    const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (int64_t)ch0 * 4);
+  *reinterpret_cast<uint2*>(out) = make_uint2(h2u(y[0], y[1]), h2u(y[2], y[3]));
+}
+// PREP_T / 2 consecutive tokens of one request whose taps all lie in the tile (rows j0 .. j0 +
+// PREP_T / 2 + 2 at `row0`); q and k rows are 2048 apart, v rows 4096, so the stores take
+// constant offsets from `out`.
+template <bool QK>
+__device__ __forceinline__ void prep_run(const __half* row0, const float (&w)[4][4], __half* out) {
+  constexpr int LDD = QK ? 2048 : 4096;
+  float h0[4], h1[4], h2[4];
+  prep_row(row0, h0);
+  prep_row(row0 + PREP_CH, h1);
+  prep_row(row0 + 2 * PREP_CH, h2);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 u = __ldg(wp + i);
-      const __half* hh = reinterpret_cast<const __half*>(&u);
+  for (int j = 0; j < PREP_T / 2; ++j) {
+    float x3[4];
+    prep_row(row0 + (j + 3) * PREP_CH, x3);
+    prep_token<QK>(w, h0, h1, h2, x3, out + j * LDD);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[(i * 8 + j) / 4][(i * 8 + j) % 4] = __half2float(hh[j]);
+    for (int c = 0; c < 4; ++c) {
+      h0[c] = h1[c];
+      h1[c] = h2[c];
+      h2[c] = x3[c];
     }
   }
-  const bool is_qk = ch0 < 4096;
-  __half* dst0 = ch0 < 2048 ? q + ch0 : (ch0 < 4096 ? k + (ch0 - 2048) : v + (ch0 - 4096));
-  const int64_t ldd = ch0 < 4096 ? 2048 : 4096;
-  const int j0 = th * (PREP_T / 2);         // first token of this thread, within the tile
-  int pos = (int)((tok0 + j0) % L);         // its position in its request
-  int64_t req = (tok0 + j0) / L;            // and the request
-  cp_async_wait<0>();
-  __syncthreads();
-  // the 4 channels of tile row r as floats
-  auto rd = [&](int r, float (&x)[4]) {
-    const uint2 u = *reinterpret_cast<const uint2*>(tile + r * PREP_CH + cl);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// The conv taps of channels ch0 .. ch0 + 3 as floats, [channel][tap].
+__device__ __forceinline__ void prep_weights(const __half* conv_w, int ch0, float (&w)[4][4]) {
+  const uint4* wp = reinterpret_cast<const uint4*>(conv_w + (int64_t)ch0 * 4);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = __ldg(wp + i);
+    const __half* hh = reinterpret_cast<const __half*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[(i * 8 + j) / 4][(i * 8 + j) % 4] = __half2float(hh[j]);
+  }
+}
+
+// Tokens of a thread's run that lie within 3 positions of a request start (their earlier taps
+// read the carried conv input, or zero) or past M: one token at a time.
+__device__ __noinline__ void prep_edge(const __half* row0, const __half* conv_w, bool is_qk,
+                                       __half* dst, int64_t ldd, const __half* conv_in, int ch0,
+                                       int tok_a, int pos, int64_t M, int L) {
+  float w[4][4];
+  prep_weights(conv_w, ch0, w);
+  int req = tok_a / L;
+  auto emit = [&](int tok, const float (&x0)[4], const float (&x1)[4], const float (&x2)[4],
+                  const float (&x3)[4]) {
+    if (is_qk)
+      prep_token<true>(w, x0, x1, x2, x3, dst + (int64_t)tok * ldd);
+    else
+      prep_token<false>(w, x0, x1, x2, x3, dst + (int64_t)tok * ldd);
   };
-  float h0[4], h1[4], h2[4];                // tokens t-3, t-2, t-1
-  rd(j0, h0);
-  rd(j0 + 1, h1);
-  rd(j0 + 2, h2);
-#pragma unroll 4
-  for (int j = j0; j < j0 + PREP_T / 2; ++j) {
-    const int64_t tok = tok0 + j;
+  float h0[4], h1[4], h2[4];            // tokens t-3, t-2, t-1
+  prep_row(row0, h0);
+  prep_row(row0 + PREP_CH, h1);
+  prep_row(row0 + 2 * PREP_CH, h2);
+#pragma unroll 1
+  for (int j = 0; j < PREP_T / 2 && tok_a + j < M; ++j) {
     float x3[4];
-    rd(j + 3, x3);
-    if (tok < M) {
-      float y[4];
-      if (pos >= 3) {                         // the same for the whole warp (one token)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          y[c] = silu_f(w[c][0] * h0[c] + w[c][1] * h1[c] + w[c][2] * h2[c] + w[c][3] * x3[c]);
-      } else {
-        // taps reaching before the request's start read the carried conv input (its last three
-        // rows, oldest first), or zero without one
-        float x0[4], x1[4], x2[4];
-        auto hist = [&](int r, float (&x)[4]) {   // carried row r = 0..2
-          if (conv_in) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(conv_in + (req * 3 + r) * 8192 + ch0));
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-            const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-            x[0] = a.x; x[1] = a.y; x[2] = bb.x; x[3] = bb.y;
-          } else {
-            x[0] = x[1] = x[2] = x[3] = 0.f;
-          }
-        };
-        // tap j reads position pos - 3 + j, i.e. carried row pos + j when that is negative
-        if (pos >= 3) { for (int c = 0; c < 4; ++c) x0[c] = h0[c]; } else hist(pos, x0);
-        if (pos >= 2) { for (int c = 0; c < 4; ++c) x1[c] = h1[c]; } else hist(pos + 1, x1);
-        if (pos >= 1) { for (int c = 0; c < 4; ++c) x2[c] = h2[c]; } else hist(pos + 2, x2);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          y[c] = silu_f(w[c][0] * x0[c] + w[c][1] * x1[c] + w[c][2] * x2[c] + w[c][3] * x3[c]);
-      }
-      if (is_qk) {
-        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float r = rsqrtf(ss + 1e-6f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) y[c] *= r;
-      }
-      *reinterpret_cast<uint2*>(dst0 + tok * ldd) = make_uint2(h2u(y[0], y[1]), h2u(y[2], y[3]));
+    prep_row(row0 + (j + 3) * PREP_CH, x3);
+    if (pos >= 3) {
+      emit(tok_a + j, h0, h1, h2, x3);
+    } else {
+      // taps reaching before the request's start read the carried conv input (its last
+      // three rows, oldest first), or zero without one
+      auto hist = [&](int r, float (&x)[4]) {   // carried row r = 0..2
+        if (conv_in) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(conv_in + ((int64_t)req * 3 + r) * 8192 + ch0));
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+          const float2 bb = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+          x[0] = a.x; x[1] = a.y; x[2] = bb.x; x[3] = bb.y;
+        } else {
+          x[0] = x[1] = x[2] = x[3] = 0.f;
+        }
+      };
+      // tap j reads position pos - 3 + j, i.e. carried row pos + j when that is negative
+      float x0[4], x1[4], x2[4];
+      if (pos >= 3) { for (int c = 0; c < 4; ++c) x0[c] = h0[c]; } else hist(pos, x0);
+      if (pos >= 2) { for (int c = 0; c < 4; ++c) x1[c] = h1[c]; } else hist(pos + 1, x1);
+      if (pos >= 1) { for (int c = 0; c < 4; ++c) x2[c] = h2[c]; } else hist(pos + 2, x2);
+      emit(tok_a + j, x0, x1, x2, x3);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -154,6 +188,69 @@ __global__ void __launch_bounds__(256) gdn_prep_kernel(
       pos = 0;
       ++req;
     }
+  }
+}
+
+__global__ void __launch_bounds__(256, PREP_CTAS_PER_SM) gdn_prep_kernel(
+    const __half* __restrict__ proj, int64_t ldp, const __half* __restrict__ conv_w,
+    const __half* __restrict__ conv_in, __half* __restrict__ q, __half* __restrict__ k,
+    __half* __restrict__ v, int64_t M, int L, int64_t n_tiles) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) uint8_t prep_smem[];
+  const int tid = threadIdx.x;
+  // copies of tile t into buffer b (row i = token tok0 - 3 + i; rows outside [0, M) zero-filled)
+  // (thread tid copies 16 bytes at column (tid mod 64) * 8 of rows tid / 64, + 4, + 8, ...)
+  auto load = [&](int64_t t, int b) {
+    const int c8 = (tid % (PREP_CH / 8)) * 8;
+    const int r0 = tid / (PREP_CH / 8);
+    const int tok0 = (int)(t / (8192 / PREP_CH)) * PREP_T;
+    const __half* src = proj + (int)(t % (8192 / PREP_CH)) * PREP_CH + c8;
+    const uint32_t dst = smem_u32(prep_smem + b * PREP_BUF) + (uint32_t)(tid * 16);
+    if (tok0 >= 3 && tok0 + PREP_T <= M) {
+      const __half* p = src + (int64_t)(tok0 - 3 + r0) * ldp;
+#pragma unroll
+      for (int m = 0; m < PREP_ROWS / 4; ++m, p += 4 * ldp) cp_async16(dst + m * 4096, p, true);
+      if (r0 + 4 * (PREP_ROWS / 4) < PREP_ROWS) cp_async16(dst + (PREP_ROWS / 4) * 4096, p, true);
+    } else {
+#pragma unroll 1
+      for (int r = r0; r < PREP_ROWS; r += 4) {
+        const int tk = tok0 - 3 + r;
+        const bool ok = tk >= 0 && tk < M;
+        cp_async16(dst + (r - r0) * 1024, src + (int64_t)(ok ? tk : 0) * ldp, ok);
+      }
+    }
+  };
+  const int cl = (tid & 127) * 4;           // this thread's 4 channels within the tile
+  const int j0 = (tid >> 7) * (PREP_T / 2); // its first token within the tile
+  int64_t t = blockIdx.x;
+  if (t < n_tiles) load(t, 0);
+  cp_async_commit();
+  for (int n = 0; t < n_tiles; ++n, t += gridDim.x) {
+    if (t + gridDim.x < n_tiles) load(t + gridDim.x, (n + 1) & 1);
+    cp_async_commit();
+    const int ch0 = (int)(t % (8192 / PREP_CH)) * PREP_CH + cl;
+    const int tok_a = (int)(t / (8192 / PREP_CH)) * PREP_T + j0;   // this thread's first token
+    float w[4][4];                          // [channel][tap]
+    prep_weights(conv_w, ch0, w);
+    const bool is_qk = ch0 < 4096;
+    __half* dst = (ch0 < 2048 ? q + ch0 : (ch0 < 4096 ? k + (ch0 - 2048) : v + (ch0 - 4096)));
+    const int64_t ldd = ch0 < 4096 ? 2048 : 4096;
+    const __half* tile = reinterpret_cast<const __half*>(prep_smem + (n & 1) * PREP_BUF) + cl;
+    cp_async_wait<1>();
+    __syncthreads();
+    int pos = tok_a % L;                    // position of the first token in its request
+    if (pos >= 3 && pos + PREP_T / 2 <= L && tok_a + PREP_T / 2 <= M) {
+      // the same for the whole warp (one token half): every tap lies in this request and the tile
+      __half* out = dst + (int64_t)tok_a * ldd;
+      if (is_qk)
+        prep_run<true>(tile + j0 * PREP_CH, w, out);
+      else
+        prep_run<false>(tile + j0 * PREP_CH, w, out);
+    } else {
+      prep_edge(tile + j0 * PREP_CH, conv_w, is_qk, dst, ldd, conv_in, ch0, tok_a, pos, M, L);
+    }
+    __syncthreads();                        // buffer n & 1 is refilled by the next iteration
   }
 }
 
@@ -600,10 +697,11 @@ clef_status gdn_prep_launch(const __half* proj, int64_t ldp, const __half* conv_
   TraceScope ts(stream, "gdn_prep", 0.0, M * (8192.0 * 2 + 8192 * 2));
   static std::atomic<uint64_t> attr{0};
   CLEF_CUDA_CHECK(smem_opt_in((const void*)gdn::gdn_prep_kernel, gdn::PREP_SMEM, &attr));
-  dim3 grid(8192 / gdn::PREP_CH, (unsigned)((M + gdn::PREP_T - 1) / gdn::PREP_T));
-  CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_prep_kernel, dim3(grid), dim3(256), gdn::PREP_SMEM, stream,
+  const int64_t n_tiles = (8192 / gdn::PREP_CH) * ((M + gdn::PREP_T - 1) / gdn::PREP_T);
+  const int64_t grid = std::min<int64_t>(n_tiles, (int64_t)gdn::PREP_CTAS_PER_SM * num_sms());
+  CLEF_CUDA_CHECK(launch_pdl(gdn::gdn_prep_kernel, dim3((unsigned)grid), dim3(256), gdn::PREP_SMEM, stream,
        proj, ldp, conv_w, conv_in, q, k, v,
-       M, (int)L));
+       M, (int)L, n_tiles));
   return CLEF_OK;
 }
 

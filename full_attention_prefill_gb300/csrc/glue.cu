@@ -148,98 +148,154 @@ __global__ void check_finite_kernel(const __half* __restrict__ x, int64_t rows, 
   }
 }
 
-// ab = xn . W_ab^T: 64 tokens x 64 outputs per CTA, k streamed in blocks of 64 through a ring of
-// AB_ST cp.async stages (three blocks in flight while one is multiplied), warp w owns tokens
-// 16w..16w+15.
-constexpr int AB_T = 64, AB_K = 64, AB_LD = AB_K + 8, AB_ST = 4;
-struct AbSmem {
-  __half X[AB_ST][AB_T][AB_LD];
-  __half W[AB_ST][64][AB_LD];
-};
+// ab = xn . W_ab^T on the tensor cores: a CTA (128 threads) takes 128 tokens x the 64 outputs
+// over its share of the 64 k blocks.  Both operands stream by TMA (128-byte swizzle, K-major)
+// through a ring of AB_ST stages (X box 128 tokens x 64 k, W box 64 outputs x 64 k): one thread of
+// warp 0 loads, one thread of warp 1 issues four MMAs per block (kind::f16, M = 128 tokens, N = 64
+// outputs, K = 16, both operands from shared memory) into a 64-column fp32 accumulator and frees
+// the stage with one commit.  Then warp w reads tensor-memory lanes 32w..32w+31 (one token per
+// thread, its 64 sums) and writes that token's gates, or with a K split its partial sums.
+constexpr int AB_T = 128, AB_K = 64, AB_ST = 6;
+constexpr int AB_X_BYTES = AB_T * AB_K * 2;           // 16 KB
+constexpr int AB_W_BYTES = 64 * AB_K * 2;             // 8 KB
+constexpr int AB_STAGE = AB_X_BYTES + AB_W_BYTES;
+constexpr int AB_OFF_BAR = AB_ST * AB_STAGE;
+constexpr int AB_NUM_BARS = 2 * AB_ST + 1;
+constexpr int AB_SMEM = AB_OFF_BAR + 8 * AB_NUM_BARS + 8 + 1024;   // + tensor-memory slot, alignment
+static_assert(AB_STAGE % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle atoms");
 
 // Gates from the summed projections: g = -exp(A_log) softplus(a + dt_bias) (>= -30), beta = sigmoid(b).
+__device__ __forceinline__ float gate_g(float v, int col, const __half* A_log, const __half* dt_bias) {
+  const float a = v + __half2float(dt_bias[col]);
+  const float sp = a > 20.f ? a : log1pf(__expf(a));
+  return fmaxf(-__expf(__half2float(A_log[col])) * sp, -30.f);
+}
 __device__ __forceinline__ void write_gate(int64_t tok, int col, float v, const __half* A_log,
                                            const __half* dt_bias, float* g, float* beta) {
-  if (col < 32) {
-    const float a = v + __half2float(dt_bias[col]);
-    const float sp = a > 20.f ? a : log1pf(__expf(a));
-    g[tok * 32 + col] = fmaxf(-__expf(__half2float(A_log[col])) * sp, -30.f);
-  } else {
+  if (col < 32)
+    g[tok * 32 + col] = gate_g(v, col, A_log, dt_bias);
+  else
     beta[tok * 32 + col - 32] = sigmoid_f(v);
-  }
 }
 
-// blockIdx.y = slice of K (gridDim.y slices).  With one slice the epilogue computes the gates;
-// otherwise it writes its partial sums to part [slice][M][64] for ab_gates_kernel.
-__global__ void __launch_bounds__(128) ab_proj_kernel(const __half* __restrict__ xn,
-                                                      const __half* __restrict__ wab,
-                                                      const __half* __restrict__ A_log,
-                                                      const __half* __restrict__ dt_bias,
-                                                      float* __restrict__ g,
-                                                      float* __restrict__ beta,
-                                                      float* __restrict__ part, int64_t M) {
+// blockIdx.y = slice of K (gridDim.y slices, at most 64).  With one slice the epilogue computes
+// the gates; otherwise it writes its partial sums to part [slice][M][64] for ab_gates_kernel.
+__global__ void __launch_bounds__(128, 1) ab_proj_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                         const __grid_constant__ CUtensorMap tmap_w,
+                                                         const __half* __restrict__ A_log,
+                                                         const __half* __restrict__ dt_bias,
+                                                         float* __restrict__ g,
+                                                         float* __restrict__ beta,
+                                                         float* __restrict__ part, int64_t M,
+                                                         unsigned* status) {
   pdl_trigger();
-  pdl_wait();
-  extern __shared__ __align__(16) uint8_t ab_smem[];
-  AbSmem& s = *reinterpret_cast<AbSmem*>(ab_smem);
+  extern __shared__ uint8_t ab_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ab_smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = (int64_t)blockIdx.x * AB_T;
   const int nkb_all = H / AB_K;
   const int kb0 = blockIdx.y * nkb_all / gridDim.y;
-  const int kb1 = (blockIdx.y + 1) * nkb_all / gridDim.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  auto load = [&](int buf, int kb) {
-    for (int i = tid; i < AB_T * (AB_K / 8); i += 128) {
-      const int r = i / (AB_K / 8), c8 = (i % (AB_K / 8)) * 8;
-      const bool ok = t0 + r < M;
-      cp_async16(smem_u32(&s.X[buf][r][c8]), xn + (ok ? t0 + r : 0) * H + kb * AB_K + c8, ok);
-      cp_async16(smem_u32(&s.W[buf][r][c8]), wab + (int64_t)r * H + kb * AB_K + c8, true);
+  const int nkb = (blockIdx.y + 1) * nkb_all / gridDim.y - kb0;
+  const uint32_t bar_full = sb + AB_OFF_BAR;           // [AB_ST] stage landed (TMA bytes)
+  const uint32_t bar_empty = bar_full + 8 * AB_ST;     // [AB_ST] stage read by its MMAs
+  const uint32_t bar_done = bar_empty + 8 * AB_ST;     // every MMA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AB_OFF_BAR + 8 * AB_NUM_BARS);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < AB_ST; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
     }
-    cp_async_commit();
-  };
-  float acc[8][4];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  for (int i = 0; i < AB_ST - 1; ++i) {
-    if (kb0 + i < kb1) load(i, kb0 + i); else cp_async_commit();
+    mbar_init(bar_done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_w);
   }
-  for (int kb = kb0; kb < kb1; ++kb) {
-    const int buf = (kb - kb0) % AB_ST;
-    cp_async_wait<AB_ST - 2>();   // block kb has landed
-    __syncthreads();              // ... for every thread, and the slot of kb - 1 is free again
-    const int nxt = kb + AB_ST - 1;
-    if (nxt < kb1) load((nxt - kb0) % AB_ST, nxt); else cp_async_commit();
-    const uint32_t sX = smem_u32(&s.X[buf][0][0]), sW = smem_u32(&s.W[buf][0][0]);
-#pragma unroll
-    for (int ks = 0; ks < AB_K / 16; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(a, a_addr(sX, AB_LD, warp * 16, ks * 16, lane));
-#pragma unroll
-      for (int n = 0; n < 8; n += 2) {
-        uint32_t bq[4];
-        ldsm_x4(bq, bn_addr(sW, AB_LD, n * 8, ks * 16, lane));
-        mma16816(acc[n], a, bq[0], bq[1]);
-        mma16816(acc[n + 1], a, bq[2], bq[3]);
-      }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // the barriers and tensor memory are set up; now the inputs
+
+  if (warp == 0 && lane == 0) {
+    int i = 0;
+    for (; i < nkb; ++i) {
+      const int s = i % AB_ST;
+      // stage s was last read by the MMAs of block i - AB_ST
+      if (i >= AB_ST && !mbar_wait(bar_empty + 8 * s, (uint32_t)(i / AB_ST - 1) & 1, status,
+                                   DEV_TIMEOUT_TMA))
+        break;
+      const uint32_t fb = bar_full + 8 * s;
+      mbar_arrive_expect_tx(fb, AB_STAGE);
+      tma_load_2d(sb + s * AB_STAGE, &tmap_x, fb, (kb0 + i) * AB_K, (int)t0);   // rows >= M read 0
+      tma_load_2d(sb + s * AB_STAGE + AB_X_BYTES, &tmap_w, fb, (kb0 + i) * AB_K, 0);
     }
+    // copies still in flight land before the CTA may exit
+    for (int h = i > AB_ST ? i - AB_ST : 0; h < i; ++h)
+      mbar_wait(bar_full + 8 * (h % AB_ST), (uint32_t)(h / AB_ST) & 1, status, DEV_TIMEOUT_TMA);
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_f16_f32(AB_T, 64);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % AB_ST;
+      // one descriptor per operand and stage; the four K slices are constant offsets of its
+      // address field (32 bytes each)
+      const uint64_t ad = sdesc_k_sw128(sb + s * AB_STAGE);
+      const uint64_t bd = sdesc_k_sw128(sb + s * AB_STAGE + AB_X_BYTES);
+      if (!mbar_wait(bar_full + 8 * s, (uint32_t)(i / AB_ST) & 1, status, DEV_TIMEOUT_MMA)) break;
+      tc_fence_after();
+      tc_mma_f16_ss(tmem, ad, bd, idesc, i != 0);
+      tc_mma_f16_ss(tmem, ad + 2, bd + 2, idesc, 1);
+      tc_mma_f16_ss(tmem, ad + 4, bd + 4, idesc, 1);
+      tc_mma_f16_ss(tmem, ad + 6, bd + 6, idesc, 1);
+      tc_commit(bar_empty + 8 * s);
+    }
+    // arrives once every MMA issued above has completed (also after a timed-out wait)
+    tc_commit(bar_done);
   }
-  cp_async_wait<0>();
-  const int gq = lane >> 2, tq = lane & 3;
-  // gates of the 32 value heads: columns 0..31 are a, 32..63 are b
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const int64_t tok = t0 + warp * 16 + gq + hf * 8;
-    if (tok >= M) continue;
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int col = n * 8 + 2 * tq;
+  __syncwarp();
+  if (mbar_wait(bar_done, 0, status, DEV_TIMEOUT_EPILOGUE)) {
+    tc_fence_after();
+    uint32_t ra[32], rb[32];     // columns 0..31 (a) and 32..63 (b) of this thread's token
+    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
+    tmem_ld_32x32b_x32(ta, ra);
+    tmem_ld_32x32b_x32(ta + 32, rb);
+    tc_wait_ld();
+    const int64_t tok = t0 + warp * 32 + lane;
+    if (tok < M) {
       if (gridDim.y == 1) {
-        write_gate(tok, col, acc[n][2 * hf], A_log, dt_bias, g, beta);
-        write_gate(tok, col + 1, acc[n][2 * hf + 1], A_log, dt_bias, g, beta);
+        float4* gp = reinterpret_cast<float4*>(g + tok * 32);
+        float4* bp = reinterpret_cast<float4*>(beta + tok * 32);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          gp[c / 4] = make_float4(gate_g(__uint_as_float(ra[c]), c, A_log, dt_bias),
+                                  gate_g(__uint_as_float(ra[c + 1]), c + 1, A_log, dt_bias),
+                                  gate_g(__uint_as_float(ra[c + 2]), c + 2, A_log, dt_bias),
+                                  gate_g(__uint_as_float(ra[c + 3]), c + 3, A_log, dt_bias));
+          bp[c / 4] = make_float4(sigmoid_f(__uint_as_float(rb[c])), sigmoid_f(__uint_as_float(rb[c + 1])),
+                                  sigmoid_f(__uint_as_float(rb[c + 2])), sigmoid_f(__uint_as_float(rb[c + 3])));
+        }
       } else {
-        *reinterpret_cast<float2*>(part + ((int64_t)blockIdx.y * M + tok) * 64 + col) =
-            make_float2(acc[n][2 * hf], acc[n][2 * hf + 1]);
+        float4* pp = reinterpret_cast<float4*>(part + ((int64_t)blockIdx.y * M + tok) * 64);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          pp[c / 4] = make_float4(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1]),
+                                  __uint_as_float(ra[c + 2]), __uint_as_float(ra[c + 3]));
+          pp[8 + c / 4] = make_float4(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1]),
+                                      __uint_as_float(rb[c + 2]), __uint_as_float(rb[c + 3]));
+        }
       }
     }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
   }
 }
 
@@ -309,10 +365,16 @@ clef_status ab_proj_launch(const __half* xn, const __half* w_ab, const __half* A
   int slices = 1;
   while (slices < kAbMaxSlices && ctas * slices * 2 <= num_sms()) slices *= 2;
   TraceScope ts(stream, "ab_proj", 2.0 * M * 64 * 4096, M * (4096.0 * 2 + 64 * 4) + 64 * 4096 * 2.0);
+  CUtensorMap tx, tw;
+  if (tma_encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xn, (uint64_t)glue::H, (uint64_t)M,
+                    (uint64_t)glue::H * 2, glue::AB_K, glue::AB_T, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess ||
+      tma_encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w_ab, (uint64_t)glue::H, 64,
+                    (uint64_t)glue::H * 2, glue::AB_K, 64, CU_TENSOR_MAP_SWIZZLE_128B) != cudaSuccess)
+    return CLEF_E_CUDA;
   static std::atomic<uint64_t> attr{0};
-  CLEF_CUDA_CHECK(smem_opt_in((const void*)glue::ab_proj_kernel, sizeof(glue::AbSmem), &attr));
-  CLEF_CUDA_CHECK(launch_pdl(glue::ab_proj_kernel, dim3(dim3((unsigned)ctas, (unsigned)slices)), dim3(128), sizeof(glue::AbSmem), stream,
-       xn, w_ab, A_log, dt_bias, g, beta, part, M));
+  CLEF_CUDA_CHECK(smem_opt_in((const void*)glue::ab_proj_kernel, glue::AB_SMEM, &attr));
+  CLEF_CUDA_CHECK(launch_pdl(glue::ab_proj_kernel, dim3((unsigned)ctas, (unsigned)slices), dim3(128), glue::AB_SMEM, stream,
+       tx, tw, A_log, dt_bias, g, beta, part, M, status_word_ptr()));
   if (slices > 1) {
     CLEF_CUDA_CHECK(launch_pdl(glue::ab_gates_kernel, dim3((unsigned)((M * 64 + 255) / 256)), dim3(256), 0, stream,
          part, slices, A_log,

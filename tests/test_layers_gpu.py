@@ -41,8 +41,10 @@ def run_layer(layer_index, L, B=1, seed=0):
         assert e_delta < DELTA_TOL
 
 
-# (4096, 1): the scan runs in pieces on two streams, with the z-gated norm per piece
-@pytest.mark.parametrize("L,B", [(1024, 1), (70, 2), (4096, 1)])
+# (4096, 1): the scan runs in pieces on two streams, with the z-gated norm per piece;
+# (9856, 1): 77 token tiles of 128, so the a/b projection runs without a K split and writes the
+# gates from its own epilogue (shorter inputs split K and sum the parts in a second kernel)
+@pytest.mark.parametrize("L,B", [(1024, 1), (70, 2), (4096, 1), (9856, 1)])
 def test_gdn_layer(L, B):
     run_layer(0, L, B)
 
