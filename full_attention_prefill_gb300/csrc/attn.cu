@@ -35,12 +35,16 @@ struct RopeFreq {
   double f[32];
 };
 
-__global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qin, int64_t ldqi,
-                                                   __half* __restrict__ qout, int64_t ldqo,
-                                                   const __half* __restrict__ kin, int64_t ldki,
-                                                   __half* __restrict__ kout, int64_t ldko, int L,
-                                                   int pos0, int64_t kctx, int mstart, int mh,
-                                                   int mw, const __grid_constant__ RopeFreq fr) {
+// One CTA (96 threads) per token.  Thread i < 80 owns head i / 4 (q heads 0..15, then the 4 k
+// heads) and the rotated pairs j = 8 (i mod 4) .. + 7: it loads dims j .. j + 7 and j + 32 ..
+// j + 39 of its head (two 16-byte loads) before the angles are formed, so the loads are in
+// flight meanwhile; the first warp forms the token's 32 angles.
+__global__ void __launch_bounds__(96) rope_kernel(const __half* __restrict__ qin, int64_t ldqi,
+                                                  __half* __restrict__ qout, int64_t ldqo,
+                                                  const __half* __restrict__ kin, int64_t ldki,
+                                                  __half* __restrict__ kout, int64_t ldko, int L,
+                                                  int pos0, int64_t kctx, int mstart, int mh,
+                                                  int mw, const __grid_constant__ RopeFreq fr) {
   pdl_trigger();
   pdl_wait();
   __shared__ float cs[32], sn[32];
@@ -50,6 +54,21 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
   // k goes to row (request * kctx + idx) of kout (kctx = L, pos0 = 0: the token's own row)
   const int64_t krow = (tok / L) * kctx + idx;
   const int tid = threadIdx.x;
+  const int head = tid / 4, j0 = (tid % 4) * 8;
+  uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+  __half* dst = nullptr;
+  if (tid < 4 * (HQ + HKV)) {
+    const __half* src;
+    if (head < HQ) {
+      src = qin + tok * ldqi + head * D;
+      dst = qout + tok * ldqo + head * D;
+    } else {
+      src = kin + tok * ldki + (head - HQ) * D;
+      dst = kout + krow * ldko + (head - HQ) * D;
+    }
+    lo = *reinterpret_cast<const uint4*>(src + j0);
+    hi = *reinterpret_cast<const uint4*>(src + j0 + 32);
+  }
   if (tid < 32) {
     // M-RoPE planes of this token (all equal to idx for text)
     const int n = mh * mw;
@@ -82,21 +101,20 @@ __global__ void __launch_bounds__(128) rope_kernel(const __half* __restrict__ qi
   }
   __syncthreads();
   const bool copy_q = qout != qin, copy_k = kout != kin;
-  // rotated dims: (head, j) pairs
-  for (int i = tid; i < (HQ + HKV) * 32; i += blockDim.x) {
-    const int head = i / 32, j = i % 32;
-    const __half* src;
-    __half* dst;
-    if (head < HQ) {
-      src = qin + tok * ldqi + head * D;
-      dst = qout + tok * ldqo + head * D;
-    } else {
-      src = kin + tok * ldki + (head - HQ) * D;
-      dst = kout + krow * ldko + (head - HQ) * D;
+  if (dst) {
+    // pairs (j, j + 32) of this thread: x1 from `lo`, x2 from `hi`
+    const __half2* l2 = reinterpret_cast<const __half2*>(&lo);
+    const __half2* h2 = reinterpret_cast<const __half2*>(&hi);
+    uint32_t ol[4], oh[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 x1 = __half22float2(l2[p]), x2 = __half22float2(h2[p]);
+      const int j = j0 + 2 * p;
+      ol[p] = pack_half2(x1.x * cs[j] - x2.x * sn[j], x1.y * cs[j + 1] - x2.y * sn[j + 1]);
+      oh[p] = pack_half2(x2.x * cs[j] + x1.x * sn[j], x2.y * cs[j + 1] + x1.y * sn[j + 1]);
     }
-    const float x1 = __half2float(src[j]), x2 = __half2float(src[j + 32]);
-    dst[j] = __float2half_rn(x1 * cs[j] - x2 * sn[j]);
-    dst[j + 32] = __float2half_rn(x2 * cs[j] + x1 * sn[j]);
+    *reinterpret_cast<uint4*>(dst + j0) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+    *reinterpret_cast<uint4*>(dst + j0 + 32) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
   }
   // pass-through dims 64..255 when writing a copy
   if (copy_q) {
@@ -527,8 +545,13 @@ clef_status rope_launch(const __half* qin, int64_t ldqi, __half* qout, int64_t l
     for (int j = 0; j < 32; ++j) f.f[j] = std::exp(-(double)j * (std::log(1e7) / 32.0));
     return f;
   }();
+  // rows are read and written with 16-byte accesses
+  const auto mis = [](const void* p, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(p) & 15) != 0 || (ld & 7) != 0;
+  };
+  if (mis(qin, ldqi) || mis(qout, ldqo) || mis(kin, ldki) || mis(kout, ldko)) return CLEF_E_ALIGN;
   TraceScope ts(stream, "rope", 0.0, M * (20.0 * 64 * 2 * 2));
-  CLEF_CUDA_CHECK(launch_pdl(attn::rope_kernel, dim3((unsigned)M), dim3(128), 0, stream,
+  CLEF_CUDA_CHECK(launch_pdl(attn::rope_kernel, dim3((unsigned)M), dim3(96), 0, stream,
        qin, ldqi, qout, ldqo, kin, ldki, kout, ldko,
        (int)L, (int)pos0, kctx, (int)mr.start,
        (int)mr.h, (int)mr.w, fr));
